@@ -1,0 +1,419 @@
+"""Benchmark of the KV retention hot path on GB300.
+
+One step = one pass of the whole path on one session:
+  IntentKV token step (8B-shaped: L36 Hq32 Hkv8 D128, N=32768 tokens, bf16 K in
+  16-slot shuffled pages): QueryMemory update with the turn's 256 query rows,
+  rule scores over all candidates, top-C* retention (C=8192), dead-slot redirect;
+  KVMEM block step (1M-token workspace: L64 Hq40 Hkv8 D128, 32768 Mean-K blocks):
+  incremental Mean-K build of 4096 new tokens, R_b over all candidate blocks for
+  2048 query tokens, sink 4 + recent 128 + top-2048 working set, re-RoPE scatter
+  of the 65,536 staged tokens into a shuffled page pool.
+
+Metric: KV rows scored per second = (L*Hkv*|H| token rows + L*Hkv*|C| index
+rows) per step / step time.  With --gpus N (torchrun, one rank per GPU) every
+rank runs its own session (replicas, weak scaling, no collective on the data
+path); the value is the rows of all ranks over the slowest rank's time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+TOKEN_WL = "8b"
+BLOCK_WL = "ws1m"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "src": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+def workload_rows(tw, bw):
+    token_rows = tw.L * tw.Hkv * tw.n_cand
+    block_rows = bw.L * bw.Hkv * bw.n_cand
+    return token_rows, block_rows
+
+
+def config_dict(tw, bw, n):
+    return {"workload": f"IntentKV token step [{tw.name}] + KVMEM block step [{bw.name}]",
+            "token": {"L": tw.L, "Hq": tw.Hq, "Hkv": tw.Hkv, "D": tw.D, "N": tw.N, "C": tw.C, "pi": tw.pi,
+                      "span": tw.span, "page": tw.page, "query_rows": tw.R},
+            "block": {"L": bw.L, "Hq": bw.Hq, "Hkv": bw.Hkv, "D": bw.D, "blocks": bw.n_blocks, "block": bw.block,
+                      "M": bw.M, "sink": bw.n_sink, "recent": bw.n_recent, "k": bw.k, "new_tokens": bw.new_tokens,
+                      "staged_tokens": min(bw.k, bw.n_cand) * bw.block},
+            "l2": "inputs larger than L2 (K pool 2.4 GB, index 4.3 GB, staging 8.6 GB); no flush",
+            "parallelism": f"replicas x{n} (independent sessions, no collective)"}
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"kvsel_clocks_{os.getpid()}_{gpu_index}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for name, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(name)
+            os.unlink(self.path)
+        except Exception:
+            pass
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def setup_session(kv, synth, ctx, tw, bw, torch):
+    """Device-resident state and per-step inputs of one session."""
+    t = synth.token_inputs(tw, "cuda")
+    b = synth.block_inputs(bw, "cuda")
+    s = {"tw": tw, "bw": bw, "pool": t["pool"], "slot_map": t["slot_map"], "turns": t["turns"],
+         "q_last": t["turns"][tw.turns - 1].contiguous(),
+         "M": torch.zeros((tw.L, tw.Hq, tw.D), device="cuda"),
+         "rule": torch.empty(tw.N, device="cuda"),
+         "keep": torch.empty(tw.N, device="cuda", dtype=torch.uint8),
+         "keep_idx": torch.empty(tw.N, device="cuda", dtype=torch.int32),
+         "slot_out": torch.empty(tw.N, device="cuda", dtype=torch.int32),
+         "raw_new": b["raw"], "index": b["index"], "q": b["q"], "staging": b["staging"], "kpool": b["pool"],
+         "R": torch.empty(bw.n_blocks, device="cuda"),
+         "ids": torch.empty(bw.n_sel, device="cuda", dtype=torch.int32)}
+    # the session's earlier turns (state before the timed turn)
+    for i in range(tw.turns - 1):
+        ctx.memory_update(t["turns"][i], tw.lam, s["M"], first_turn=(i == 0))
+    s["src_block"], s["dst_page"], s["dst_pos0"] = synth.scatter_plan_incremental(bw, b["page_perm"])
+    return s
+
+
+# kernel launches per C-ABI call (counted from the launchers in csrc/)
+LAUNCHES = {"memory_update": 1, "rule_scores": 3, "topk_retain": 1, "redirect_slots": 1, "meank_build": 1,
+            "block_scores": 3, "select_blocks": 1, "rerope_scatter": 1}
+
+
+def run_step(ctx, s, ev=None):
+    """One pass of the whole path; ev: optional dict name -> list of (start, end) events."""
+    tw, bw = s["tw"], s["bw"]
+
+    def mark(name, fn):
+        if ev is None:
+            fn()
+            return
+        import torch
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        ev.setdefault(name, []).append((a, b))
+
+    mark("memory_update", lambda: ctx.memory_update(s["q_last"], tw.lam, s["M"]))
+    mark("rule_scores", lambda: ctx.rule_scores(s["pool"], s["M"], tw.L, tw.Hq, tw.Hkv, tw.N, tw.D, tw.pi, tw.q_s,
+                                                tw.q_e, s["rule"], slot_map=s["slot_map"], n_slots=tw.N))
+    mark("topk_retain", lambda: ctx.topk_retain(s["rule"], tw.pi, tw.q_s, tw.q_e, tw.C, keep=s["keep"],
+                                                keep_idx=s["keep_idx"]))
+    mark("redirect_slots", lambda: ctx.redirect_slots(s["slot_map"], s["keep"], tw.dead_slot, s["slot_out"]))
+    mark("meank_build", lambda: ctx.meank_build(s["raw_new"], bw.block, s["index"], first_block=bw.first_new_block))
+    mark("block_scores", lambda: ctx.block_scores(s["q"], s["index"], bw.n_blocks, bw.n_sink, bw.n_recent, s["R"]))
+    mark("select_blocks", lambda: ctx.select_blocks(s["R"], bw.n_sink, bw.n_recent, bw.k, s["ids"]))
+    mark("rerope_scatter", lambda: ctx.rerope_scatter(s["staging"], s["src_block"], s["dst_page"], s["dst_pos0"],
+                                                      s["kpool"], bw.rope_base))
+
+
+def kernel_algorithmic(tw, bw):
+    """Algorithmic bytes (HBM kernels) or flops (tensor kernel) per call."""
+    n_top = min(bw.k, bw.n_cand)
+    return {
+        "rule_scores": ("hbm", tw.L * tw.n_cand * tw.Hkv * tw.D * 2 + tw.N * 4),
+        "memory_update": ("hbm", tw.L * tw.Hq * tw.R * tw.D * 2 + 2 * tw.L * tw.Hq * tw.D * 4),
+        "meank_build": ("hbm", bw.L * bw.Hkv * bw.new_tokens * bw.D * 2 + bw.L * bw.Hkv * (bw.new_tokens // bw.block) * bw.D * 2),
+        "rerope_scatter": ("hbm", 2 * bw.L * bw.Hkv * n_top * bw.block * bw.D * 2),
+        "block_scores": ("tensor", 2 * bw.L * bw.Hq * bw.M * bw.n_cand * bw.D),
+    }
+
+
+def ours(args, rank, world, local_rank):
+    import torch
+
+    import kv_cache_retention_gb300 as kv
+    from kv_cache_retention_gb300 import synth
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    tw, bw = synth.TOKEN[TOKEN_WL], synth.BLOCK[BLOCK_WL]
+    ctx = kv.Context(local_rank)
+    s = setup_session(kv, synth, ctx, tw, bw, torch)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        run_step(ctx, s)
+    ctx.check_device()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = {}
+    start.record()
+    for _ in range(args.steps):
+        run_step(ctx, s, ev)
+    end.record()
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms_total = start.elapsed_time(end)
+    ms_t = torch.tensor([ms_total], device="cuda")
+    if dist is not None:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    per_call = {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in ev.items()}
+    ctx.check_device()
+
+    # end-to-end: fresh per-step inputs from pinned host memory, results back to the host
+    h_in = {k: s[k].detach().cpu().pin_memory() for k in ("q_last", "raw_new", "q", "staging")}
+    h_out = {k: torch.empty_like(s[k], device="cpu").pin_memory() for k in ("rule", "slot_out", "keep_idx", "R", "ids")}
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+
+    def e2e_step():
+        for k, t in h_in.items():
+            s[k].copy_(t, non_blocking=True)
+        run_step(ctx, s)
+        for k, t in h_out.items():
+            t.copy_(s[k], non_blocking=True)
+
+    e2e_steps = max(1, args.steps)
+    for _ in range(max(1, min(args.warmup, 2))):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e_end.record()
+    torch.cuda.synchronize()
+    barrier()
+    e_ms = torch.tensor([e_start.elapsed_time(e_end)], device="cuda")
+    if dist is not None:
+        dist.all_reduce(e_ms, op=dist.ReduceOp.MAX)
+
+    token_rows, block_rows = workload_rows(tw, bw)
+    rows_step = token_rows + block_rows
+    value = world * rows_step * args.steps / (ms_max / 1e3)
+    e2e_value = world * rows_step * e2e_steps / (float(e_ms.item()) / 1e3)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    peaks = _peaks()
+    alg = kernel_algorithmic(tw, bw)
+    kernels = {}
+    for name, (bound, amount) in alg.items():
+        ms = per_call.get(name)
+        if not ms:
+            continue
+        if bound == "hbm":
+            ach = amount / (ms / 1e3) / 1e9
+            kernels[name] = {"bound": "hbm", "ms": ms, "achieved": ach, "unit": "GB/s", "peak": peaks["hbm_gbs"],
+                             "frac": ach / peaks["hbm_gbs"], "algorithmic_bytes": amount}
+        else:
+            ach = amount / (ms / 1e3) / 1e12
+            kernels[name] = {"bound": "tensor", "ms": ms, "achieved": ach, "unit": "TFLOP/s",
+                             "peak": peaks["bf16_tflops_sustained"], "frac": ach / peaks["bf16_tflops_sustained"],
+                             "algorithmic_flops": amount}
+    for name in ("topk_retain", "redirect_slots", "select_blocks"):
+        if name in per_call:
+            kernels[name] = {"bound": "latency", "ms": per_call[name]}
+    dom = max((k for k in kernels if "achieved" in kernels[k]), key=lambda k: kernels[k]["ms"])
+    d = kernels[dom]
+    traffic = _profiled_traffic(dom)
+    roofline = {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"], "unit": d["unit"],
+                "frac": d["frac"], "traffic": traffic,
+                "peak_src": f"{peaks['src']} ({'bf16_tflops_sustained' if d['bound'] == 'tensor' else 'hbm_gbs'})"}
+    cpu = cpu_baseline(args, tw, bw) if not args.no_cpu_baseline else None
+    line = {
+        "metric": "KV rows scored/s", "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "us_per_select_step": 1e3 * ms_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; shapes of the pages' workloads)", "config": config_dict(tw, bw, world),
+        "rows_per_step": {"token": token_rows, "block": block_rows},
+        "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": float(e_ms.item()) / e2e_steps,
+                "inputs": "per-step query rows, new raw K and staged top-block K from pinned host; "
+                          "K pool and Mean-K index resident on the device"},
+        "gpu_launches": sum(LAUNCHES.values()) * args.steps,
+        "roofline": roofline, "kernels": kernels, "clocks": clk, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def _profiled_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        e = t.get(kernel)
+        return e["dram_bytes_per_call"] if e and e.get("current") else None
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline / reference arm: the fp64 oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_sample(tw, bw, budget_layers=2, block_queries=256):
+    """Time the oracle on a bounded sample of the step; return (sec_per_full_step_estimate, description).
+
+    Token part: the whole IntentKV step restricted to `budget_layers` layers.
+    Block part: the R_b mass of one (layer, kv head) with `block_queries`
+    query tokens per head, plus Mean-K of one (layer, kv head) of the new tokens.
+    Each part's time is scaled by its share of the full step's work."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from kv_cache_retention_gb300 import synth
+
+    oracle.build()
+    tws = synth.scaled(tw, L=budget_layers)
+    ti = synth.token_inputs(tws, "cpu")
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    t0 = time.perf_counter()
+    M, _ = oracle.memory_update(bits(ti["turns"][-1]), tws.lam, first_turn=True)
+    rule = oracle.rule_scores(bits(ti["pool"]).ravel(), M, tws.L, tws.Hq, tws.Hkv, tws.N, tws.D, tws.pi, tws.q_s,
+                              tws.q_e, slot_map=ti["slot_map"].numpy())
+    keep, _ = oracle.topk_retain(rule, tws.pi, tws.q_s, tws.q_e, tws.C)
+    oracle.redirect_slots(ti["slot_map"].numpy(), keep, tws.dead_slot)
+    t_tok = time.perf_counter() - t0
+    bws = synth.scaled(bw, L=1, Hkv=1, Hq=bw.Hq // bw.Hkv, M=block_queries, new_tokens=bw.new_tokens)
+    gen = torch.Generator().manual_seed(bw.seed)
+    q = torch.randn((1, bws.Hq, block_queries, bw.D), generator=gen).to(torch.bfloat16)
+    ix = (torch.randn((1, 1, bw.n_blocks, bw.D), generator=gen) * 0.5).to(torch.bfloat16)
+    raw = torch.randn((1, 1, bw.new_tokens, bw.D), generator=gen).to(torch.bfloat16)
+    t0 = time.perf_counter()
+    oracle.meank_build(bits(raw), bw.block, Bcap=bw.new_tokens // bw.block)
+    oracle.block_mass(bits(q), bits(ix), bw.n_blocks, bw.n_sink, bw.n_recent, 0, 0)
+    t_blk = time.perf_counter() - t0
+    est = t_tok * (tw.L / budget_layers) + t_blk * (bw.L * bw.Hkv) * (bw.M / block_queries)
+    desc = (f"oracle, 1 thread: token step on {budget_layers} of {tw.L} layers ({t_tok:.2f} s) and R_b of 1 of "
+            f"{bw.L * bw.Hkv} (layer, kv head) pairs with {block_queries} of {bw.M} query tokens ({t_blk:.2f} s), "
+            f"scaled by work share to one full step ({est:.1f} s)")
+    return est, desc
+
+
+def cpu_baseline(args, tw, bw):
+    est, desc = oracle_sample(tw, bw)
+    token_rows, block_rows = workload_rows(tw, bw)
+    return {"value": (token_rows + block_rows) / est, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": desc}
+
+
+def reference(args, rank, world):
+    if rank != 0:
+        return
+    from kv_cache_retention_gb300 import synth
+    tw, bw = synth.TOKEN[TOKEN_WL], synth.BLOCK[BLOCK_WL]
+    for _ in range(args.warmup):
+        oracle_sample(tw, bw, budget_layers=1, block_queries=64)
+    ests, desc = [], ""
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        est, desc = oracle_sample(tw, bw, budget_layers=1, block_queries=64)
+        ests.append(est)
+    wall = time.perf_counter() - t0
+    token_rows, block_rows = workload_rows(tw, bw)
+    sec = sum(ests)
+    value = (token_rows + block_rows) * args.steps / sec
+    line = {"impl": "reference", "metric": "KV rows scored/s", "value": value, "unit": "rows/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; shapes of the pages' workloads)", "config": config_dict(tw, bw, world),
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": wall}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus if "RANK" in os.environ else 1)))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        reference(args, rank, world)
+    else:
+        ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

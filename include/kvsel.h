@@ -1,0 +1,229 @@
+/*
+ * kvsel.h: C ABI of libkvsel, query-driven KV-cache retention scoring and
+ * selection on one NVIDIA GB300 GPU (sm_103a).
+ *
+ * Two methods share the library:
+ *   IntentKV  ("IntentKV: cross-turn intent-aware KV cache pruning for agent
+ *             reasoning"): QueryMemory (Sec. 3.2, Eq. 2), rule scores
+ *             (Sec. 3.2, Eq. 3-4), budgeted top-C* retention with a forced set
+ *             (Sec. 3.1, Eq. 1) and the dead-slot redirect of the layout layer
+ *             (abstract; Sec. 3 overview).
+ *   KVMEM     ("KVMEM: virtualising million-token agent workspaces onto one
+ *             laptop GPU"): the Mean-K block index, the block relevance R_b and
+ *             the sink + recent + top-R_b working set (section "design and
+ *             trade-offs: step-level attention trigger and Mean-K model-native
+ *             retrieval"), and the position-consistent restore that re-applies
+ *             RoPE to raw K at new compact positions (section "engineering:
+ *             tiered movement, page-table aliasing and position-consistent
+ *             rebuild").
+ *
+ * Conventions shared by every call
+ *   - Tensor pointers are DEVICE pointers on the context's device, owned by
+ *     the caller; the library never frees or keeps them.  Arguments named
+ *     *_host are host pointers.
+ *   - Layouts are row-major with the innermost (head-dim) axis contiguous.
+ *     bf16 tensors are passed as void* holding IEEE bfloat16 values.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream) and never synchronises the host.
+ *   - Every call returns a kvsel_status.  Arguments are validated on the host
+ *     before anything is launched; on an error nothing is launched, nothing is
+ *     written, and kvsel_last_error_string() says why.  Calls never throw.
+ *   - A context is not thread-safe: use one context per host thread, and do
+ *     not let calls on one context overlap on different streams (they share
+ *     the context's scratch workspace).
+ *   - Scratch: calls that need temporary device memory take it from the
+ *     context's workspace, which grows on first use at a larger size
+ *     (cudaMalloc, synchronous).  Make one call at the largest size before
+ *     capturing calls into a CUDA graph.
+ */
+#ifndef KVSEL_H_
+#define KVSEL_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct kvsel_ctx kvsel_ctx;
+
+typedef enum {
+    KVSEL_OK = 0,
+    KVSEL_ERR_INVALID_ARG = -1, /* null pointer, negative size, bad enum     */
+    KVSEL_ERR_SHAPE = -2,       /* inconsistent sizes or ranges               */
+    KVSEL_ERR_ALIGN = -3,       /* pointer or stride breaks 16-byte alignment */
+    KVSEL_ERR_UNSUPPORTED = -4, /* valid but not supported (e.g. head dim)    */
+    KVSEL_ERR_CUDA = -5,        /* a CUDA runtime call failed                 */
+    KVSEL_ERR_TIMEOUT = -6,     /* a bounded device wait gave up              */
+    KVSEL_ERR_DEVICE_CHECK = -7 /* a kernel found bad data (see below)        */
+} kvsel_status;
+
+typedef enum { KVSEL_F32 = 0, KVSEL_BF16 = 1 } kvsel_dtype;
+
+/* RoPE pairing: NeoX / rotate-half pairs (i, i + D/2); interleaved (2i, 2i+1). */
+typedef enum { KVSEL_ROPE_NEOX = 0, KVSEL_ROPE_INTERLEAVED = 1 } kvsel_rope_style;
+
+/* ------------------------------------------------------------------------ */
+/* context                                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Create a context on CUDA device `device` (made current for the call). */
+int kvsel_ctx_create(int device, kvsel_ctx** out);
+/* Free the context's workspace and tables; waits for the device. NULL is ok. */
+int kvsel_ctx_destroy(kvsel_ctx* ctx);
+/* Detail of the last error on this context ("" if none); valid until the next call. */
+const char* kvsel_last_error_string(const kvsel_ctx* ctx);
+/* Synchronise `stream`, then read and clear the device error word that kernels
+ * set when they meet bad data (a slot, block id or position out of range):
+ * returns KVSEL_OK or KVSEL_ERR_DEVICE_CHECK. */
+int kvsel_check_device(kvsel_ctx* ctx, void* stream);
+/* Library version, major * 10000 + minor * 100 + patch. */
+int kvsel_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* IntentKV                                                                  */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * QueryMemory update for one turn (IntentKV Sec. 3.2, Eq. 2):
+ *   E[l,h,:] = (1/R) sum_r q_rows[l,h,r,:]   (the actionable span's post-RoPE
+ *                                             query rows; Enc = their mean)
+ *   norm_mode 0: M <- normalise(e^-lambda * M + E)          (state = M)
+ *   norm_mode 1: A <- e^-lambda * A + E;  M <- normalise(A) (state = A)
+ * normalise() divides each (l,h) vector by its L2 norm over D; a zero vector
+ * stays zero.  first_turn != 0 treats the previous state as zero.
+ *   q_rows  [L][Hq][R][D], q_dtype F32 or BF16, 16-byte aligned
+ *   M       [L][Hq][D] fp32, in/out (mode 0) or out (mode 1)
+ *   A       [L][Hq][D] fp32 in/out, mode 1 only (NULL in mode 0)
+ * Requires R >= 1, D % 8 == 0 (BF16) or D % 4 == 0 (F32), D <= 1024.
+ */
+int kvsel_memory_update(kvsel_ctx* ctx, const void* q_rows, int q_dtype, int L, int Hq, int R,
+                        int D, float lambda, int first_turn, int norm_mode, float* M, float* A,
+                        void* stream);
+
+/*
+ * Rule scores (IntentKV Sec. 3.2, Eq. 3-4):
+ *   rule[j] = sum_{l<L, h<Hq} softmax_{i in H}( M[l,h] . K[l,g(h),i] / sqrt(D) )_j
+ * for j in H = [0,N) \ F, F = [0,pi) U [q_s,q_e); rule[j] = 0 for j in F, and
+ * no position of F enters a denominator.  g(h) = h / (Hq/Hkv).
+ * K is read in place from a paged pool: the row of token j, kv head g, layer l
+ * starts at element  l*layer_stride + slot(j)*slot_stride + g*D  of k_pool,
+ * slot(j) = slot_map[j] (slot_map == NULL: slot(j) = j).  Rows of a slot hold
+ * the Hkv heads back to back.
+ *   k_pool   k_dtype F32 or BF16; base, layer_stride and slot_stride 16-byte
+ *            aligned in bytes
+ *   slot_map int32 [N] or NULL; slots of candidate positions must lie in
+ *            [0, n_slots) (a slot outside is read as a zero row and sets the
+ *            device error word, see kvsel_check_device)
+ *   n_slots  rows per layer in the pool (>= N when slot_map == NULL)
+ *   M        [L][Hq][D] fp32 (normalised QueryMemory)
+ *   rule     [N] fp32 out
+ * Requires Hq % Hkv == 0, Hq/Hkv <= 8, D in {16,32,64,128,256},
+ * 0 <= pi <= N, 0 <= q_s <= q_e <= N.  Uses workspace: 4*L*Hq*N bytes + a little.
+ */
+int kvsel_rule_scores(kvsel_ctx* ctx, const void* k_pool, int k_dtype, const int32_t* slot_map,
+                      int n_slots, int L, int Hq, int Hkv, int N, int D, int64_t layer_stride,
+                      int64_t slot_stride, const float* M, int pi, int q_s, int q_e, float* rule,
+                      void* stream);
+
+/*
+ * Budgeted retention (IntentKV Sec. 3.1, Eq. 1):
+ *   K* = F U (the C* largest scores of H),  C* = max(0, C - |F|)
+ * Ties between equal scores go to the lower index; NaN ranks below every
+ * number; -0 equals +0.  If N <= C every position is kept.
+ *   score     [N] fp32
+ *   keep      [N] uint8 out (1 = kept) or NULL
+ *   keep_idx  [|K*|] int32 out, kept positions ascending, or NULL
+ *   n_keep_host  host out: |K*| = |F| + min(C*, |H|) (closed form, no sync)
+ */
+int kvsel_topk_retain(kvsel_ctx* ctx, const float* score, int N, int pi, int q_s, int q_e,
+                      int C, uint8_t* keep, int32_t* keep_idx, int* n_keep_host, void* stream);
+
+/*
+ * Dead-slot redirect (IntentKV abstract; Sec. 3 overview, layout layer):
+ *   slot_out[j] = keep[j] ? slot_in[j] : dead_slot
+ * Kept rows never move.  slot_out may alias slot_in.  Int32 [N], uint8 [N].
+ */
+int kvsel_redirect_slots(kvsel_ctx* ctx, const int32_t* slot_in, const uint8_t* keep, int N,
+                         int32_t dead_slot, int32_t* slot_out, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* KVMEM                                                                     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Mean-K index build (KVMEM retrieval index):
+ *   index[l,g,first_block+b,:] = bf16( mean over tokens i of block b of Ktilde[l,g,i,:] )
+ * Block b covers tokens [b*block, min((b+1)*block, T)) of k_src (a short last
+ * block averages the tokens it has).  Ktilde = k_src when src_pos == NULL (raw,
+ * position-free K), else k_src with the rotation of position src_pos[i]
+ * removed (rope_base, rope_style).  Accumulation is fp32, the store rounds to
+ * nearest even.  Index blocks outside [first_block, first_block + ceil(T/block))
+ * are not touched.
+ *   k_src   bf16 [L][Hkv][T][D], 16-byte aligned
+ *   src_pos int32 [T] or NULL; positions in [0, 2^24)
+ *   index   bf16 [L][Hkv][Bcap][D]
+ * Requires D in {16,32,64,128,256}, block >= 1, first_block + ceil(T/block) <= Bcap.
+ */
+int kvsel_meank_build(kvsel_ctx* ctx, const void* k_src, int L, int Hkv, int T, int D, int block,
+                      int first_block, const int32_t* src_pos, double rope_base, int rope_style,
+                      void* index, int Bcap, void* stream);
+
+/*
+ * Block relevance (KVMEM retrieval):
+ *   R[b] = 1/(L*Hq) * sum_{l,h,m} softmax_{b' in C}( q[l,h,m] . index[l,g(h),b'] / sqrt(D) )_b
+ * C = [n_sink, n_blocks - n_recent): sink and recent blocks are always kept
+ * and take no part in the softmax; R[b] = 0 outside C (and everywhere if C is
+ * empty).  q holds position-free (pre-RoPE) query rows.
+ *   q          bf16 [L][Hq][M][D]
+ *   index      bf16 [L][Hkv][Bcap][D]
+ *   R          [n_blocks] fp32 out
+ *   R_partial  [L*Hkv][n_blocks] fp32 out or NULL: the unnormalised mass of
+ *              each (l, g), sum over its Hq/Hkv heads and M query tokens
+ * The dot products run on the tensor cores (bf16 in, fp32 accumulate), the
+ * softmax in fp32.  Requires D == 128, Hq % Hkv == 0, n_blocks <= Bcap,
+ * 16-byte aligned q and index.  Uses workspace: 4*L*Hq*M + 4*L*Hkv*n_blocks bytes.
+ */
+int kvsel_block_scores(kvsel_ctx* ctx, const void* q, const void* index, int L, int Hq, int Hkv,
+                       int M, int D, int n_blocks, int Bcap, int n_sink, int n_recent, float* R,
+                       float* R_partial, void* stream);
+
+/*
+ * Working set (KVMEM retrieval):
+ *   W = [0, n_sink) U [n_blocks - n_recent, n_blocks) U (the k largest R over C)
+ * ties to the lower block id; ids ascending.  This is Eq. 1's selection with
+ * the sink and recent blocks as the forced set.
+ *   R         [n_blocks] fp32
+ *   ids       [|W|] int32 out
+ *   n_sel_host host out: |W| = |sink U recent| + min(k, |C|)
+ */
+int kvsel_select_blocks(kvsel_ctx* ctx, const float* R, int n_blocks, int n_sink, int n_recent,
+                        int k, int32_t* ids, int* n_sel_host, void* stream);
+
+/*
+ * Position-consistent restore (KVMEM, re-RoPE scatter): for entry i < n,
+ * token t < page, layer l, kv head g, the raw position-free row
+ *   k_src[l*src_layer_stride + g*src_head_stride + (src_block[i]*page + t)*D + :]
+ * is rotated to position dst_pos0[i] + t and stored (bf16, nearest even) at
+ *   pool[l][dst_page[i]][t][g][:]
+ * Pool pages not named in dst_page are not touched; entries should name
+ * distinct pages.
+ *   k_src  bf16; strides in elements, 16-byte aligned in bytes; each head row
+ *          holds src_tokens tokens
+ *   src_block, dst_page, dst_pos0  int32 [n]; (src_block+1)*page <= src_tokens,
+ *          dst_page < P, positions in [0, 2^24).  An entry breaking these is
+ *          skipped and sets the device error word.
+ *   pool   bf16 [L][P][page][Hkv][D]
+ * Requires D in {16,32,64,128,256}.
+ */
+int kvsel_rerope_scatter(kvsel_ctx* ctx, const void* k_src, int64_t src_layer_stride,
+                         int64_t src_head_stride, int src_tokens, const int32_t* src_block,
+                         const int32_t* dst_page, const int32_t* dst_pos0, int n, int L, int Hkv,
+                         int D, int page, double rope_base, int rope_style, void* pool, int P,
+                         void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVSEL_H_ */

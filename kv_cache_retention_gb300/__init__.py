@@ -1,0 +1,288 @@
+"""kv_cache_retention_gb300: Python binding of libkvsel, the GB300 library for
+query-driven KV-cache retention scoring and selection (IntentKV rule scoring
+with dead-slot redirect; KVMEM Mean-K block retrieval with re-RoPE restore).
+
+The binding only marshals arguments: every step runs in the CUDA kernels of
+``libkvsel.so`` (built in-tree by ``_build.build()``).  Importing this package
+fails loudly when the library is missing; there is no fallback.
+
+Two layers:
+  * module functions ``kvsel_*`` with exactly the C signatures (raw pointers
+    as ints, sizes, stream handle) from ``include/kvsel.h``;
+  * ``Context``: the same calls taking torch tensors, checking dtype, device
+    and contiguity, and passing ``data_ptr()`` plus the current CUDA stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+_LIB_PATH = _build.LIB
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_SHAPE = -2
+ERR_ALIGN = -3
+ERR_UNSUPPORTED = -4
+ERR_CUDA = -5
+ERR_TIMEOUT = -6
+ERR_DEVICE_CHECK = -7
+
+F32 = 0
+BF16 = 1
+ROPE_NEOX = 0
+ROPE_INTERLEAVED = 1
+
+# name -> (restype, argtypes), mirroring include/kvsel.h
+_P, _I, _I64, _F, _D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_double
+_IP = ctypes.POINTER(ctypes.c_int)
+SIGNATURES = {
+    "kvsel_version": (_I, []),
+    "kvsel_ctx_create": (_I, [_I, ctypes.POINTER(_P)]),
+    "kvsel_ctx_destroy": (_I, [_P]),
+    "kvsel_last_error_string": (ctypes.c_char_p, [_P]),
+    "kvsel_check_device": (_I, [_P, _P]),
+    "kvsel_memory_update": (_I, [_P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P]),
+    "kvsel_rule_scores": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I64, _I64, _P, _I, _I, _I, _P, _P]),
+    "kvsel_topk_retain": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _IP, _P]),
+    "kvsel_redirect_slots": (_I, [_P, _P, _P, _I, ctypes.c_int32, _P, _P]),
+    "kvsel_meank_build": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _D, _I, _P, _I, _P]),
+    "kvsel_block_scores": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "kvsel_select_blocks": (_I, [_P, _P, _I, _I, _I, _I, _P, _IP, _P]),
+    "kvsel_rerope_scatter": (_I, [_P, _P, _I64, _I64, _I, _P, _P, _P, _I, _I, _I, _I, _I, _D, _I, _P, _I, _P]),
+}
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            f"libkvsel.so not found at {_LIB_PATH}: build it first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(_LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+LIB_PATH = _LIB_PATH
+
+
+class KvselError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"kvsel error {code}: {msg}")
+        self.code = code
+
+
+# ---------------------------------------------------------------------------
+# raw C-ABI functions (same names and argument order as include/kvsel.h)
+# ---------------------------------------------------------------------------
+
+def kvsel_version() -> int:
+    return _lib.kvsel_version()
+
+
+def kvsel_ctx_create(device: int) -> int:
+    h = _P()
+    rc = _lib.kvsel_ctx_create(device, ctypes.byref(h))
+    if rc != OK:
+        raise KvselError(rc, f"kvsel_ctx_create(device={device}) failed")
+    return h.value
+
+
+def kvsel_ctx_destroy(ctx: int) -> int:
+    return _lib.kvsel_ctx_destroy(ctx)
+
+
+def kvsel_last_error_string(ctx: int) -> str:
+    return _lib.kvsel_last_error_string(ctx).decode()
+
+
+def kvsel_check_device(ctx, stream):
+    return _lib.kvsel_check_device(ctx, stream)
+
+
+def kvsel_memory_update(ctx, q_rows, q_dtype, L, Hq, R, D, lam, first_turn, norm_mode, M, A, stream):
+    return _lib.kvsel_memory_update(ctx, q_rows, q_dtype, L, Hq, R, D, lam, first_turn, norm_mode, M, A, stream)
+
+
+def kvsel_rule_scores(ctx, k_pool, k_dtype, slot_map, n_slots, L, Hq, Hkv, N, D, layer_stride, slot_stride, M,
+                      pi, q_s, q_e, rule, stream):
+    return _lib.kvsel_rule_scores(ctx, k_pool, k_dtype, slot_map, n_slots, L, Hq, Hkv, N, D, layer_stride,
+                                  slot_stride, M, pi, q_s, q_e, rule, stream)
+
+
+def kvsel_topk_retain(ctx, score, N, pi, q_s, q_e, C, keep, keep_idx, n_keep_host, stream):
+    return _lib.kvsel_topk_retain(ctx, score, N, pi, q_s, q_e, C, keep, keep_idx, n_keep_host, stream)
+
+
+def kvsel_redirect_slots(ctx, slot_in, keep, N, dead_slot, slot_out, stream):
+    return _lib.kvsel_redirect_slots(ctx, slot_in, keep, N, dead_slot, slot_out, stream)
+
+
+def kvsel_meank_build(ctx, k_src, L, Hkv, T, D, block, first_block, src_pos, rope_base, rope_style, index, Bcap,
+                      stream):
+    return _lib.kvsel_meank_build(ctx, k_src, L, Hkv, T, D, block, first_block, src_pos, rope_base, rope_style,
+                                  index, Bcap, stream)
+
+
+def kvsel_block_scores(ctx, q, index, L, Hq, Hkv, M, D, n_blocks, Bcap, n_sink, n_recent, R, R_partial, stream):
+    return _lib.kvsel_block_scores(ctx, q, index, L, Hq, Hkv, M, D, n_blocks, Bcap, n_sink, n_recent, R, R_partial,
+                                   stream)
+
+
+def kvsel_select_blocks(ctx, R, n_blocks, n_sink, n_recent, k, ids, n_sel_host, stream):
+    return _lib.kvsel_select_blocks(ctx, R, n_blocks, n_sink, n_recent, k, ids, n_sel_host, stream)
+
+
+def kvsel_rerope_scatter(ctx, k_src, src_layer_stride, src_head_stride, src_tokens, src_block, dst_page, dst_pos0,
+                         n, L, Hkv, D, page, rope_base, rope_style, pool, P, stream):
+    return _lib.kvsel_rerope_scatter(ctx, k_src, src_layer_stride, src_head_stride, src_tokens, src_block, dst_page,
+                                     dst_pos0, n, L, Hkv, D, page, rope_base, rope_style, pool, P, stream)
+
+
+# ---------------------------------------------------------------------------
+# tensor-level wrapper
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    """data_ptr of a contiguous CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor (libkvsel has no CPU path)")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return t.data_ptr()
+
+
+def _code(t):
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+class Context:
+    """A libkvsel context on one CUDA device; methods mirror the C calls."""
+
+    def __init__(self, device: int = 0):
+        self.device = device
+        self.handle = kvsel_ctx_create(device)
+
+    def close(self):
+        if self.handle:
+            kvsel_ctx_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _stream(self, stream):
+        if stream is not None:
+            return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        return _torch().cuda.current_stream(self.device).cuda_stream
+
+    def _check(self, rc):
+        if rc != OK:
+            raise KvselError(rc, kvsel_last_error_string(self.handle))
+
+    def check_device(self, stream=None):
+        self._check(kvsel_check_device(self.handle, self._stream(stream)))
+
+    # IntentKV -------------------------------------------------------------
+    def memory_update(self, q_rows, lam, M, first_turn=False, norm_mode=0, A=None, stream=None):
+        torch = _torch()
+        L, Hq, R, D = q_rows.shape
+        self._check(kvsel_memory_update(self.handle, _ptr(q_rows, name="q_rows"), _code(q_rows), L, Hq, R, D,
+                                        float(lam), int(bool(first_turn)), int(norm_mode),
+                                        _ptr(M, torch.float32, "M"), _ptr(A, torch.float32, "A"),
+                                        self._stream(stream)))
+
+    def rule_scores(self, k_pool, M, L, Hq, Hkv, N, D, pi, q_s, q_e, rule, slot_map=None, n_slots=None,
+                    layer_stride=None, slot_stride=None, stream=None):
+        torch = _torch()
+        if slot_stride is None:
+            slot_stride = Hkv * D
+        if n_slots is None:
+            n_slots = k_pool.numel() // (L * slot_stride)
+        if layer_stride is None:
+            layer_stride = n_slots * slot_stride
+        self._check(kvsel_rule_scores(self.handle, _ptr(k_pool, name="k_pool"), _code(k_pool),
+                                      _ptr(slot_map, torch.int32, "slot_map"), int(n_slots), L, Hq, Hkv, N, D,
+                                      int(layer_stride), int(slot_stride), _ptr(M, torch.float32, "M"),
+                                      pi, q_s, q_e, _ptr(rule, torch.float32, "rule"), self._stream(stream)))
+
+    def topk_retain(self, score, pi, q_s, q_e, C, keep=None, keep_idx=None, stream=None):
+        torch = _torch()
+        n = ctypes.c_int(0)
+        self._check(kvsel_topk_retain(self.handle, _ptr(score, torch.float32, "score"), score.numel(), pi, q_s,
+                                      q_e, C, _ptr(keep, torch.uint8, "keep"), _ptr(keep_idx, torch.int32, "keep_idx"),
+                                      ctypes.byref(n), self._stream(stream)))
+        return n.value
+
+    def redirect_slots(self, slot_in, keep, dead_slot, slot_out, stream=None):
+        torch = _torch()
+        self._check(kvsel_redirect_slots(self.handle, _ptr(slot_in, torch.int32, "slot_in"),
+                                         _ptr(keep, torch.uint8, "keep"), slot_in.numel(), int(dead_slot),
+                                         _ptr(slot_out, torch.int32, "slot_out"), self._stream(stream)))
+
+    # KVMEM ----------------------------------------------------------------
+    def meank_build(self, k_src, block, index, first_block=0, src_pos=None, rope_base=1e6, rope_style=ROPE_NEOX,
+                    stream=None):
+        torch = _torch()
+        L, Hkv, T, D = k_src.shape
+        self._check(kvsel_meank_build(self.handle, _ptr(k_src, torch.bfloat16, "k_src"), L, Hkv, T, D, block,
+                                      first_block, _ptr(src_pos, torch.int32, "src_pos"), float(rope_base),
+                                      int(rope_style), _ptr(index, torch.bfloat16, "index"), index.shape[2],
+                                      self._stream(stream)))
+
+    def block_scores(self, q, index, n_blocks, n_sink, n_recent, R, R_partial=None, stream=None):
+        torch = _torch()
+        L, Hq, M, D = q.shape
+        Hkv, Bcap = index.shape[1], index.shape[2]
+        self._check(kvsel_block_scores(self.handle, _ptr(q, torch.bfloat16, "q"), _ptr(index, torch.bfloat16, "index"),
+                                       L, Hq, Hkv, M, D, n_blocks, Bcap, n_sink, n_recent,
+                                       _ptr(R, torch.float32, "R"), _ptr(R_partial, torch.float32, "R_partial"),
+                                       self._stream(stream)))
+
+    def select_blocks(self, R, n_sink, n_recent, k, ids, n_blocks=None, stream=None):
+        torch = _torch()
+        n = ctypes.c_int(0)
+        nb = R.numel() if n_blocks is None else n_blocks
+        self._check(kvsel_select_blocks(self.handle, _ptr(R, torch.float32, "R"), nb, n_sink, n_recent, k,
+                                        _ptr(ids, torch.int32, "ids"), ctypes.byref(n), self._stream(stream)))
+        return n.value
+
+    def rerope_scatter(self, k_src, src_block, dst_page, dst_pos0, pool, rope_base, rope_style=ROPE_NEOX,
+                       n=None, stream=None):
+        """k_src: bf16 [L][Hkv][T][D] (contiguous); pool: bf16 [L][P][page][Hkv][D]."""
+        torch = _torch()
+        L, Hkv, T, D = k_src.shape
+        _, P, page, _, _ = pool.shape
+        n = src_block.numel() if n is None else n
+        self._check(kvsel_rerope_scatter(self.handle, _ptr(k_src, torch.bfloat16, "k_src"), Hkv * T * D, T * D, T,
+                                         _ptr(src_block, torch.int32, "src_block"),
+                                         _ptr(dst_page, torch.int32, "dst_page"),
+                                         _ptr(dst_pos0, torch.int32, "dst_pos0"), n, L, Hkv, D, page,
+                                         float(rope_base), int(rope_style), _ptr(pool, torch.bfloat16, "pool"), P,
+                                         self._stream(stream)))

@@ -1,0 +1,83 @@
+// Internal declarations shared by the libkvsel translation units (not part of
+// the public ABI; see include/kvsel.h for the calls and their contracts).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/kvsel.h"
+
+struct kvsel_ctx {
+    int device = 0;
+    int num_sms = 0;
+    // Scratch workspace; grows on demand (see kvsel.h "Scratch").
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    // Device error word: kernels OR kvsel_devcheck bits into it on bad data.
+    unsigned* dev_err = nullptr;
+    // RoPE angle tables, one per (D, base): split-position cos/sin pairs.
+    struct RopeTab {
+        int D = 0;
+        double base = 0.0;
+        float2* lo = nullptr;  // [KVSEL_ROPE_LO][D/2]: angle lo * theta_i
+        float2* hi = nullptr;  // [KVSEL_ROPE_HI][D/2]: angle hi * LO * theta_i
+    };
+    RopeTab rope[8];
+    int n_rope = 0;
+    char err[512] = {0};
+};
+
+// Device error-word bits.
+enum kvsel_devcheck : unsigned {
+    KVSEL_DEV_BAD_SLOT = 1u << 0,
+    KVSEL_DEV_BAD_POSITION = 1u << 1,
+    KVSEL_DEV_BAD_BLOCK = 1u << 2,
+    KVSEL_DEV_BAD_PAGE = 1u << 3,
+};
+
+// Positions p are split as p = hi * KVSEL_ROPE_LO + lo; both tables in fp64 -> fp32.
+#define KVSEL_ROPE_LO_BITS 10
+#define KVSEL_ROPE_LO (1 << KVSEL_ROPE_LO_BITS)
+#define KVSEL_ROPE_HI (1 << 14)
+#define KVSEL_MAX_POS (KVSEL_ROPE_LO * KVSEL_ROPE_HI)  // 2^24
+
+// Returns a pointer into the context workspace of at least `bytes` (256-byte
+// aligned), growing it if needed; nullptr on allocation failure.
+void* kvsel_workspace(kvsel_ctx* ctx, size_t bytes);
+// Finds or builds the RoPE tables for (D, base); nullptr on failure.
+const kvsel_ctx::RopeTab* kvsel_rope_tables(kvsel_ctx* ctx, int D, double base, cudaStream_t s);
+
+// ---- launchers (return cudaGetLastError() of their launches) ---------------
+
+cudaError_t launch_memory_update(const void* q, int dtype, int L, int Hq, int R, int D, float lambda,
+                                 int first_turn, int norm_mode, float* M, float* A, cudaStream_t s);
+
+cudaError_t launch_rule_scores(kvsel_ctx* ctx, const void* k_pool, int dtype, const int32_t* slot_map,
+                               int n_slots, int L, int Hq, int Hkv, int N, int D, int64_t layer_stride,
+                               int64_t slot_stride, const float* M, int pi, int q_s, int q_e,
+                               float* rule, void* ws, cudaStream_t s);
+size_t rule_scores_workspace(kvsel_ctx* ctx, int L, int Hq, int N);
+
+// need: how many of the non-forced positions to keep by score (0..|H|).
+cudaError_t launch_topk(const float* score, int N, int pi, int q_s, int q_e, int need, int n_cand,
+                        uint8_t* keep, int32_t* keep_idx, cudaStream_t s);
+
+cudaError_t launch_redirect(const int32_t* slot_in, const uint8_t* keep, int N, int32_t dead,
+                            int32_t* slot_out, cudaStream_t s);
+
+cudaError_t launch_rope_tables(float2* lo, float2* hi, int D, double base, cudaStream_t s);
+
+cudaError_t launch_meank(const void* k_src, int L, int Hkv, int T, int D, int block, int first_block,
+                         const int32_t* src_pos, const kvsel_ctx::RopeTab* tab, int rope_style,
+                         void* index, int Bcap, unsigned* dev_err, cudaStream_t s);
+
+cudaError_t launch_rerope(const void* k_src, int64_t sls, int64_t shs, int src_tokens,
+                          const int32_t* src_block, const int32_t* dst_page, const int32_t* dst_pos0,
+                          int n, int L, int Hkv, int D, int page, const kvsel_ctx::RopeTab* tab,
+                          int rope_style, void* pool, int P, unsigned* dev_err, cudaStream_t s);
+
+cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index, int L, int Hq, int Hkv,
+                                int M, int D, int n_blocks, int Bcap, int n_sink, int n_recent, float* R,
+                                float* R_partial, void* ws, cudaStream_t s);
+size_t block_scores_workspace(int L, int Hq, int Hkv, int M, int n_blocks);

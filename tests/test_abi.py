@@ -1,0 +1,64 @@
+"""The C-ABI library builds, loads, and exports every call include/kvsel.h declares
+(CPU only: no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "kvsel.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvsel_[a-z_0-9]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from kv_cache_retention_gb300 import _build
+    path = _build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_path():
+    names = _declared()
+    for call in ["kvsel_memory_update", "kvsel_rule_scores", "kvsel_topk_retain", "kvsel_redirect_slots",
+                 "kvsel_meank_build", "kvsel_block_scores", "kvsel_select_blocks", "kvsel_rerope_scatter"]:
+        assert call in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_signatures_cover_header():
+    import kv_cache_retention_gb300 as kv
+    assert sorted(kv.SIGNATURES) == _declared()
+    for name in _declared():
+        assert callable(getattr(kv, name))
+
+
+def test_version_and_null_context(lib):
+    lib.kvsel_version.restype = ctypes.c_int
+    assert lib.kvsel_version() == 100
+    lib.kvsel_last_error_string.restype = ctypes.c_char_p
+    lib.kvsel_last_error_string.argtypes = [ctypes.c_void_p]
+    assert lib.kvsel_last_error_string(None) == b"null context"
+    lib.kvsel_ctx_destroy.argtypes = [ctypes.c_void_p]
+    assert lib.kvsel_ctx_destroy(None) == 0
+    # every call rejects a null context without touching the device
+    lib.kvsel_redirect_slots.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+    assert lib.kvsel_redirect_slots(None, None, None, 0, 0, None, None) == -1
+
+
+def test_no_oracle_in_product_sources():
+    """The product library and binding never reference the oracle."""
+    pkg = os.path.join(ROOT, "kv_cache_retention_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".h", ".cuh")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text and "orc_" not in text, f
