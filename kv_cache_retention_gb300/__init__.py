@@ -17,9 +17,7 @@ from __future__ import annotations
 import ctypes
 import os
 
-from . import _build
-
-_LIB_PATH = _build.LIB
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvsel.so")
 
 OK = 0
 ERR_INVALID_ARG = -1

@@ -11,6 +11,11 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built libkvsel.so")
     config.addinivalue_line("markers", "slow: long-running case (full-size oracle comparison)")
+    # libkvsel.so and the oracle are built in-tree (only when stale) before collection
+    import __graft_entry__
+    __graft_entry__.load_builder().build()
+    import oracle
+    oracle.build()
 
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")

@@ -17,8 +17,8 @@ def _declared():
 
 @pytest.fixture(scope="module")
 def lib():
-    from kv_cache_retention_gb300 import _build
-    path = _build.build()
+    import __graft_entry__
+    path = __graft_entry__.load_builder().build()
     return ctypes.CDLL(path)
 
 
@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert not missing, missing
 
 
-def test_binding_signatures_cover_header():
+def test_binding_signatures_cover_header(lib):
     import kv_cache_retention_gb300 as kv
     assert sorted(kv.SIGNATURES) == _declared()
     for name in _declared():

@@ -7,7 +7,7 @@ import torch
 
 pytestmark = pytest.mark.gpu
 
-kv = pytest.importorskip("kv_cache_retention_gb300")
+import kv_cache_retention_gb300 as kv  # noqa: E402
 
 
 @pytest.fixture(scope="module")
