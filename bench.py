@@ -398,6 +398,68 @@ def reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def profile_case(args):
+    """Small case for ncu captures: only `--profile-kernel` runs, on the bench's
+    workloads cut to `--profile-layers` layers (inputs still larger than L2)."""
+    import dataclasses
+
+    import torch
+
+    import kv_cache_retention_gb300 as kv
+    from kv_cache_retention_gb300 import synth
+
+    torch.cuda.set_device(0)
+    tw = dataclasses.replace(synth.TOKEN[TOKEN_WL], L=args.profile_layers)
+    bw = dataclasses.replace(synth.BLOCK[BLOCK_WL], L=args.profile_layers)
+    ctx = kv.Context(0)
+    s = setup_session(kv, synth, ctx, tw, bw, torch)
+    name = args.profile_kernel
+    ev = {}
+
+    def one():
+        sub = {}
+        run_step_only(ctx, s, name, sub)
+        for k, v in sub.items():
+            ev.setdefault(k, []).extend(v)
+
+    for _ in range(args.warmup):
+        run_step_only(ctx, s, name, None)
+    torch.cuda.synchronize()
+    for _ in range(args.steps):
+        one()
+    torch.cuda.synchronize()
+    ctx.check_device()
+    ms = sum(a.elapsed_time(b) for a, b in ev[name]) / len(ev[name])
+    print(json.dumps({"profile_case": name, "layers": args.profile_layers, "ms_per_call": ms}), flush=True)
+
+
+def run_step_only(ctx, s, name, ev):
+    """Run only the call `name` of the step (for profiling captures)."""
+    tw, bw = s["tw"], s["bw"]
+    table = {
+        "memory_update": lambda: ctx.memory_update(s["q_last"], tw.lam, s["M"]),
+        "rule_scores": lambda: ctx.rule_scores(s["pool"], s["M"], tw.L, tw.Hq, tw.Hkv, tw.N, tw.D, tw.pi, tw.q_s,
+                                               tw.q_e, s["rule"], slot_map=s["slot_map"], n_slots=tw.N),
+        "topk_retain": lambda: ctx.topk_retain(s["rule"], tw.pi, tw.q_s, tw.q_e, tw.C, keep=s["keep"],
+                                               keep_idx=s["keep_idx"]),
+        "meank_build": lambda: ctx.meank_build(s["raw_new"], bw.block, s["index"], first_block=bw.first_new_block),
+        "block_scores": lambda: ctx.block_scores(s["q"], s["index"], bw.n_blocks, bw.n_sink, bw.n_recent, s["R"]),
+        "select_blocks": lambda: ctx.select_blocks(s["R"], bw.n_sink, bw.n_recent, bw.k, s["ids"]),
+        "rerope_scatter": lambda: ctx.rerope_scatter(s["staging"], s["src_block"], s["dst_page"], s["dst_pos0"],
+                                                     s["kpool"], bw.rope_base),
+    }
+    fn = table[name]
+    if ev is None:
+        fn()
+        return
+    import torch
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    fn()
+    b.record()
+    ev.setdefault(name, []).append((a, b))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -405,7 +467,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-kernel", default=None, help="run only this call on a cut-down case (for ncu)")
+    ap.add_argument("--profile-layers", type=int, default=4)
     args = ap.parse_args()
+    if args.profile_kernel:
+        profile_case(args)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus if "RANK" in os.environ else 1)))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

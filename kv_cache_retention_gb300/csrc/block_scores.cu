@@ -1,16 +1,37 @@
-// KVMEM block relevance R_b (retrieval step: per (layer, query head, query
-// token) softmax over the candidate blocks of q . kbar / sqrt(d), summed over
-// query tokens and averaged over layer-heads).
+// KVMEM block relevance R_b on the 5th-generation tensor cores (tcgen05).
+//
+// Retrieval step of the KVMEM page: for every (layer l, query head h, query
+// token m) a softmax over the candidate blocks b in C of q . kbar / sqrt(d);
+// the probabilities are summed over query tokens and averaged over all
+// layer-heads.
 //
 // For one (layer l, kv head g) the G = Hq/Hkv query heads' rows form one
-// contiguous [G*M][D] matrix Q_lg and the index rows one [n_blocks][D] matrix
-// K_lg.  The work is two passes over the logits S = Q_lg K_lg^T:
-//   pass 1 (row pass):    lse2[r] = log2 sum_{b in C} 2^(S[r,b] * log2e/sqrt(D))
-//   pass 2 (column pass): mass[lg][b] = sum_r 2^(S[r,b] * log2e/sqrt(D) - lse2[r])
-//   pass 3:               R[b] = sum_lg mass[lg][b] / (L*Hq)   (fixed order)
-// Both passes walk the whole logit matrix; nothing of size rows x blocks is
-// ever stored.  Each pass reduces along the axis its threads own, so no
-// cross-thread reduction of the big matrix is needed.
+// contiguous [G*M][128] bf16 matrix Q_lg and the index one [Bcap][128] matrix
+// K_lg.  The logits S = Q_lg K_lg^T are never stored; two passes recompute them
+// on the tensor cores, each reducing along the axis its epilogue threads own:
+//   row pass:    A = 128 query rows (TMEM lanes), B = 256 candidate blocks per
+//                tile; each lane keeps an online (max, sum 2^x) over its row
+//                -> lse2[r] = log2 sum_{b in C} 2^(S[r,b] log2e/sqrt(d))
+//   column pass: A = 128 candidate blocks (TMEM lanes), B = 256 query rows per
+//                tile; each lane sums 2^(S[b,r] log2e/sqrt(d) - lse2[r]) over
+//                all rows of the group -> mass[lg][b], complete per CTA
+//   finalize:    R[b] = sum_lg mass[lg][b] / (L*Hq), in fixed (l,g) order.
+//
+// Kernel structure (one persistent CTA per SM, 320 threads):
+//   warp 0      TMA producer: A tile per unit, B tiles through a 2-stage ring
+//               (128-byte swizzled, K-major, no multicast)
+//   warp 1      allocates 512 TMEM columns; lane 0 issues tcgen05.mma
+//               (kind::f16, bf16 x bf16 -> fp32, M=128 N=256 K=16, 8 per tile)
+//               into one of two 256-column accumulators and commits to
+//               mbarriers that free the smem stage and hand the accumulator on
+//   warps 2-9   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
+//               32*(w%4)..+31, columns split in two halves), exp2 on the MUFU,
+//               packed fp32 adds; then the accumulator is handed back
+// Every mbarrier wait is bounded (1 s of globaltimer); on a timeout the CTA
+// flags KVSEL_ERR_TIMEOUT in the device error word, drains its own copies and
+// MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
 #include "kvsel_internal.h"
@@ -18,169 +39,445 @@
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr unsigned kFull = 0xffffffffu;
-constexpr int kTile = 64;   // rows x cols per CTA tile (CUDA-core engine)
 constexpr int kD = 128;
+constexpr int BM = 128;                         // A rows per unit = TMEM lanes
+constexpr int BN = 256;                         // B rows per tile = accumulator columns
+constexpr int kABytes = BM * kD * 2;            // 32 KB: two 64-column K blocks of 16 KB
+constexpr int kBBytes = BN * kD * 2;            // 64 KB: two K blocks of 32 KB
+constexpr int kNA = 2, kNB = 2, kNAcc = 2;
+constexpr int kTmemCols = 512;
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreads = 64 + kEpiThreads;
+constexpr uint64_t kWaitNs = 1000000000ull;     // 1 s per wait
 
-// Load a 64-row x 128 bf16 tile (rows row0.., clipped to [lo, hi)) transposed
-// into fp32 shared memory as sm[d][row].
-__device__ void load_tile_t(const __nv_bfloat16* __restrict__ base, int row0, int lo, int hi,
-                            float (*sm)[kTile + 4]) {
-    for (int idx = threadIdx.x; idx < kTile * (kD / 8); idx += blockDim.x) {
-        const int r = idx / (kD / 8), c = idx % (kD / 8);
-        const int row = row0 + r;
-        uint4 raw = make_uint4(0, 0, 0, 0);
-        if (row >= lo && row < hi) raw = __ldg(reinterpret_cast<const uint4*>(base + (int64_t)row * kD + 8 * c));
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            sm[8 * c + 2 * k][r] = __uint_as_float(w[k] << 16);
-            sm[8 * c + 2 * k + 1][r] = __uint_as_float(w[k] & 0xffff0000u);
-        }
-    }
-}
+// instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, N=256, M=128
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
 
-// acc[i][j] = sum_d A[d][ty*4+i] * B[d][tx*4+j]
-__device__ __forceinline__ void mma_tile(const float (*A)[kTile + 4], const float (*B)[kTile + 4], int ty, int tx,
-                                         float (&acc)[4][4]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-#pragma unroll 8
-    for (int d = 0; d < kD; ++d) {
-        const float4 a = *reinterpret_cast<const float4*>(&A[d][ty * 4]);
-        const float4 b = *reinterpret_cast<const float4*>(&B[d][tx * 4]);
-        const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-    }
-}
-
-struct BSArgs {
-    const __nv_bfloat16* q;      // [L][Hq][M][D]
-    const __nv_bfloat16* index;  // [L][Hkv][Bcap][D]
-    int L, Hq, Hkv, M, Bcap, n_blocks, c0, c1;
-    float scale;                 // log2(e)/sqrt(D)
-    float* lse2;                 // [L*Hq*M], row order of the [G*M] group matrices
-    float* mass;                 // [L*Hkv][n_blocks]
-    float* R;
+struct TcArgs {
+    int mode;          // 0 row pass, 1 column pass
+    int n_units;
+    int units_per_lg;
+    int n_bt;          // B tiles per unit
+    int rows_g;        // G*M
+    int c0, c1;        // candidate blocks [c0, c1)
+    int Bcap;
+    int n_blocks;
+    float scale;       // log2(e)/sqrt(D)
+    float* lse2;       // [L*Hkv*rows_g]
+    float* mass;       // [L*Hkv][n_blocks]
+    unsigned* err;
 };
 
-// pass 1: grid (row tiles, L*Hkv); 256 threads as 16 x 16, 4x4 outputs each.
-__global__ void __launch_bounds__(256) bs_rows_simt(const BSArgs a) {
-    extern __shared__ float smem[];
-    float (*Qs)[kTile + 4] = reinterpret_cast<float (*)[kTile + 4]>(smem);
-    float (*Ks)[kTile + 4] = reinterpret_cast<float (*)[kTile + 4]>(smem + kD * (kTile + 4));
-    const int lg = blockIdx.y;
-    const int l = lg / a.Hkv, g = lg % a.Hkv;
-    const int G = a.Hq / a.Hkv;
-    const int rows = G * a.M;
-    const int row0 = blockIdx.x * kTile;
-    const __nv_bfloat16* Q = a.q + ((int64_t)l * a.Hq + (int64_t)g * G) * a.M * kD;
-    const __nv_bfloat16* K = a.index + ((int64_t)l * a.Hkv + g) * a.Bcap * kD;
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    load_tile_t(Q, row0, 0, rows, Qs);
-    float m[4], s[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        m[i] = -INFINITY;
-        s[i] = 0.f;
-    }
-    for (int col0 = a.c0; col0 < a.c1; col0 += kTile) {
-        __syncthreads();
-        load_tile_t(K, col0, a.c0, a.c1, Ks);
-        __syncthreads();
-        float acc[4][4];
-        mma_tile(Qs, Ks, ty, tx, acc);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float v[4], tmax = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const bool ok = col0 + tx * 4 + j < a.c1;
-                v[j] = ok ? acc[i][j] * a.scale : -INFINITY;
-                tmax = fmaxf(tmax, v[j]);
+struct __align__(8) SmemTail {
+    float colv[kNAcc][BN];        // column pass: lse2 of the tile's query rows
+    float red[2][BM][2];          // merge of the two column halves at unit end
+    uint64_t full_a[kNA], empty_a[kNA], full_b[kNB], empty_b[kNB], acc_full[kNAcc], acc_empty[kNAcc];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+constexpr size_t kSmemBytes = (size_t)kNA * kABytes + (size_t)kNB * kBBytes + sizeof(SmemTail) + 1024;
+
+// ---- PTX wrappers ----------------------------------------------------------
+
+__device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(saddr(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t gtimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for the phase of parity `parity`.  Returns false if this or
+// another role gave up (the CTA is then draining).
+__device__ __noinline__ bool wait_phase(uint64_t* b, uint32_t parity, volatile int* abort_flag, unsigned* err) {
+    if (mbar_test(b, parity)) return true;
+    const uint64_t t0 = gtimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test(b, parity)) return true;
+        if ((i & 63) == 0) {
+            if (*abort_flag) return false;
+            if (gtimer() - t0 > kWaitNs) {
+                *abort_flag = 1;
+                atomicOr(err, (unsigned)KVSEL_DEV_TIMEOUT);
+                return false;
             }
-#pragma unroll
-            for (int o = 1; o < 16; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, o));
-            const float mn = fmaxf(m[i], tmax);
-            float ts = 0.f;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) ts += exp2f(v[j] - mn);
-#pragma unroll
-            for (int o = 1; o < 16; o <<= 1) ts += __shfl_xor_sync(kFull, ts, o);
-            s[i] = s[i] * exp2f(m[i] - mn) + ts;
-            m[i] = mn;
-        }
-    }
-    if (tx == 0) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = row0 + ty * 4 + i;
-            if (r < rows) a.lse2[((int64_t)l * a.Hq + (int64_t)g * G) * a.M + r] = m[i] + log2f(s[i]);
         }
     }
 }
 
-// pass 2: grid (candidate column tiles, L*Hkv).  Threads own 4 blocks x 4 rows.
-__global__ void __launch_bounds__(256) bs_cols_simt(const BSArgs a) {
-    extern __shared__ float smem[];
-    float (*Ks)[kTile + 4] = reinterpret_cast<float (*)[kTile + 4]>(smem);
-    float (*Qs)[kTile + 4] = reinterpret_cast<float (*)[kTile + 4]>(smem + kD * (kTile + 4));
-    float* lse_s = smem + 2 * kD * (kTile + 4);
-    const int lg = blockIdx.y;
-    const int l = lg / a.Hkv, g = lg % a.Hkv;
-    const int G = a.Hq / a.Hkv;
-    const int rows = G * a.M;
-    const int col0 = a.c0 + blockIdx.x * kTile;
-    const __nv_bfloat16* Q = a.q + ((int64_t)l * a.Hq + (int64_t)g * G) * a.M * kD;
-    const __nv_bfloat16* K = a.index + ((int64_t)l * a.Hkv + g) * a.Bcap * kD;
-    const float* lse_lg = a.lse2 + ((int64_t)l * a.Hq + (int64_t)g * G) * a.M;
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    load_tile_t(K, col0, a.c0, a.c1, Ks);
-    float colsum[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int row0 = 0; row0 < rows; row0 += kTile) {
-        __syncthreads();
-        load_tile_t(Q, row0, 0, rows, Qs);
-        for (int r = threadIdx.x; r < kTile; r += blockDim.x)
-            lse_s[r] = row0 + r < rows ? lse_lg[row0 + r] : INFINITY;
-        __syncthreads();
-        float acc[4][4];
-        mma_tile(Ks, Qs, ty, tx, acc);  // acc[i][j]: block ty*4+i, row tx*4+j
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) colsum[i] += exp2f(acc[i][j] * a.scale - lse_s[tx * 4 + j]);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float v = colsum[i];
-#pragma unroll
-        for (int o = 1; o < 16; o <<= 1) v += __shfl_xor_sync(kFull, v, o);
-        const int b = col0 + ty * 4 + i;
-        if (tx == 0 && b < a.c1) a.mass[(int64_t)lg * a.n_blocks + b] = v;
+// Bounded wait that ignores the abort flag: used to drain this thread's own
+// copies and MMAs before the CTA frees TMEM and exits.
+__device__ __noinline__ void drain_phase(uint64_t* b, uint32_t parity) {
+    const uint64_t t0 = gtimer();
+    while (!mbar_test(b, parity) && gtimer() - t0 < kWaitNs) {
     }
 }
 
-// pass 3: R[b] = sum_lg mass[lg][b] / (L*Hq) on C; zero outside C (also in mass).
-__global__ void bs_finalize(const BSArgs a) {
+__device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* bar, void* dst, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            saddr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(saddr(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+    return (uint64_t)((addr & 0x3FFFFu) >> 4)   // start address
+           | ((uint64_t)1 << 16)                // leading byte offset (unused with 128B swizzle)
+           | ((uint64_t)(1024 >> 4) << 32)      // stride byte offset: 8 rows x 128 B
+           | ((uint64_t)1 << 46)                // descriptor version
+           | ((uint64_t)2 << 61);               // 128-byte swizzle
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accum)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%"
+        "19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); }
+// Barrier over the epilogue threads that also ANDs a flag across them, so that
+// every epilogue thread takes the same continue / give-up decision.
+__device__ __forceinline__ bool epi_bar_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(kEpiThreads)
+        : "memory");
+    return r != 0;
+}
+
+// ---- the kernel -----------------------------------------------------------
+
+__global__ void __launch_bounds__(kThreads, 1)
+    block_scores_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, const TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* sA = smem;                                   // [kNA][kABytes]
+    uint8_t* sB = smem + kNA * kABytes;                   // [kNB][kBBytes]
+    SmemTail& t = *reinterpret_cast<SmemTail*>(sB + kNB * kBBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int* abort_flag = &t.abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kNA; ++i) {
+            mbar_init(&t.full_a[i], 1);
+            mbar_init(&t.empty_a[i], 1);
+        }
+        for (int i = 0; i < kNB; ++i) {
+            mbar_init(&t.full_b[i], 1);
+            mbar_init(&t.empty_b[i], 1);
+        }
+        for (int i = 0; i < kNAcc; ++i) {
+            mbar_init(&t.acc_full[i], 1);
+            mbar_init(&t.acc_empty[i], kEpiThreads);
+        }
+        mbar_init(&t.mma_done, 1);
+        t.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapB)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&t.tmem_base)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = t.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            uint32_t a_it = 0, b_it = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
+                const int lg = u / a.units_per_lg, ta = u % a.units_per_lg;
+                int ya, yb0;
+                if (a.mode == 0) {
+                    ya = lg * a.rows_g + ta * BM;
+                    yb0 = lg * a.Bcap + a.c0;
+                } else {
+                    ya = lg * a.Bcap + a.c0 + ta * BM;
+                    yb0 = lg * a.rows_g;
+                }
+                const int sa = a_it % kNA;
+                if (!(ok = wait_phase(&t.empty_a[sa], ((a_it / kNA) & 1) ^ 1, abort_flag, a.err))) break;
+                mbar_expect_tx(&t.full_a[sa], kABytes);
+                tma_load_2d(&mapA, &t.full_a[sa], sA + sa * kABytes, 0, ya);
+                tma_load_2d(&mapA, &t.full_a[sa], sA + sa * kABytes + kABytes / 2, 64, ya);
+                ++a_it;
+                for (int tb = 0; tb < a.n_bt; ++tb) {
+                    const int sb = b_it % kNB;
+                    if (!(ok = wait_phase(&t.empty_b[sb], ((b_it / kNB) & 1) ^ 1, abort_flag, a.err))) break;
+                    mbar_expect_tx(&t.full_b[sb], kBBytes);
+                    tma_load_2d(&mapB, &t.full_b[sb], sB + sb * kBBytes, 0, yb0 + tb * BN);
+                    tma_load_2d(&mapB, &t.full_b[sb], sB + sb * kBBytes + kBBytes / 2, 64, yb0 + tb * BN);
+                    ++b_it;
+                }
+            }
+            // drain: wait until every copy this thread started has landed
+            for (uint32_t i = (b_it > (uint32_t)kNB ? b_it - kNB : 0); i < b_it; ++i)
+                drain_phase(&t.full_b[i % kNB], (i / kNB) & 1);
+            for (uint32_t i = (a_it > (uint32_t)kNA ? a_it - kNA : 0); i < a_it; ++i)
+                drain_phase(&t.full_a[i % kNA], (i / kNA) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ------------------------------
+        if (lane == 0) {
+            uint32_t a_it = 0, b_it = 0, acc_it = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
+                const int sa = a_it % kNA;
+                if (!(ok = wait_phase(&t.full_a[sa], (a_it / kNA) & 1, abort_flag, a.err))) break;
+                tc_fence_after();
+                const uint32_t a_base = saddr(sA + sa * kABytes);
+                for (int tb = 0; tb < a.n_bt; ++tb) {
+                    const int sb = b_it % kNB;
+                    const int k = acc_it % kNAcc;
+                    if (!(ok = wait_phase(&t.full_b[sb], (b_it / kNB) & 1, abort_flag, a.err))) break;
+                    if (!(ok = wait_phase(&t.acc_empty[k], ((acc_it / kNAcc) & 1) ^ 1, abort_flag, a.err))) break;
+                    tc_fence_after();
+                    const uint32_t b_base = saddr(sB + sb * kBBytes);
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(k * BN);
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint32_t off = (uint32_t)((kk & 3) * 32);
+                        const uint64_t ad = sw128_desc(a_base + (kk >> 2) * (kABytes / 2) + off);
+                        const uint64_t bd = sw128_desc(b_base + (kk >> 2) * (kBBytes / 2) + off);
+                        umma_bf16(d_tmem, ad, bd, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&t.empty_b[sb]);
+                    umma_commit(&t.acc_full[k]);
+                    ++b_it;
+                    ++acc_it;
+                }
+                if (ok) umma_commit(&t.empty_a[sa]);
+                ++a_it;
+            }
+            // drain: every MMA issued by this thread completes before TMEM is freed
+            umma_commit(&t.mma_done);
+            drain_phase(&t.mma_done, 0);
+        }
+    } else {
+        // ------------------------------ epilogue ------------------------------
+        const int ew = warp - 2;                 // 0..7
+        const int q = warp & 3;                  // TMEM lane quarter this warp may access
+        const int half = ew >> 2;                // column half
+        const int r_local = q * 32 + lane;       // TMEM lane = A row of the unit
+        const int etid = ew * 32 + lane;         // 0..255
+        uint32_t acc_it = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
+            const int lg = u / a.units_per_lg, ta = u % a.units_per_lg;
+            float m_run = -INFINITY;
+            float2 s2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                            make_float2(0.f, 0.f)};
+            for (int tb = 0; tb < a.n_bt; ++tb) {
+                const int k = acc_it % kNAcc;
+                if (a.mode == 1) {
+                    const int r = tb * BN + etid;  // query row of column etid
+                    t.colv[k][etid] = r < a.rows_g ? a.lse2[(int64_t)lg * a.rows_g + r] : INFINITY;
+                }
+                ok = wait_phase(&t.acc_full[k], (acc_it / kNAcc) & 1, abort_flag, a.err);
+                if (!(ok = epi_bar_and(ok))) break;  // also publishes colv to the other epilogue warps
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(k * BN + half * 128);
+                float v[4][32];
+                tmem_ld32(taddr, v[0]);
+                tmem_ld32(taddr + 32, v[1]);
+                tmem_ld32(taddr + 64, v[2]);
+                tmem_ld32(taddr + 96, v[3]);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&t.acc_empty[k]);  // the accumulator is free for the next tile
+                if (a.mode == 0) {
+                    // row pass: online (max, sum 2^x) over this half's 128 columns
+                    const int col0 = a.c0 + tb * BN + half * 128;   // block id of column 0 of this half
+                    const int nvalid = a.c1 - col0;                 // columns >= nvalid are masked
+                    if (nvalid < 128) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (c * 32 + i >= nvalid) v[c][i] = -INFINITY;
+                    }
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) mx = max3(mx, v[c][i], v[c][i + 1]);
+                    const float m_new = fmaxf(m_run, mx * a.scale);
+                    if (m_new != -INFINITY) {
+                        if (m_new > m_run) {
+                            const float f = ex2(m_run - m_new);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) s2[j] = make_float2(s2[j].x * f, s2[j].y * f);
+                            m_run = m_new;
+                        }
+                        const float2 sc = make_float2(a.scale, a.scale), nm = make_float2(-m_run, -m_run);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+#pragma unroll
+                            for (int i = 0; i < 32; i += 2) {
+                                const float2 x = __ffma2_rn(make_float2(v[c][i], v[c][i + 1]), sc, nm);
+                                s2[(i >> 1) & 3] = __fadd2_rn(s2[(i >> 1) & 3], make_float2(ex2(x.x), ex2(x.y)));
+                            }
+                    }
+                } else {
+                    // column pass: sum over this half's 128 query rows of 2^(x - lse2[row])
+                    const float2 sc = make_float2(a.scale, a.scale);
+                    const float* cv = &t.colv[k][half * 128];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 l4 = *reinterpret_cast<const float4*>(cv + c * 32 + i);
+                            const float2 x0 = __ffma2_rn(make_float2(v[c][i], v[c][i + 1]), sc, make_float2(-l4.x, -l4.y));
+                            const float2 x1 =
+                                __ffma2_rn(make_float2(v[c][i + 2], v[c][i + 3]), sc, make_float2(-l4.z, -l4.w));
+                            s2[(i >> 2) & 3] = __fadd2_rn(s2[(i >> 2) & 3], make_float2(ex2(x0.x), ex2(x0.y)));
+                            s2[((i >> 2) + 2) & 3] =
+                                __fadd2_rn(s2[((i >> 2) + 2) & 3], make_float2(ex2(x1.x), ex2(x1.y)));
+                        }
+                }
+                ++acc_it;
+            }
+            if (!ok) break;
+            // merge the two column halves of each lane
+            const float s_half = (s2[0].x + s2[0].y) + (s2[1].x + s2[1].y) + (s2[2].x + s2[2].y) + (s2[3].x + s2[3].y);
+            t.red[half][r_local][0] = m_run;
+            t.red[half][r_local][1] = s_half;
+            epi_bar();
+            if (half == 0) {
+                if (a.mode == 0) {
+                    const int row = ta * BM + r_local;
+                    if (row < a.rows_g) {
+                        const float m0 = t.red[0][r_local][0], m1 = t.red[1][r_local][0];
+                        const float m = fmaxf(m0, m1);
+                        float s = 0.f;
+                        if (m != -INFINITY) s = t.red[0][r_local][1] * ex2(m0 - m) + t.red[1][r_local][1] * ex2(m1 - m);
+                        a.lse2[(int64_t)lg * a.rows_g + row] = s > 0.f ? m + __log2f(s) : -INFINITY;
+                    }
+                } else {
+                    const int b = a.c0 + ta * BM + r_local;
+                    if (b < a.c1) a.mass[(int64_t)lg * a.n_blocks + b] = t.red[0][r_local][1] + t.red[1][r_local][1];
+                }
+            }
+            epi_bar();
+        }
+    }
+
+    // all roles: TMEM is released once every MMA has completed (MMA lane drained above)
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// R[b] = sum_lg mass[lg][b] / (L*Hq) on C; zero outside C (also in mass).
+__global__ void bs_finalize(const float* __restrict__ mass_in, float* mass, float* R, int LH, int n_blocks, int c0,
+                            int c1, float inv) {
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= a.n_blocks) return;
-    const int LH = a.L * a.Hkv;
-    if (b < a.c0 || b >= a.c1) {
-        a.R[b] = 0.f;
-        for (int lg = 0; lg < LH; ++lg) a.mass[(int64_t)lg * a.n_blocks + b] = 0.f;
+    if (b >= n_blocks) return;
+    if (b < c0 || b >= c1) {
+        R[b] = 0.f;
+        for (int lg = 0; lg < LH; ++lg) mass[(int64_t)lg * n_blocks + b] = 0.f;
         return;
     }
     float acc = 0.f;
-    for (int lg = 0; lg < LH; ++lg) acc += a.mass[(int64_t)lg * a.n_blocks + b];
-    a.R[b] = acc / ((float)a.L * (float)a.Hq);
+    for (int lg = 0; lg < LH; ++lg) acc += mass_in[(int64_t)lg * n_blocks + b];
+    R[b] = acc * inv;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 [rows][128] view, box {64 columns, box_rows}, 128-byte swizzle, zero fill.
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+    auto fn = encoder();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 }  // namespace
 
@@ -191,36 +488,53 @@ size_t block_scores_workspace(int L, int Hq, int Hkv, int M, int n_blocks) {
 cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index, int L, int Hq, int Hkv, int M, int D,
                                 int n_blocks, int Bcap, int n_sink, int n_recent, float* R, float* R_partial, void* ws,
                                 cudaStream_t s) {
-    (void)ctx;
     (void)D;
-    BSArgs a;
-    a.q = static_cast<const __nv_bfloat16*>(q);
-    a.index = static_cast<const __nv_bfloat16*>(index);
-    a.L = L;
-    a.Hq = Hq;
-    a.Hkv = Hkv;
-    a.M = M;
-    a.Bcap = Bcap;
-    a.n_blocks = n_blocks;
-    a.c0 = n_sink < n_blocks ? n_sink : n_blocks;
-    a.c1 = n_blocks - n_recent > a.c0 ? n_blocks - n_recent : a.c0;
-    a.scale = kLog2e / sqrtf(128.f);
-    char* w = static_cast<char*>(ws);
-    a.lse2 = reinterpret_cast<float*>(w);
-    w += align256((size_t)L * Hq * M * sizeof(float));
-    a.mass = R_partial ? R_partial : reinterpret_cast<float*>(w);
-    a.R = R;
     const int G = Hq / Hkv;
-    const int rows = G * M;
-    const int ncand = a.c1 - a.c0;
+    const int rows_g = G * M;
+    const int c0 = n_sink < n_blocks ? n_sink : n_blocks;
+    const int c1 = n_blocks - n_recent > c0 ? n_blocks - n_recent : c0;
+    const int ncand = c1 - c0;
+    const int LH = L * Hkv;
+    char* w = static_cast<char*>(ws);
+    float* lse2 = reinterpret_cast<float*>(w);
+    w += align256((size_t)L * Hq * M * sizeof(float));
+    float* mass = R_partial ? R_partial : reinterpret_cast<float*>(w);
+
     if (ncand > 0) {
-        const size_t smem = sizeof(float) * 2 * kD * (kTile + 4);
-        cudaFuncSetAttribute(bs_rows_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        bs_rows_simt<<<dim3((rows + kTile - 1) / kTile, L * Hkv), 256, smem, s>>>(a);
-        const size_t smem2 = smem + sizeof(float) * kTile;
-        cudaFuncSetAttribute(bs_cols_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
-        bs_cols_simt<<<dim3((ncand + kTile - 1) / kTile, L * Hkv), 256, smem2, s>>>(a);
+        CUtensorMap qA, qB, iA, iB;
+        const uint64_t q_rows = (uint64_t)L * Hq * M, i_rows = (uint64_t)LH * Bcap;
+        if (!make_map(&qA, q, q_rows, BM) || !make_map(&qB, q, q_rows, BN) || !make_map(&iA, index, i_rows, BM) ||
+            !make_map(&iB, index, i_rows, BN))
+            return cudaErrorInvalidValue;
+        cudaError_t e = cudaFuncSetAttribute(block_scores_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        TcArgs a;
+        a.rows_g = rows_g;
+        a.c0 = c0;
+        a.c1 = c1;
+        a.Bcap = Bcap;
+        a.n_blocks = n_blocks;
+        a.scale = kLog2e / sqrtf((float)kD);
+        a.lse2 = lse2;
+        a.mass = mass;
+        a.err = ctx->dev_err;
+        // row pass
+        a.mode = 0;
+        a.units_per_lg = (rows_g + BM - 1) / BM;
+        a.n_units = LH * a.units_per_lg;
+        a.n_bt = (ncand + BN - 1) / BN;
+        int grid = a.n_units < ctx->num_sms ? a.n_units : ctx->num_sms;
+        block_scores_tc<<<grid, kThreads, kSmemBytes, s>>>(qA, iB, a);
+        // column pass
+        a.mode = 1;
+        a.units_per_lg = (ncand + BM - 1) / BM;
+        a.n_units = LH * a.units_per_lg;
+        a.n_bt = (rows_g + BN - 1) / BN;
+        grid = a.n_units < ctx->num_sms ? a.n_units : ctx->num_sms;
+        block_scores_tc<<<grid, kThreads, kSmemBytes, s>>>(iA, qB, a);
     }
-    bs_finalize<<<(n_blocks + 255) / 256, 256, 0, s>>>(a);
+    bs_finalize<<<(n_blocks + 255) / 256, 256, 0, s>>>(mass, mass, R, LH, n_blocks, c0, c1,
+                                                       1.0f / ((float)L * (float)Hq));
     return cudaGetLastError();
 }

@@ -145,6 +145,7 @@ int kvsel_check_device(kvsel_ctx* ctx, void* stream) {
     if (e != cudaSuccess) return cuda_fail(ctx, e, "read device error word");
     if (!word) return KVSEL_OK;
     cudaMemset(ctx->dev_err, 0, sizeof(unsigned));
+    if (word & KVSEL_DEV_TIMEOUT) return fail(ctx, KVSEL_ERR_TIMEOUT, "a bounded device wait gave up (tensor-core pipeline)");
     return fail(ctx, KVSEL_ERR_DEVICE_CHECK, "device check failed:%s%s%s%s",
                 (word & KVSEL_DEV_BAD_SLOT) ? " slot out of range" : "",
                 (word & KVSEL_DEV_BAD_POSITION) ? " position out of range" : "",

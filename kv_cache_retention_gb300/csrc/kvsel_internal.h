@@ -34,6 +34,7 @@ enum kvsel_devcheck : unsigned {
     KVSEL_DEV_BAD_POSITION = 1u << 1,
     KVSEL_DEV_BAD_BLOCK = 1u << 2,
     KVSEL_DEV_BAD_PAGE = 1u << 3,
+    KVSEL_DEV_TIMEOUT = 1u << 8,  // a bounded wait inside a kernel gave up
 };
 
 // Positions p are split as p = hi * KVSEL_ROPE_LO + lo; both tables in fp64 -> fp32.
