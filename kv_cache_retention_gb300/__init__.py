@@ -44,6 +44,7 @@ SIGNATURES = {
     "kvsel_check_device": (_I, [_P, _P]),
     "kvsel_memory_update": (_I, [_P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P]),
     "kvsel_rule_scores": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I64, _I64, _P, _I, _I, _I, _P, _P]),
+    "kvsel_rule_scores_noalloc": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I64, _I64, _P, _I, _I, _I, _P, _P]),
     "kvsel_topk_retain": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _IP, _P]),
     "kvsel_redirect_slots": (_I, [_P, _P, _P, _I, ctypes.c_int32, _P, _P]),
     "kvsel_meank_build": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _D, _I, _P, _I, _P]),
@@ -112,6 +113,15 @@ def kvsel_rule_scores(ctx, k_pool, k_dtype, slot_map, n_slots, L, Hq, Hkv, N, D,
                       pi, q_s, q_e, rule, stream):
     return _lib.kvsel_rule_scores(ctx, k_pool, k_dtype, slot_map, n_slots, L, Hq, Hkv, N, D, layer_stride,
                                   slot_stride, M, pi, q_s, q_e, rule, stream)
+
+
+def kvsel_rule_scores_noalloc(ctx, k_pool, k_dtype, slot_map, n_slots, L, Hq, Hkv, N, D, layer_stride, slot_stride,
+                              M, pi, q_s, q_e, rule, stream):
+    """kvsel_rule_scores on the library's fixed scratch array: no device allocation
+    (for callers that cannot allocate; sizes needing more than 64 MiB of scratch
+    are rejected)."""
+    return _lib.kvsel_rule_scores_noalloc(ctx, k_pool, k_dtype, slot_map, n_slots, L, Hq, Hkv, N, D, layer_stride,
+                                          slot_stride, M, pi, q_s, q_e, rule, stream)
 
 
 def kvsel_topk_retain(ctx, score, N, pi, q_s, q_e, C, keep, keep_idx, n_keep_host, stream):

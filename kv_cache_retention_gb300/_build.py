@@ -21,6 +21,7 @@ SOURCES = [
     "select_kernels.cu",
     "kvmem_kernels.cu",
     "block_scores.cu",
+    "rule_scores_noalloc.cu",
 ]
 HEADERS = ["kvsel_internal.h", os.path.join("..", "..", "include", "kvsel.h")]
 
