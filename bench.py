@@ -33,6 +33,20 @@ TOKEN_WL = "8b"
 BLOCK_WL = "ws1m"
 
 
+def aggregate(ms_local, rows_per_step, steps, dist=None, device=None):
+    """Whole-job throughput of replicas: every rank ran `steps` steps of
+    `rows_per_step` rows; the job takes as long as its slowest rank.
+    Returns (rows/s over all ranks, max ms over ranks)."""
+    import torch
+    t = torch.tensor([float(ms_local)], dtype=torch.float64, device=device)
+    world = 1
+    if dist is not None and dist.is_initialized():
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        world = dist.get_world_size()
+    ms_max = float(t.item())
+    return world * rows_per_step * steps / (ms_max / 1e3), ms_max
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -222,10 +236,6 @@ def ours(args, rank, world, local_rank):
     barrier()
     clk = clocks.stop()
     ms_total = start.elapsed_time(end)
-    ms_t = torch.tensor([ms_total], device="cuda")
-    if dist is not None:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
     per_call = {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in ev.items()}
     ctx.check_device()
 
@@ -254,14 +264,10 @@ def ours(args, rank, world, local_rank):
     e_end.record()
     torch.cuda.synchronize()
     barrier()
-    e_ms = torch.tensor([e_start.elapsed_time(e_end)], device="cuda")
-    if dist is not None:
-        dist.all_reduce(e_ms, op=dist.ReduceOp.MAX)
-
     token_rows, block_rows = workload_rows(tw, bw)
     rows_step = token_rows + block_rows
-    value = world * rows_step * args.steps / (ms_max / 1e3)
-    e2e_value = world * rows_step * e2e_steps / (float(e_ms.item()) / 1e3)
+    value, ms_max = aggregate(ms_total, rows_step, args.steps, dist, "cuda")
+    e2e_value, e2e_ms_max = aggregate(e_start.elapsed_time(e_end), rows_step, e2e_steps, dist, "cuda")
 
     if rank != 0:
         if dist is not None:
@@ -300,7 +306,7 @@ def ours(args, rank, world, local_rank):
         "data": "synthetic (seeded; shapes of the pages' workloads)", "config": config_dict(tw, bw, world),
         "rows_per_step": {"token": token_rows, "block": block_rows},
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": float(e_ms.item()) / e2e_steps,
+                "ms_per_step": e2e_ms_max / e2e_steps,
                 "inputs": "per-step query rows, new raw K and staged top-block K from pinned host; "
                           "K pool and Mean-K index resident on the device"},
         "gpu_launches": sum(LAUNCHES.values()) * args.steps,
@@ -315,7 +321,7 @@ def ours(args, rank, world, local_rank):
 # bench workload; an entry is removed whenever its kernel changes.  Source: profiles/*.md.
 PROFILED_TRAFFIC = {
     # block_scores_tc, 4-layer capture (357.4 + 359.5 MB for the two passes) x 16 layers groups
-    "block_scores": 16 * (357.412e6 + 359.533e6),
+    # (no current capture: the kernel changed since the last one)
 }
 
 

@@ -236,7 +236,7 @@ int kvsel_select_blocks(kvsel_ctx* ctx, const float* R, int n_blocks, int n_sink
  *          dst_page < P, positions in [0, 2^24).  An entry breaking these is
  *          skipped and sets the device error word.
  *   pool   bf16 [L][P][page][Hkv][D]
- * Requires D in {16,32,64,128,256}.
+ * Requires D in {16,32,64,128,256}, page*D <= 16384.
  */
 int kvsel_rerope_scatter(kvsel_ctx* ctx, const void* k_src, int64_t src_layer_stride,
                          int64_t src_head_stride, int src_tokens, const int32_t* src_block,

@@ -17,16 +17,17 @@
 //                all rows of the group -> mass[lg][b], complete per CTA
 //   finalize:    R[b] = sum_lg mass[lg][b] / (L*Hq), in fixed (l,g) order.
 //
-// Kernel structure (one persistent CTA per SM, 320 threads):
+// Kernel structure (one persistent CTA per SM, 576 threads):
 //   warp 0      TMA producer: A tile per unit, B tiles through a 2-stage ring
 //               (128-byte swizzled, K-major, no multicast)
 //   warp 1      allocates 512 TMEM columns; lane 0 issues tcgen05.mma
 //               (kind::f16, bf16 x bf16 -> fp32, M=128 N=256 K=16, 8 per tile)
 //               into one of two 256-column accumulators and commits to
 //               mbarriers that free the smem stage and hand the accumulator on
-//   warps 2-9   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
-//               32*(w%4)..+31, columns split in two halves), exp2 on the MUFU,
-//               packed fp32 adds; then the accumulator is handed back
+//   warps 2-17  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
+//               32*(w%4)..+31; four column slices of 64), exp2 on the MUFU,
+//               packed fp32 adds; the accumulator is handed back as soon as it
+//               is in registers
 // Every mbarrier wait is bounded (1 s of globaltimer); on a timeout the CTA
 // flags KVSEL_ERR_TIMEOUT in the device error word, drains its own copies and
 // MMAs, frees TMEM and returns.
@@ -46,10 +47,13 @@ constexpr int kABytes = BM * kD * 2;            // 32 KB: two 64-column K blocks
 constexpr int kBBytes = BN * kD * 2;            // 64 KB: two K blocks of 32 KB
 constexpr int kNA = 2, kNB = 2, kNAcc = 2;
 constexpr int kTmemCols = 512;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;                   // 4 TMEM lane quarters x kSlices column slices
+constexpr int kSlices = kEpiWarps / 4;
+constexpr int kSliceCols = BN / kSlices;        // accumulator columns per epilogue thread and tile
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr uint64_t kWaitNs = 1000000000ull;     // 1 s per wait
+constexpr uint32_t kSuspendNs = 20000;          // try_wait may park the thread this long (woken on completion)
 
 // instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, N=256, M=128
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
@@ -61,19 +65,21 @@ struct TcArgs {
     int units_per_lg;
     int n_bt;          // B tiles per unit
     int rows_g;        // G*M
+    int rows_pad;      // rows_g rounded up to a multiple of 4 (row stride of lse2)
     int c0, c1;        // candidate blocks [c0, c1)
     int Bcap;
     int n_blocks;
     float scale;       // log2(e)/sqrt(D)
-    float* lse2;       // [L*Hkv*rows_g]
+    float* lse2;       // [L*Hkv][rows_pad]; pad entries hold +inf
     float* mass;       // [L*Hkv][n_blocks]
     unsigned* err;
 };
 
 struct __align__(8) SmemTail {
-    float colv[kNAcc][BN];        // column pass: lse2 of the tile's query rows
-    float red[2][BM][2];          // merge of the two column halves at unit end
+    float colv[kNAcc][BN];        // column pass: lse2 of the tile's query rows (bulk-copied)
+    float red[kSlices][BM][2];    // merge of the column slices at unit end
     uint64_t full_a[kNA], empty_a[kNA], full_b[kNB], empty_b[kNB], acc_full[kNAcc], acc_empty[kNAcc];
+    uint64_t lse_full[kNAcc], lse_empty[kNAcc];  // column pass: colv ring, one slot per accumulator
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -96,9 +102,9 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
 __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(saddr(b)), "r"(parity)
+        : "r"(saddr(b)), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -142,6 +148,54 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* ba
         : "memory");
 }
 
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Plain bulk copy global -> shared (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     saddr(dst)),
+                 "l"(src), "r"(bytes), "r"(saddr(bar))
+                 : "memory");
+}
+
+// 2^x on the FMA pipe, for a share of the exponentials (the MUFU computes the
+// rest): x = n + f with n = rint(x) (added to 1.5*2^23 and subtracted back),
+// |f| <= 1/2; 2^f = e^(f ln 2) by its Taylor series to degree 5 (truncation
+// below 3.4e-6 relative); 2^n goes into the exponent field.  x is clamped at
+// -125, so x = -inf gives ~2e-38 instead of 0 (far below anything summed here).
+__device__ __forceinline__ float2 exp2_fma(float2 x) {
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    constexpr float c1 = 0.693147182464599609375f, c2 = 0.2402265071868896484375f, c3 = 0.0555041097104549407958984375f,
+                    c4 = 0.009618128649890422821044921875f, c5 = 0.001333355787210166454315185546875f;
+    x = make_float2(fmaxf(x.x, -125.f), fmaxf(x.y, -125.f));
+    const float2 t = __fadd2_rn(x, make_float2(kMagic, kMagic));
+    const float2 n = __fadd2_rn(t, make_float2(-kMagic, -kMagic));
+    const float2 f = __fadd2_rn(x, make_float2(-n.x, -n.y));
+    float2 p = __ffma2_rn(make_float2(c5, c5), f, make_float2(c4, c4));
+    p = __ffma2_rn(p, f, make_float2(c3, c3));
+    p = __ffma2_rn(p, f, make_float2(c2, c2));
+    p = __ffma2_rn(p, f, make_float2(c1, c1));
+    p = __ffma2_rn(p, f, make_float2(1.f, 1.f));
+    const int ex = (__float_as_int(t.x) - __float_as_int(kMagic)) << 23;
+    const int ey = (__float_as_int(t.y) - __float_as_int(kMagic)) << 23;
+    return make_float2(__int_as_float(__float_as_int(p.x) + ex), __int_as_float(__float_as_int(p.y) + ey));
+}
+
+// Exponentials of a pair: pairs with index < kPolyPairs (of 16 per 32-column
+// chunk) go to the FMA pipe, the rest to the MUFU.
+#ifndef KVSEL_POLY_PAIRS
+#define KVSEL_POLY_PAIRS 0
+#endif
+constexpr int kPolyPairs = KVSEL_POLY_PAIRS;
+__device__ __forceinline__ float2 exp2_pair(float2 x, int pair) {
+    if (pair < kPolyPairs) return exp2_fma(x);
+    return make_float2(ex2(x.x), ex2(x.y));
+}
+
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
     return (uint64_t)((addr & 0x3FFFFu) >> 4)   // start address
            | ((uint64_t)1 << 16)                // leading byte offset (unused with 128B swizzle)
@@ -179,11 +233,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -200,6 +249,31 @@ __device__ __forceinline__ bool epi_bar_and(bool v) {
         : "r"((uint32_t)v), "n"(kEpiThreads)
         : "memory");
     return r != 0;
+}
+
+// Column-pass accumulation of one slice: s2 += 2^(v*scale - lse[col]); with MASK,
+// columns >= nvalid are skipped (their lse slots may hold stale data).
+template <bool MASK>
+__device__ __forceinline__ void col_accumulate(const float (&v)[kSliceCols / 32][32], const float* cv, float scale,
+                                               int nvalid, float2 (&s2)[4]) {
+    const float2 sc = make_float2(scale, scale);
+#pragma unroll
+    for (int c = 0; c < kSliceCols / 32; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(cv + c * 32 + i);
+            float2 x0 = __ffma2_rn(make_float2(v[c][i], v[c][i + 1]), sc, make_float2(-l4.x, -l4.y));
+            float2 x1 = __ffma2_rn(make_float2(v[c][i + 2], v[c][i + 3]), sc, make_float2(-l4.z, -l4.w));
+            if (MASK) {
+                const int col = c * 32 + i;
+                if (col >= nvalid) x0.x = -INFINITY;
+                if (col + 1 >= nvalid) x0.y = -INFINITY;
+                if (col + 2 >= nvalid) x1.x = -INFINITY;
+                if (col + 3 >= nvalid) x1.y = -INFINITY;
+            }
+            s2[(i >> 2) & 3] = __fadd2_rn(s2[(i >> 2) & 3], exp2_pair(x0, i >> 1));
+            s2[((i >> 2) + 2) & 3] = __fadd2_rn(s2[((i >> 2) + 2) & 3], exp2_pair(x1, (i >> 1) + 1));
+        }
 }
 
 // ---- the kernel -----------------------------------------------------------
@@ -225,7 +299,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kNAcc; ++i) {
             mbar_init(&t.acc_full[i], 1);
-            mbar_init(&t.acc_empty[i], kEpiThreads);
+            mbar_init(&t.acc_empty[i], kEpiWarps);  // one arrival per epilogue warp
+            mbar_init(&t.lse_full[i], 1);
+            mbar_init(&t.lse_empty[i], kEpiWarps);
         }
         mbar_init(&t.mma_done, 1);
         t.abort_flag = 0;
@@ -271,6 +347,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_expect_tx(&t.full_b[sb], kBBytes);
                     tma_load_2d(&mapB, &t.full_b[sb], sB + sb * kBBytes, 0, yb0 + tb * BN);
                     tma_load_2d(&mapB, &t.full_b[sb], sB + sb * kBBytes + kBBytes / 2, 64, yb0 + tb * BN);
+                    if (a.mode == 1) {
+                        // the log-sum-exps of this tile's query rows, one slot per accumulator
+                        const int k = b_it % kNAcc;
+                        if (!(ok = wait_phase(&t.lse_empty[k], ((b_it / kNAcc) & 1) ^ 1, abort_flag, a.err))) break;
+                        const int r0 = tb * BN;
+                        const uint32_t bytes = 4u * (uint32_t)min(BN, a.rows_pad - r0);
+                        mbar_expect_tx(&t.lse_full[k], bytes);
+                        bulk_copy(&t.colv[k][0], a.lse2 + (int64_t)lg * a.rows_pad + r0, bytes, &t.lse_full[k]);
+                    }
                     ++b_it;
                 }
             }
@@ -279,6 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 drain_phase(&t.full_b[i % kNB], (i / kNB) & 1);
             for (uint32_t i = (a_it > (uint32_t)kNA ? a_it - kNA : 0); i < a_it; ++i)
                 drain_phase(&t.full_a[i % kNA], (i / kNA) & 1);
+            if (a.mode == 1)
+                for (uint32_t i = (b_it > (uint32_t)kNAcc ? b_it - kNAcc : 0); i < b_it; ++i)
+                    drain_phase(&t.lse_full[i % kNAcc], (i / kNAcc) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
@@ -319,11 +407,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------ epilogue ------------------------------
-        const int ew = warp - 2;                 // 0..7
+        const int ew = warp - 2;                 // 0 .. kEpiWarps-1
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
-        const int half = ew >> 2;                // column half
+        const int slice = ew >> 2;               // column slice
         const int r_local = q * 32 + lane;       // TMEM lane = A row of the unit
-        const int etid = ew * 32 + lane;         // 0..255
+        const int etid = ew * 32 + lane;
         uint32_t acc_it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
@@ -333,36 +421,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                             make_float2(0.f, 0.f)};
             for (int tb = 0; tb < a.n_bt; ++tb) {
                 const int k = acc_it % kNAcc;
-                if (a.mode == 1) {
-                    const int r = tb * BN + etid;  // query row of column etid
-                    t.colv[k][etid] = r < a.rows_g ? a.lse2[(int64_t)lg * a.rows_g + r] : INFINITY;
+                // a timed-out wait makes this thread skip its work; the epilogue warps
+                // agree on giving up at the end of the unit
+                if (ok) ok = wait_phase(&t.acc_full[k], (acc_it / kNAcc) & 1, abort_flag, a.err);
+                if (ok && a.mode == 1) ok = wait_phase(&t.lse_full[k], (acc_it / kNAcc) & 1, abort_flag, a.err);
+                ok = __all_sync(0xffffffffu, ok);  // warp-uniform: TMEM loads are warp-collective
+                if (!ok) {
+                    ++acc_it;
+                    continue;
                 }
-                ok = wait_phase(&t.acc_full[k], (acc_it / kNAcc) & 1, abort_flag, a.err);
-                if (!(ok = epi_bar_and(ok))) break;  // also publishes colv to the other epilogue warps
                 tc_fence_after();
-                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(k * BN + half * 128);
-                float v[4][32];
-                tmem_ld32(taddr, v[0]);
-                tmem_ld32(taddr + 32, v[1]);
-                tmem_ld32(taddr + 64, v[2]);
-                tmem_ld32(taddr + 96, v[3]);
+                const uint32_t taddr =
+                    tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(k * BN + slice * kSliceCols);
+                float v[kSliceCols / 32][32];
+#pragma unroll
+                for (int c = 0; c < kSliceCols / 32; ++c) tmem_ld32(taddr + 32 * c, v[c]);
                 tmem_ld_wait();
                 tc_fence_before();
-                mbar_arrive(&t.acc_empty[k]);  // the accumulator is free for the next tile
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&t.acc_empty[k]);  // this warp's part of the accumulator is read
                 if (a.mode == 0) {
-                    // row pass: online (max, sum 2^x) over this half's 128 columns
-                    const int col0 = a.c0 + tb * BN + half * 128;   // block id of column 0 of this half
-                    const int nvalid = a.c1 - col0;                 // columns >= nvalid are masked
-                    if (nvalid < 128) {
+                    // row pass: online (max, sum 2^x) over this slice's columns
+                    const int col0 = a.c0 + tb * BN + slice * kSliceCols;  // block id of the slice's column 0
+                    const int nvalid = a.c1 - col0;                        // columns >= nvalid are masked
+                    if (nvalid < kSliceCols) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
+                        for (int c = 0; c < kSliceCols / 32; ++c)
 #pragma unroll
                             for (int i = 0; i < 32; ++i)
                                 if (c * 32 + i >= nvalid) v[c][i] = -INFINITY;
                     }
                     float mx = -INFINITY;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
+                    for (int c = 0; c < kSliceCols / 32; ++c)
 #pragma unroll
                         for (int i = 0; i < 32; i += 2) mx = max3(mx, v[c][i], v[c][i + 1]);
                     const float m_new = fmaxf(m_run, mx * a.scale);
@@ -375,51 +466,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         const float2 sc = make_float2(a.scale, a.scale), nm = make_float2(-m_run, -m_run);
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
+                        for (int c = 0; c < kSliceCols / 32; ++c)
 #pragma unroll
                             for (int i = 0; i < 32; i += 2) {
                                 const float2 x = __ffma2_rn(make_float2(v[c][i], v[c][i + 1]), sc, nm);
-                                s2[(i >> 1) & 3] = __fadd2_rn(s2[(i >> 1) & 3], make_float2(ex2(x.x), ex2(x.y)));
+                                s2[(i >> 1) & 3] = __fadd2_rn(s2[(i >> 1) & 3], exp2_pair(x, i >> 1));
                             }
                     }
                 } else {
-                    // column pass: sum over this half's 128 query rows of 2^(x - lse2[row])
-                    const float2 sc = make_float2(a.scale, a.scale);
-                    const float* cv = &t.colv[k][half * 128];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-#pragma unroll
-                        for (int i = 0; i < 32; i += 4) {
-                            const float4 l4 = *reinterpret_cast<const float4*>(cv + c * 32 + i);
-                            const float2 x0 = __ffma2_rn(make_float2(v[c][i], v[c][i + 1]), sc, make_float2(-l4.x, -l4.y));
-                            const float2 x1 =
-                                __ffma2_rn(make_float2(v[c][i + 2], v[c][i + 3]), sc, make_float2(-l4.z, -l4.w));
-                            s2[(i >> 2) & 3] = __fadd2_rn(s2[(i >> 2) & 3], make_float2(ex2(x0.x), ex2(x0.y)));
-                            s2[((i >> 2) + 2) & 3] =
-                                __fadd2_rn(s2[((i >> 2) + 2) & 3], make_float2(ex2(x1.x), ex2(x1.y)));
-                        }
+                    // column pass: sum over this slice's query rows of 2^(x - lse2[row]);
+                    // rows past the group (last tile only) contribute nothing
+                    const int nvalid = a.rows_g - (tb * BN + slice * kSliceCols);
+                    const float* cv = &t.colv[k][slice * kSliceCols];
+                    if (nvalid >= kSliceCols)
+                        col_accumulate<false>(v, cv, a.scale, nvalid, s2);
+                    else
+                        col_accumulate<true>(v, cv, a.scale, nvalid, s2);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&t.lse_empty[k]);  // colv slot k may be refilled
                 }
                 ++acc_it;
             }
-            if (!ok) break;
-            // merge the two column halves of each lane
-            const float s_half = (s2[0].x + s2[0].y) + (s2[1].x + s2[1].y) + (s2[2].x + s2[2].y) + (s2[3].x + s2[3].y);
-            t.red[half][r_local][0] = m_run;
-            t.red[half][r_local][1] = s_half;
+            if (!(ok = epi_bar_and(ok))) break;
+            // merge the column slices of each lane, in slice order
+            const float s_part = (s2[0].x + s2[0].y) + (s2[1].x + s2[1].y) + (s2[2].x + s2[2].y) + (s2[3].x + s2[3].y);
+            t.red[slice][r_local][0] = m_run;
+            t.red[slice][r_local][1] = s_part;
             epi_bar();
-            if (half == 0) {
+            if (slice == 0) {
                 if (a.mode == 0) {
                     const int row = ta * BM + r_local;
+                    if (row >= a.rows_g && row < a.rows_pad) a.lse2[(int64_t)lg * a.rows_pad + row] = INFINITY;
                     if (row < a.rows_g) {
-                        const float m0 = t.red[0][r_local][0], m1 = t.red[1][r_local][0];
-                        const float m = fmaxf(m0, m1);
-                        float s = 0.f;
-                        if (m != -INFINITY) s = t.red[0][r_local][1] * ex2(m0 - m) + t.red[1][r_local][1] * ex2(m1 - m);
-                        a.lse2[(int64_t)lg * a.rows_g + row] = s > 0.f ? m + __log2f(s) : -INFINITY;
+                        float m = -INFINITY;
+#pragma unroll
+                        for (int j = 0; j < kSlices; ++j) m = fmaxf(m, t.red[j][r_local][0]);
+                        float sum = 0.f;
+                        if (m != -INFINITY) {
+#pragma unroll
+                            for (int j = 0; j < kSlices; ++j) sum += t.red[j][r_local][1] * ex2(t.red[j][r_local][0] - m);
+                        }
+                        a.lse2[(int64_t)lg * a.rows_pad + row] = sum > 0.f ? m + __log2f(sum) : -INFINITY;
                     }
                 } else {
                     const int b = a.c0 + ta * BM + r_local;
-                    if (b < a.c1) a.mass[(int64_t)lg * a.n_blocks + b] = t.red[0][r_local][1] + t.red[1][r_local][1];
+                    if (b < a.c1) {
+                        float sum = 0.f;
+#pragma unroll
+                        for (int j = 0; j < kSlices; ++j) sum += t.red[j][r_local][1];
+                        a.mass[(int64_t)lg * a.n_blocks + b] = sum;
+                    }
                 }
             }
             epi_bar();
@@ -482,7 +578,8 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_ro
 }  // namespace
 
 size_t block_scores_workspace(int L, int Hq, int Hkv, int M, int n_blocks) {
-    return align256((size_t)L * Hq * M * sizeof(float)) + align256((size_t)L * Hkv * n_blocks * sizeof(float));
+    const size_t rows_pad = (((size_t)(Hq / Hkv) * M + 3) & ~(size_t)3);
+    return align256((size_t)L * Hkv * rows_pad * sizeof(float)) + align256((size_t)L * Hkv * n_blocks * sizeof(float));
 }
 
 cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index, int L, int Hq, int Hkv, int M, int D,
@@ -497,7 +594,8 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
     const int LH = L * Hkv;
     char* w = static_cast<char*>(ws);
     float* lse2 = reinterpret_cast<float*>(w);
-    w += align256((size_t)L * Hq * M * sizeof(float));
+    const int rows_pad = (rows_g + 3) & ~3;
+    w += align256((size_t)LH * rows_pad * sizeof(float));
     float* mass = R_partial ? R_partial : reinterpret_cast<float*>(w);
 
     if (ncand > 0) {
@@ -511,6 +609,7 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
         if (e != cudaSuccess) return e;
         TcArgs a;
         a.rows_g = rows_g;
+        a.rows_pad = rows_pad;
         a.c0 = c0;
         a.c1 = c1;
         a.Bcap = Bcap;

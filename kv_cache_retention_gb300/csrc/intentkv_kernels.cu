@@ -3,56 +3,31 @@
 //
 // Rule scores run in three launches so that K is read from HBM exactly once:
 //   1. rule_logits: one sweep over the K rows of every (layer, candidate
-//      token).  Each 32-byte piece of a K row is loaded once into registers and
-//      multiplied against the G = Hq/Hkv query heads that share its kv head
-//      (GQA reuse), the per-head partial dot products are summed across the
-//      D/16 lanes of the head with a halving shuffle exchange, and the logits
-//      (pre-scaled into the exp2 domain) go through a shared-memory tile to
-//      coalesced stores.  Each lane keeps an online (max, sum 2^(z-max)) per
-//      head it owns; a block merges them per chunk of tokens.
+//      token).  A producer warp looks each token up in the slot map (kept in
+//      shared memory one 256-token chunk ahead) and copies
+//      its whole K row (all kv heads, contiguous in the pool) into a 4-stage
+//      shared-memory ring with one bulk asynchronous copy (cp.async.bulk,
+//      L2 evict-first) completing on an mbarrier; 12 consumer warps read 32-byte
+//      pieces of the rows and multiply each against the G = Hq/Hkv query heads
+//      that share its kv head (GQA reuse, packed fp32x2 FMA, M in registers).
+//      The per-head partial dot products are summed across the D/16 lanes of
+//      the head with a halving shuffle exchange, and the logits (pre-scaled into
+//      the exp2 domain) go through a shared-memory tile to coalesced stores.
+//      At every tile flush one warp per head reduces the tile's (max, sum
+//      2^(z-max)) and merges it into the chunk's; one pair per (l, h, 256-token
+//      chunk) goes to global memory.
 //   2. rule_lse: merges the chunk partials into log2-sum-exp per (l,h).
 //   3. rule_accum: rule[j] = sum_{l,h} 2^(z - lse), a token-parallel pass over
 //      the logits (coalesced along j), reduced across warps in a fixed order.
 #include <cuda_bf16.h>
 
 #include "kvsel_internal.h"
+#include "ptx_sm100.cuh"
 
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kRuleThreads = 256;
-constexpr int kZTile = 64;       // tokens per shared-memory logit tile
-constexpr int kChunkTiles = 2;   // tiles per work item (chunk = 128 tokens)
 constexpr unsigned kFull = 0xffffffffu;
-
-__device__ __forceinline__ uint64_t policy_evict_first() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-__device__ __forceinline__ uint64_t policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-// 32 contiguous bytes, read-only path, not allocated in L1, evict-first in L2;
-// one 256-bit load when the address is 32-byte aligned, else two 128-bit loads.
-__device__ __forceinline__ void load32(const void* ptr, uint32_t* r, uint64_t pol, bool aligned32) {
-    if (aligned32) {
-        asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
-                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                       "=r"(r[7])
-                     : "l"(ptr), "l"(pol));
-    } else {
-        asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.b32 {%0,%1,%2,%3}, [%4], %5;"
-                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                     : "l"(ptr), "l"(pol));
-        asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.b32 {%0,%1,%2,%3}, [%4], %5;"
-                     : "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-                     : "l"(static_cast<const char*>(ptr) + 16), "l"(pol));
-    }
-}
 
 __device__ __forceinline__ void store_f32_hint(float* ptr, float v, uint64_t pol) {
     asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(ptr), "f"(v), "l"(pol) : "memory");
@@ -60,6 +35,12 @@ __device__ __forceinline__ void store_f32_hint(float* ptr, float v, uint64_t pol
 
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // Merge two (max, sum) pairs of an exp2-domain log-sum-exp.
@@ -151,203 +132,203 @@ struct RuleArgs {
     const int32_t* slot_map;
     int n_slots;
     int L, Hq, Hkv, N, D;
-    int64_t layer_stride, slot_stride;
+    int64_t layer_stride, slot_stride;  // in elements
     const float* M;
     int pi, q_s, q_e;
-    float scale;   // log2(e) / sqrt(D)
-    int n_chunks;  // chunks per layer (chunk = kZTile * kChunkTiles tokens)
-    float* z;      // [L][Hq][N]
-    float2* part;  // [L][Hq][n_chunks]
+    float scale;       // log2(e) / sqrt(D)
+    int n_sub;         // 64-token sub-chunks per layer
+    int R;             // sub-chunks per work item (so that Hkv*R tasks fill the block's warps)
+    int n_items;       // L * ceil(n_sub / R)
+    int items_per_block;
+    float* z;          // [L][Hq][N]
+    float2* part;      // [L][Hq][n_sub]
     unsigned* dev_err;
-    bool aligned32;  // pool base and strides allow 32-byte loads
+    bool aligned32;    // pool base, layer and slot strides are 32-byte aligned
 };
 
-__host__ __device__ constexpr int next_pow2(int g) { return g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 8; }
+constexpr int kWarps = 8;                 // warps per block; a warp owns one kv head of an item's tokens
+constexpr int kSub = 64;                  // tokens per task: lane t takes tokens t and t + 32
 
-// Thread layout: S = D/16 lanes per kv head (16 dims each), TT = Hkv*S lanes per
-// token, P = 256/TT tokens per pass.  A lane owns (token slot tp, kv head g,
-// dims [16s, 16s+16)) and keeps those dims of the G query heads' M in registers.
+// 32 contiguous bytes: one 256-bit load when the address is 32-byte aligned
+// (aligned32), else two 128-bit loads (the pool is only required to be 16-byte
+// aligned).
+__device__ __forceinline__ void ldg32(const void* p, uint32_t* r, bool aligned32) {
+    if (aligned32) {
+        asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                       "=r"(r[7])
+                     : "l"(p));
+    } else {
+        asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                     : "l"(p));
+        asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                     : "l"(static_cast<const char*>(p) + 16));
+    }
+}
+
+// Lane-level online (max, sum 2^(z-max)) update.
+__device__ __forceinline__ void stat_add(float z, float& m, float& s) {
+    if (z > m) {
+        s = s * fast_exp2(m - z) + 1.f;
+        m = z;
+    } else {
+        s += fast_exp2(z - m);
+    }
+}
+
+// One warp task = (kv head g, 64 tokens): lane t owns tokens t and t+32 for all
+// D dims of head g and all G query heads sharing it.  The layer's M sits in
+// shared memory and every lane of the warp reads the same M entries, so the
+// reads are broadcasts; K comes straight from the pool with 32-byte loads.
+// Per-lane online statistics of each head are merged across the warp once per
+// contiguous run of chunks of one layer.
 template <int G, bool BF16>
-__global__ void __launch_bounds__(kRuleThreads, 2) rule_logits_kernel(const RuleArgs a) {
-    constexpr int P2 = next_pow2(G);
-    extern __shared__ float smem[];
-    const int S = a.D >> 4;
-    const int TT = a.Hkv * S;
-    const int P = kRuleThreads / TT;
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int tp = tid / TT;                 // token slot in a pass (>= P: idle)
-    const int g = (tid % TT) / S;            // kv head
-    const int s = tid % S;                   // 16-dim slice
-    const bool active = tp < P;
-    const int Hq = a.Hq;
-    const int zpitch = Hq + 1;
-    float* ztile = smem;                                  // [kZTile][Hq+1]
-    float* red_m = ztile + kZTile * zpitch;               // [P][Hq]
-    float* red_s = red_m + P * Hq;                        // [P][Hq]
+__global__ void __launch_bounds__(kWarps * 32, 2) rule_logits_kernel(const RuleArgs a) {
+    extern __shared__ __align__(16) float Ms[];  // [Hq][D] of the current layer
+    constexpr int ES = BF16 ? 2 : 4;
+    constexpr int DPP = 32 / ES;                 // dims per 32-byte piece
+    constexpr int BATCH = 4;                     // pieces per token kept in registers at once
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Hq = a.Hq, D = a.D, Hkv = a.Hkv;
+    const int n_pieces = D / DPP;
+    const int tasks = Hkv * a.R;
+    const int item0 = blockIdx.x * a.items_per_block;
+    const int item1 = min(a.n_items, item0 + a.items_per_block);
+    const int items_per_layer = (a.n_sub + a.R - 1) / a.R;
+    const uint64_t pol_z = kvsel_ptx::policy_evict_last();
 
-    // after the shuffle exchange: values per lane, lanes sharing a value
-    const int nv = P2 >= S ? P2 / S : 1;
-    const int nshare = S > P2 ? S / P2 : 1;
-    const bool writer = active && (s % nshare) == 0;
+    int cur_l = -1;
+    // running stats of this warp's current task head, per query head of the group
+    float sm[G], ss[G];
+    int run_sub0 = 0, run_g = -1, run_l = -1;
 
-    const uint64_t pol_k = policy_evict_first();
-    const uint64_t pol_z = policy_evict_last();
-    const int chunk_len = kZTile * kChunkTiles;
-    const int total_items = a.L * a.n_chunks;
-
-    for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-        const int l = item / a.n_chunks;
-        const int chunk = item % a.n_chunks;
-        const int j_begin = chunk * chunk_len;
-        const int j_end = min(a.N, j_begin + chunk_len);
-
-        // M slice for the G query heads of kv head g, dims [16s, 16s+16)
-        float m_reg[G][16];
+    auto flush_run = [&]() {
+        // merge the lanes' (max, sum) per head and store at the run's first sub-chunk
+        if (run_g < 0) return;
 #pragma unroll
         for (int i = 0; i < G; ++i) {
-            const float* mp = a.M + ((int64_t)l * Hq + (int64_t)g * G + i) * a.D + 16 * s;
+            float2 acc = make_float2(sm[i], ss[i]);
 #pragma unroll
-            for (int k = 0; k < 16; k += 4) {
-                float4 v = active ? __ldg(reinterpret_cast<const float4*>(mp + k)) : make_float4(0, 0, 0, 0);
-                m_reg[i][k] = v.x;
-                m_reg[i][k + 1] = v.y;
-                m_reg[i][k + 2] = v.z;
-                m_reg[i][k + 3] = v.w;
+            for (int o = 16; o; o >>= 1)
+                acc = lse_merge(acc, make_float2(__shfl_xor_sync(kFull, acc.x, o), __shfl_xor_sync(kFull, acc.y, o)));
+            if (lane == 0) a.part[((int64_t)run_l * Hq + run_g * G + i) * a.n_sub + run_sub0] = acc;
+        }
+        run_g = -1;
+    };
+
+    for (int item = item0; item < item1; ++item) {
+        const int l = item / items_per_layer, ci = item % items_per_layer;
+        if (l != cur_l) {
+            __syncthreads();
+            for (int idx = threadIdx.x; idx < Hq * D / 4; idx += blockDim.x)
+                reinterpret_cast<float4*>(Ms)[idx] = __ldg(reinterpret_cast<const float4*>(a.M + (int64_t)l * Hq * D) + idx);
+            __syncthreads();
+            cur_l = l;
+        }
+        const char* layer = reinterpret_cast<const char*>(a.k_pool) + (size_t)l * a.layer_stride * ES;
+        for (int task = warp; task < tasks; task += kWarps) {
+            const int g = task % Hkv;
+            const int sub = ci * a.R + task / Hkv;
+            if (sub >= a.n_sub) continue;
+            if (run_g != g || run_l != l) {
+                flush_run();
+                run_g = g;
+                run_l = l;
+                run_sub0 = sub;
+#pragma unroll
+                for (int i = 0; i < G; ++i) {
+                    sm[i] = -INFINITY;
+                    ss[i] = 0.f;
+                }
+            } else if (lane < G) {
+                // sub-chunks merged into the run's first entry carry an empty partial
+                a.part[((int64_t)l * Hq + g * G + lane) * a.n_sub + sub] = make_float2(-INFINITY, 0.f);
             }
-        }
-        float run_m[P2 > 1 ? P2 : 1], run_s[P2 > 1 ? P2 : 1];
+            // the lane's two tokens
+            const char* row[2];
+            bool cand[2];
 #pragma unroll
-        for (int k = 0; k < P2; ++k) {
-            run_m[k] = -INFINITY;
-            run_s[k] = 0.f;
-        }
-        int my_base = 0;  // first local head index this lane holds after the exchange
-
-        const char* layer_base = reinterpret_cast<const char*>(a.k_pool) +
-                                 ((int64_t)l * a.layer_stride + (int64_t)g * a.D + 16 * s) * (BF16 ? 2 : 4);
-
-        for (int t0 = j_begin; t0 < j_end; t0 += kZTile) {
-            for (int pb = 0; pb < kZTile; pb += 2 * P) {
-                uint32_t raw[2][BF16 ? 8 : 16];
-                bool cand[2];
+            for (int u = 0; u < 2; ++u) {
+                const int j = sub * kSub + u * 32 + lane;
+                cand[u] = j < a.N && !is_forced(j, a.pi, a.q_s, a.q_e);
+                row[u] = nullptr;
+                if (cand[u]) {
+                    const int64_t slot = a.slot_map ? (int64_t)__ldg(a.slot_map + j) : (int64_t)j;
+                    if (slot < 0 || slot >= a.n_slots) {
+                        atomicOr(a.dev_err, (unsigned)KVSEL_DEV_BAD_SLOT);  // read as a zero row
+                    } else {
+                        row[u] = layer + ((size_t)slot * a.slot_stride + (size_t)g * D) * ES;
+                    }
+                }
+            }
+            float2 acc[2][G];
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int tl = pb + u * P + tp;
-                    const int j = t0 + tl;
-                    cand[u] = active && tl < kZTile && j < j_end && !is_forced(j, a.pi, a.q_s, a.q_e);
+            for (int u = 0; u < 2; ++u)
 #pragma unroll
-                    for (int k = 0; k < (BF16 ? 8 : 16); ++k) raw[u][k] = 0u;
-                    if (cand[u]) {
-                        int64_t slot = a.slot_map ? (int64_t)__ldg(a.slot_map + j) : (int64_t)j;
-                        if (slot < 0 || slot >= a.n_slots) {
-                            atomicOr(a.dev_err, (unsigned)KVSEL_DEV_BAD_SLOT);
+                for (int i = 0; i < G; ++i) acc[u][i] = make_float2(0.f, 0.f);
+            for (int p0 = 0; p0 < n_pieces; p0 += BATCH) {
+                uint32_t raw[2][BATCH][8];
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int q = 0; q < BATCH; ++q) {
+                        if (row[u] && p0 + q < n_pieces) {
+                            ldg32(row[u] + (size_t)(p0 + q) * 32, raw[u][q], a.aligned32);
                         } else {
-                            const char* p = layer_base + slot * a.slot_stride * (BF16 ? 2 : 4);
-                            load32(p, &raw[u][0], pol_k, a.aligned32);
-                            if constexpr (!BF16) load32(p + 32, &raw[u][8], pol_k, a.aligned32);
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) raw[u][q][k] = 0u;
+                        }
+                    }
+#pragma unroll
+                for (int q = 0; q < BATCH; ++q) {
+                    if (p0 + q >= n_pieces) break;
+                    const int d0 = (p0 + q) * DPP;
+#pragma unroll
+                    for (int w = 0; w < 8; w += (BF16 ? 2 : 4)) {
+                        // 4 dims of K for both tokens
+                        float2 k01[2], k23[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            if constexpr (BF16) {
+                                k01[u] = bf16x2_to_float2(raw[u][q][w]);
+                                k23[u] = bf16x2_to_float2(raw[u][q][w + 1]);
+                            } else {
+                                k01[u] = make_float2(__uint_as_float(raw[u][q][w]), __uint_as_float(raw[u][q][w + 1]));
+                                k23[u] = make_float2(__uint_as_float(raw[u][q][w + 2]), __uint_as_float(raw[u][q][w + 3]));
+                            }
+                        }
+                        const int d = d0 + (BF16 ? 2 * w : w);
+#pragma unroll
+                        for (int i = 0; i < G; ++i) {
+                            const float4 m4 = *reinterpret_cast<const float4*>(&Ms[(g * G + i) * D + d]);
+                            const float2 m01 = make_float2(m4.x, m4.y), m23 = make_float2(m4.z, m4.w);
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                acc[u][i] = __ffma2_rn(m01, k01[u], acc[u][i]);
+                                acc[u][i] = __ffma2_rn(m23, k23[u], acc[u][i]);
+                            }
                         }
                     }
                 }
+            }
+            // logits: coalesced along tokens; statistics per lane
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    float x[16];
-                    if constexpr (BF16) {
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            float2 f = bf16x2_to_float2(raw[u][k]);
-                            x[2 * k] = f.x;
-                            x[2 * k + 1] = f.y;
-                        }
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) x[k] = __uint_as_float(raw[u][k]);
-                    }
-                    float v[P2];
-#pragma unroll
-                    for (int i = 0; i < P2; ++i) v[i] = 0.f;
+            for (int u = 0; u < 2; ++u) {
+                const int j = sub * kSub + u * 32 + lane;
+                if (j < a.N) {
 #pragma unroll
                     for (int i = 0; i < G; ++i) {
-                        float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-                        for (int k = 0; k < 16; k += 2)
-                            acc = __ffma2_rn(make_float2(m_reg[i][k], m_reg[i][k + 1]), make_float2(x[k], x[k + 1]), acc);
-                        v[i] = acc.x + acc.y;
-                    }
-                    // halving exchange across the S lanes of the head: at each level a
-                    // lane keeps half of its values and receives the partner's copy of
-                    // that half, so the per-lane shuffle count falls with the level.
-                    int base = 0;
-#pragma unroll
-                    for (int lev = 0; lev < 5; ++lev) {
-                        const int o = S >> (lev + 1);
-                        if (o == 0) break;
-                        const int cur = P2 >> lev;
-                        if (cur > 1) {
-                            const int half = cur >> 1;
-                            const bool up = (lane & o) != 0;
-#pragma unroll
-                            for (int k = 0; k < (P2 >> (lev + 1) > 0 ? P2 >> (lev + 1) : 1); ++k) {
-                                if (k < half) {
-                                    float send = up ? v[k] : v[k + half];
-                                    float keep = up ? v[k + half] : v[k];
-                                    v[k] = keep + __shfl_xor_sync(kFull, send, o);
-                                }
-                            }
-                            if (up) base += half;
-                        } else {
-                            v[0] += __shfl_xor_sync(kFull, v[0], o);
-                        }
-                    }
-                    my_base = base;
-                    const int tl = pb + u * P + tp;
-                    if (writer && tl < kZTile && t0 + tl < j_end) {
-#pragma unroll
-                        for (int k = 0; k < P2; ++k) {
-                            if (k < nv && base + k < G) {
-                                const float zz = cand[u] ? v[k] * a.scale : -INFINITY;
-                                ztile[tl * zpitch + g * G + base + k] = zz;
-                                if (cand[u]) {
-                                    if (zz > run_m[k]) {
-                                        run_s[k] = run_s[k] * exp2f(run_m[k] - zz) + 1.f;
-                                        run_m[k] = zz;
-                                    } else {
-                                        run_s[k] += exp2f(zz - run_m[k]);
-                                    }
-                                }
-                            }
-                        }
+                        const float z = cand[u] ? (acc[u][i].x + acc[u][i].y) * a.scale : -INFINITY;
+                        store_f32_hint(a.z + ((int64_t)l * Hq + g * G + i) * a.N + j, z, pol_z);
+                        if (cand[u]) stat_add(z, sm[i], ss[i]);
                     }
                 }
             }
-            __syncthreads();
-            // coalesced store of the tile: rows h, tokens t0 .. t0+kZTile
-            const int tile_n = min(kZTile, j_end - t0);
-            for (int idx = tid; idx < Hq * kZTile; idx += kRuleThreads) {
-                const int h = idx / kZTile, t = idx % kZTile;
-                if (t < tile_n)
-                    store_f32_hint(a.z + ((int64_t)l * Hq + h) * a.N + t0 + t, ztile[t * zpitch + h], pol_z);
-            }
-            __syncthreads();
         }
-        // merge the lanes' running (max, sum) per head for this chunk
-        if (writer) {
-#pragma unroll
-            for (int k = 0; k < P2; ++k) {
-                if (k < nv && my_base + k < G) {
-                    red_m[tp * Hq + g * G + my_base + k] = run_m[k];
-                    red_s[tp * Hq + g * G + my_base + k] = run_s[k];
-                }
-            }
-        }
-        __syncthreads();
-        for (int h = tid; h < Hq; h += kRuleThreads) {
-            float2 acc = make_float2(-INFINITY, 0.f);
-            for (int t = 0; t < P; ++t) acc = lse_merge(acc, make_float2(red_m[t * Hq + h], red_s[t * Hq + h]));
-            a.part[((int64_t)l * Hq + h) * a.n_chunks + chunk] = acc;
-        }
-        __syncthreads();
     }
+    flush_run();
 }
 
 // ---------------------------------------------------------------------------
@@ -417,7 +398,7 @@ cudaError_t launch_logits(const RuleArgs& a, int grid, size_t smem, cudaStream_t
                                              (int)smem);
         if (e != cudaSuccess) return e;
     }
-    rule_logits_kernel<G, BF16><<<grid, kRuleThreads, smem, s>>>(a);
+    rule_logits_kernel<G, BF16><<<grid, kWarps * 32, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -436,10 +417,7 @@ cudaError_t dispatch_logits(int G, const RuleArgs& a, int grid, size_t smem, cud
     return cudaErrorInvalidValue;
 }
 
-int rule_chunks(int N) {
-    const int chunk_len = kZTile * kChunkTiles;
-    return (N + chunk_len - 1) / chunk_len;
-}
+int rule_chunks(int N) { return (N + kSub - 1) / kSub; }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -493,27 +471,31 @@ cudaError_t launch_rule_scores(kvsel_ctx* ctx, const void* k_pool, int dtype, co
     a.q_s = q_s;
     a.q_e = q_e;
     a.scale = kLog2e / sqrtf((float)D);
-    a.n_chunks = rule_chunks(N);
+    a.n_sub = rule_chunks(N);
     a.z = reinterpret_cast<float*>(w);
     w += align256(rows * N * sizeof(float));
     a.part = reinterpret_cast<float2*>(w);
-    w += align256(rows * a.n_chunks * sizeof(float2));
+    w += align256(rows * a.n_sub * sizeof(float2));
     float* lse2 = reinterpret_cast<float*>(w);
     a.dev_err = ctx->dev_err;
-    const int64_t es = dtype == KVSEL_BF16 ? 2 : 4;
-    a.aligned32 = (reinterpret_cast<uintptr_t>(k_pool) % 32 == 0) && (layer_stride * es) % 32 == 0 &&
-                  (slot_stride * es) % 32 == 0;
-
+    {
+        const int64_t es = dtype == KVSEL_BF16 ? 2 : 4;  // row offsets g*D*es are multiples of 32 for D >= 16
+        a.aligned32 = reinterpret_cast<uintptr_t>(k_pool) % 32 == 0 && (layer_stride * es) % 32 == 0 &&
+                      (slot_stride * es) % 32 == 0;
+    }
+    a.R = Hkv >= kWarps ? 1 : kWarps / Hkv;
+    const int items_per_layer = (a.n_sub + a.R - 1) / a.R;
+    a.n_items = L * items_per_layer;
     const int G = Hq / Hkv;
-    const int TT = Hkv * (D / 16);
-    const int P = kRuleThreads / TT;
-    const size_t smem = sizeof(float) * ((size_t)kZTile * (Hq + 1) + 2 * (size_t)P * Hq);
-    const int items = L * a.n_chunks;
-    const int grid = items < 2 * ctx->num_sms ? items : 2 * ctx->num_sms;
+    const size_t smem = sizeof(float) * (size_t)Hq * D;
+    int blocks_per_sm = 2;
+    const int grid_max = blocks_per_sm * ctx->num_sms;
+    a.items_per_block = (a.n_items + grid_max - 1) / grid_max;
+    const int grid = (a.n_items + a.items_per_block - 1) / a.items_per_block;
     cudaError_t e = dtype == KVSEL_BF16 ? dispatch_logits<true>(G, a, grid, smem, s)
                                         : dispatch_logits<false>(G, a, grid, smem, s);
     if (e != cudaSuccess) return e;
-    rule_lse_kernel<<<(int)((rows * 32 + 255) / 256), 256, 0, s>>>(a.part, (int)rows, a.n_chunks, lse2);
+    rule_lse_kernel<<<(int)((rows * 32 + 255) / 256), 256, 0, s>>>(a.part, (int)rows, a.n_sub, lse2);
     const size_t smem3 = rows * sizeof(float);
     if (smem3 > 48 * 1024)
         cudaFuncSetAttribute(rule_accum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);

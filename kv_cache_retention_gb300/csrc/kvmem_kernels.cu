@@ -156,43 +156,77 @@ __global__ void __launch_bounds__(256) meank_kernel(const __nv_bfloat16* __restr
     }
 }
 
-// One block per (entry i, layer l).  Thread idx covers 16 bytes of the page:
-// row r = t*Hkv + g, chunk c; source and destination rows are contiguous.
+// One block per (entry i, group of kLayerGroup layers).  The block first fills
+// a shared [page][D/2] table of (cos, sin) for positions dst_pos0[i] + t (the
+// same for every layer and kv head), then moves the page: a lane owns one
+// rotation pair of 16-byte chunks of a row -- chunks c and c + D/16, i.e. the
+// NeoX halves (i, i + D/2) of 8 frequencies, or two chunks of interleaved
+// pairs -- so no data crosses lanes.  Rows r = t*Hkv + g are contiguous in the
+// destination page; each source row is contiguous too.
+constexpr int kLayerGroup = 8;
+
 __global__ void __launch_bounds__(256) rerope_kernel(const __nv_bfloat16* __restrict__ k_src, int64_t sls, int64_t shs,
                                                      int src_tokens, const int32_t* __restrict__ src_block,
                                                      const int32_t* __restrict__ dst_page,
                                                      const int32_t* __restrict__ dst_pos0, int L, int Hkv, int D,
                                                      int page, const float2* tlo, const float2* thi, int style,
                                                      __nv_bfloat16* __restrict__ pool, int P, unsigned* dev_err) {
-    const int i = blockIdx.x / L, l = blockIdx.x % L;
+    extern __shared__ float2 cs[];  // [page][D/2]
+    const int i = blockIdx.x;
+    const int l0 = blockIdx.y * kLayerGroup, l1 = min(L, l0 + kLayerGroup);
     const int sb = __ldg(src_block + i), dp = __ldg(dst_page + i), p0 = __ldg(dst_pos0 + i);
     const bool ok_src = sb >= 0 && (int64_t)(sb + 1) * page <= src_tokens;
     const bool ok_dst = dp >= 0 && dp < P;
     const bool ok_pos = p0 >= 0 && (int64_t)p0 + page <= KVSEL_MAX_POS;
     if (!(ok_src && ok_dst && ok_pos)) {
-        if (threadIdx.x == 0)
+        if (threadIdx.x == 0 && blockIdx.y == 0)
             atomicOr(dev_err, (ok_src ? 0u : (unsigned)KVSEL_DEV_BAD_BLOCK) | (ok_dst ? 0u : (unsigned)KVSEL_DEV_BAD_PAGE) |
                                   (ok_pos ? 0u : (unsigned)KVSEL_DEV_BAD_POSITION));
         return;  // whole block leaves together
     }
-    const int LR = D >> 3;
-    const int total = page * Hkv * LR;
-    const __nv_bfloat16* src_l = k_src + (int64_t)l * sls + (int64_t)sb * page * D;
-    __nv_bfloat16* dst = pool + ((int64_t)l * P + dp) * (int64_t)page * Hkv * D;
-    for (int base = 0; base < total; base += blockDim.x) {  // uniform trip count: rotate8 shuffles
-        const int idx = base + threadIdx.x;
-        const bool valid = idx < total;
-        const int c = idx % LR, r = idx / LR;
-        const int t = r / Hkv, g = r % Hkv;
-        float x[8];
-        if (valid) {
-            unpack8(__ldcs(reinterpret_cast<const uint4*>(src_l + (int64_t)g * shs + (int64_t)t * D + 8 * c)), x);
-        } else {
+    const int half = D / 2;
+    for (int idx = threadIdx.x; idx < page * half; idx += blockDim.x)
+        cs[idx] = rope_cs(tlo, thi, half, p0 + idx / half, idx % half);
+    __syncthreads();
+    const int PR = D >> 4;              // chunk pairs per row
+    const int total = page * Hkv * PR;
+    for (int l = l0; l < l1; ++l) {
+        const __nv_bfloat16* src_l = k_src + (int64_t)l * sls + (int64_t)sb * page * D;
+        __nv_bfloat16* dst = pool + ((int64_t)l * P + dp) * (int64_t)page * Hkv * D;
+        for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+            const int cp = idx % PR, r = idx / PR;
+            const int t = r / Hkv, g = r % Hkv;
+            const __nv_bfloat16* srow = src_l + (int64_t)g * shs + (int64_t)t * D;
+            __nv_bfloat16* drow = dst + (int64_t)r * D;
+            const float2* cst = cs + t * half;
+            // NeoX: chunk cp holds dims 8cp.. (first half), chunk cp + PR holds dims 8cp + D/2..
+            // interleaved: chunks cp and cp + PR each hold 4 adjacent pairs
+            const int ca = cp, cb = cp + PR;
+            float xa[8], xb[8];
+            unpack8(__ldcs(reinterpret_cast<const uint4*>(srow + 8 * ca)), xa);
+            unpack8(__ldcs(reinterpret_cast<const uint4*>(srow + 8 * cb)), xb);
+            if (style == KVSEL_ROPE_NEOX) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) x[k] = 0.f;
+                for (int k = 0; k < 8; ++k) {
+                    const float2 c = cst[8 * cp + k];
+                    const float a = xa[k], b = xb[k];
+                    xa[k] = fmaf(a, c.x, -b * c.y);
+                    xb[k] = fmaf(b, c.x, a * c.y);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; k += 2) {
+                    const float2 c1 = cst[4 * ca + k / 2], c2 = cst[4 * cb + k / 2];
+                    const float a1 = xa[k], b1 = xa[k + 1], a2 = xb[k], b2 = xb[k + 1];
+                    xa[k] = fmaf(a1, c1.x, -b1 * c1.y);
+                    xa[k + 1] = fmaf(b1, c1.x, a1 * c1.y);
+                    xb[k] = fmaf(a2, c2.x, -b2 * c2.y);
+                    xb[k + 1] = fmaf(b2, c2.x, a2 * c2.y);
+                }
+            }
+            __stcs(reinterpret_cast<uint4*>(drow + 8 * ca), pack8(xa));
+            __stcs(reinterpret_cast<uint4*>(drow + 8 * cb), pack8(xb));
         }
-        rotate8(x, c, LR, D, valid ? p0 + t : 0, false, style, tlo, thi);
-        if (valid) __stcs(reinterpret_cast<uint4*>(dst + (int64_t)idx * 8), pack8(x));
     }
 }
 
@@ -222,8 +256,13 @@ cudaError_t launch_rerope(const void* k_src, int64_t sls, int64_t shs, int src_t
                           const int32_t* dst_page, const int32_t* dst_pos0, int n, int L, int Hkv, int D, int page,
                           const kvsel_ctx::RopeTab* tab, int rope_style, void* pool, int P, unsigned* dev_err,
                           cudaStream_t s) {
-    const int64_t grid = (int64_t)n * L;
-    rerope_kernel<<<(unsigned)grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(k_src), sls, shs, src_tokens,
+    const dim3 grid((unsigned)n, (unsigned)((L + kLayerGroup - 1) / kLayerGroup));
+    const size_t smem = sizeof(float2) * (size_t)page * (D / 2);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(rerope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    rerope_kernel<<<grid, 256, smem, s>>>(static_cast<const __nv_bfloat16*>(k_src), sls, shs, src_tokens,
                                                  src_block, dst_page, dst_pos0, L, Hkv, D, page, tab->lo, tab->hi,
                                                  rope_style, static_cast<__nv_bfloat16*>(pool), P, dev_err);
     return cudaGetLastError();

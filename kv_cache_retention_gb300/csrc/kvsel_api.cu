@@ -291,6 +291,7 @@ int kvsel_rerope_scatter(kvsel_ctx* ctx, const void* k_src, int64_t src_layer_st
     if (!k_src || !src_block || !dst_page || !dst_pos0 || !pool) return fail(ctx, KVSEL_ERR_INVALID_ARG, "rerope_scatter: null pointer");
     if (n < 0 || L <= 0 || Hkv <= 0 || page <= 0 || P <= 0 || src_tokens < 0) return fail(ctx, KVSEL_ERR_SHAPE, "rerope_scatter: bad sizes");
     if (!pow2_head_dim(D)) return fail(ctx, KVSEL_ERR_UNSUPPORTED, "rerope_scatter: D=%d unsupported", D);
+    if ((int64_t)page * D > 16384) return fail(ctx, KVSEL_ERR_UNSUPPORTED, "rerope_scatter: page*D=%lld > 16384", (long long)page * D);
     if (rope_style != KVSEL_ROPE_NEOX && rope_style != KVSEL_ROPE_INTERLEAVED) return fail(ctx, KVSEL_ERR_INVALID_ARG, "rerope_scatter: bad rope_style");
     if (!(rope_base > 1.0)) return fail(ctx, KVSEL_ERR_INVALID_ARG, "rerope_scatter: rope_base must be > 1");
     if (src_head_stride < (int64_t)src_tokens * D || src_layer_stride < 0) return fail(ctx, KVSEL_ERR_SHAPE, "rerope_scatter: head stride < src_tokens*D");

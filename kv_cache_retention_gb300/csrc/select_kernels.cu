@@ -1,14 +1,21 @@
 // Budgeted top-k with a forced set (IntentKV Sec. 3.1, Eq. 1), also used for
 // the KVMEM working set (sink + recent blocks forced, top-R_b candidates).
 //
-// One 1024-thread block: four 8-bit radix passes over order-preserving
-// uint32 keys find the need-th largest candidate key (the threshold); a final
-// pass keeps every forced position, every candidate above the threshold, and
-// the lowest-index candidates equal to it until `need` are taken; block-wide
-// exclusive scans over per-thread contiguous index ranges write the kept
-// indices in ascending order.  The keep set is therefore a pure function of
-// the scores: ties resolve to the lower index, NaN ranks lowest, -0 == +0.
+// Four 8-bit radix passes over order-preserving uint32 keys find the need-th
+// largest candidate key (the threshold); a final pass keeps every forced
+// position, every candidate above the threshold, and the lowest-index
+// candidates equal to it until `need` are taken; exclusive scans over
+// per-thread contiguous index ranges write the kept indices in ascending order.
+// The keep set is therefore a pure function of the scores: ties resolve to the
+// lower index, NaN ranks lowest, -0 == +0.
+//
+// N <= 131072 (every workload here): one cluster of 8 CTAs, keys in registers.
+// Larger N: one 1024-thread block re-reading the scores for each pass.
+#include <cooperative_groups.h>
+
 #include "kvsel_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace {
 
@@ -169,10 +176,165 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict_
     }
 }
 
+// ---------------------------------------------------------------------------
+// Cluster variant: 8 CTAs x 1024 threads, each thread holding up to kKeys keys
+// of a contiguous index range in registers (N <= 8 * 1024 * kKeys).  Each radix
+// pass builds per-CTA histograms in shared memory; every CTA then sums the 8
+// histograms through distributed shared memory and takes the same digit
+// decision.  The ordered compaction uses block scans plus the lower-ranked
+// CTAs' totals read through distributed shared memory.  Cluster barriers are
+// hardware barriers: no thread spins.
+// ---------------------------------------------------------------------------
+constexpr int kCluster = 8;
+constexpr int kKeys = 16;
+constexpr int kClusterCap = kCluster * kThreads * kKeys;
+
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
+    topk_cluster_kernel(const float* __restrict__ score, int N, int pi, int q_s, int q_e, int need, int n_cand,
+                        uint8_t* __restrict__ keep, int32_t* __restrict__ keep_idx) {
+    __shared__ uint32_t sub[8][256];        // per-warp-group sub-histograms
+    __shared__ uint32_t hist[2][256];       // this CTA's histogram, double-buffered across passes
+    __shared__ uint32_t tot[256];
+    __shared__ int warp_sums[33];
+    __shared__ int cta_tot[2];              // this CTA's (ties, kept) totals
+    __shared__ uint32_t s_prefix, s_remaining;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    // contiguous ranges: CTA rank -> [cb, ce), thread -> [j0, j1)
+    const int per_cta = (N + kCluster - 1) / kCluster;
+    const int cb = min(N, rank * per_cta), ce = min(N, cb + per_cta);
+    const int per_thr = (ce - cb + kThreads - 1) / kThreads;
+    const int j0 = min(ce, cb + tid * per_thr), j1 = min(ce, j0 + per_thr);
+    uint32_t key[kKeys];
+    uint32_t cand_mask = 0;  // bit k: element j0+k is a candidate (not forced)
+#pragma unroll
+    for (int k = 0; k < kKeys; ++k) {
+        const int j = j0 + k;
+        key[k] = 0;
+        if (j < j1) {
+            key[k] = score_key(__ldg(score + j));
+            if (!is_forced(j, pi, q_s, q_e)) cand_mask |= 1u << k;
+        }
+    }
+    const bool select = need > 0 && need < n_cand;
+    const bool keep_all = need >= n_cand;
+    uint32_t prefix = 0, mask = 0, remaining = (uint32_t)need;
+    if (select) {
+        int buf = 0;
+        for (int shift = 24; shift >= 0; shift -= 8, buf ^= 1) {
+            for (int i = tid; i < 8 * 256; i += kThreads) (&sub[0][0])[i] = 0;
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < kKeys; ++k)
+                if (((cand_mask >> k) & 1u) && (key[k] & mask) == prefix)
+                    atomicAdd(&sub[warp & 7][(key[k] >> shift) & 255u], 1u);
+            __syncthreads();
+            if (tid < 256) {
+                uint32_t c = 0;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) c += sub[w][tid];
+                hist[buf][tid] = c;
+            }
+            cluster.sync();  // every CTA's histogram is complete
+            if (tid < 256) {
+                uint32_t c = 0;
+                for (int r = 0; r < kCluster; ++r) c += cluster.map_shared_rank(&hist[buf][0], r)[tid];
+                tot[tid] = c;
+            }
+            __syncthreads();
+            if (warp == 0) {
+                uint32_t cnt[8], lsum = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    cnt[i] = tot[255 - 8 * lane - i];
+                    lsum += cnt[i];
+                }
+                uint32_t incl = lsum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    uint32_t t = __shfl_up_sync(kFull, incl, o);
+                    if (lane >= o) incl += t;
+                }
+                const uint32_t excl = incl - lsum;
+                if (excl < remaining && remaining <= incl) {
+                    uint32_t above = excl;
+                    int digit = 255 - 8 * lane;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (above + cnt[i] >= remaining) {
+                            digit = 255 - 8 * lane - i;
+                            break;
+                        }
+                        above += cnt[i];
+                    }
+                    s_prefix = prefix | ((uint32_t)digit << shift);
+                    s_remaining = remaining - above;
+                }
+            }
+            __syncthreads();
+            prefix = s_prefix;
+            remaining = s_remaining;
+            mask |= 255u << shift;
+        }
+    }
+    const uint32_t thr = prefix;
+
+    // ties equal to the threshold, in global index order
+    int ties = 0;
+    if (select) {
+#pragma unroll
+        for (int k = 0; k < kKeys; ++k) ties += ((cand_mask >> k) & 1u) && key[k] == thr;
+    }
+    int total;
+    int tie_base = block_exclusive_scan(ties, warp_sums, total);
+    if (tid == 0) cta_tot[0] = total;
+    cluster.sync();
+    for (int r = 0; r < rank; ++r) tie_base += cluster.map_shared_rank(&cta_tot[0], r)[0];
+
+    int kept = 0;
+    uint32_t keep_bits = 0;
+    {
+        int tie_rank = tie_base;
+#pragma unroll
+        for (int k = 0; k < kKeys; ++k) {
+            if (j0 + k >= j1) continue;
+            bool kk;
+            if (!((cand_mask >> k) & 1u) || keep_all) {
+                kk = true;
+            } else if (!select) {
+                kk = false;
+            } else {
+                kk = key[k] > thr || (key[k] == thr && (uint32_t)(tie_rank++) < remaining);
+            }
+            keep_bits |= (uint32_t)kk << k;
+            kept += kk;
+        }
+    }
+    int out_base = block_exclusive_scan(kept, warp_sums, total);
+    if (tid == 0) cta_tot[1] = total;
+    cluster.sync();
+    for (int r = 0; r < rank; ++r) out_base += cluster.map_shared_rank(&cta_tot[1], r)[0];
+    int pos = out_base;
+#pragma unroll
+    for (int k = 0; k < kKeys; ++k) {
+        if (j0 + k >= j1) continue;
+        const bool kk = (keep_bits >> k) & 1u;
+        if (keep) keep[j0 + k] = (uint8_t)kk;
+        if (kk && keep_idx) keep_idx[pos] = j0 + k;
+        pos += kk;
+    }
+    cluster.sync();  // no CTA leaves while another may still read its shared memory
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const float* score, int N, int pi, int q_s, int q_e, int need, int n_cand, uint8_t* keep,
                         int32_t* keep_idx, cudaStream_t s) {
-    topk_kernel<<<1, kThreads, 0, s>>>(score, N, pi, q_s, q_e, need, n_cand, keep, keep_idx);
+    if (N <= kClusterCap)
+        topk_cluster_kernel<<<kCluster, kThreads, 0, s>>>(score, N, pi, q_s, q_e, need, n_cand, keep, keep_idx);
+    else
+        topk_kernel<<<1, kThreads, 0, s>>>(score, N, pi, q_s, q_e, need, n_cand, keep, keep_idx);
     return cudaGetLastError();
 }
