@@ -146,8 +146,18 @@ struct RuleArgs {
     bool aligned32;    // pool base, layer and slot strides are 32-byte aligned
 };
 
+#ifndef KVSEL_RULE_TPL
+#define KVSEL_RULE_TPL 2
+#endif
+#ifndef KVSEL_RULE_MINB
+#define KVSEL_RULE_MINB 2
+#endif
+#ifndef KVSEL_RULE_BATCH
+#define KVSEL_RULE_BATCH 2
+#endif
 constexpr int kWarps = 8;                 // warps per block; a warp owns one kv head of an item's tokens
-constexpr int kSub = 64;                  // tokens per task: lane t takes tokens t and t + 32
+constexpr int kTPL = KVSEL_RULE_TPL;      // tokens per lane in a task
+constexpr int kSub = 32 * kTPL;           // tokens per task: lane t takes tokens t, t + 32, ...
 
 // 32 contiguous bytes: one 256-bit load when the address is 32-byte aligned
 // (aligned32), else two 128-bit loads (the pool is only required to be 16-byte
@@ -178,157 +188,233 @@ __device__ __forceinline__ void stat_add(float z, float& m, float& s) {
     }
 }
 
-// One warp task = (kv head g, 64 tokens): lane t owns tokens t and t+32 for all
-// D dims of head g and all G query heads sharing it.  The layer's M sits in
-// shared memory and every lane of the warp reads the same M entries, so the
-// reads are broadcasts; K comes straight from the pool with 32-byte loads.
-// Per-lane online statistics of each head are merged across the warp once per
-// contiguous run of chunks of one layer.
-template <int G, bool BF16>
-__global__ void __launch_bounds__(kWarps * 32, 2) rule_logits_kernel(const RuleArgs a) {
-    extern __shared__ __align__(16) float Ms[];  // [Hq][D] of the current layer
-    constexpr int ES = BF16 ? 2 : 4;
-    constexpr int DPP = 32 / ES;                 // dims per 32-byte piece
-    constexpr int BATCH = 4;                     // pieces per token kept in registers at once
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int Hq = a.Hq, D = a.D, Hkv = a.Hkv;
-    const int n_pieces = D / DPP;
-    const int tasks = Hkv * a.R;
-    const int item0 = blockIdx.x * a.items_per_block;
-    const int item1 = min(a.n_items, item0 + a.items_per_block);
-    const int items_per_layer = (a.n_sub + a.R - 1) / a.R;
-    const uint64_t pol_z = kvsel_ptx::policy_evict_last();
+// Per-warp online (max, sum) statistics of one run: consecutive sub-chunks of
+// one layer and one kv head.  Each lane keeps its own pair per query head of
+// the group; a flush merges them across the warp and stores the result at the
+// run's first sub-chunk, the run's other sub-chunks carrying (-inf, 0).
+template <int G>
+struct RunStats {
+    float m[G], s[G];
+    int sub0 = 0, g = -1, l = -1;
 
-    int cur_l = -1;
-    // running stats of this warp's current task head, per query head of the group
-    float sm[G], ss[G];
-    int run_sub0 = 0, run_g = -1, run_l = -1;
-
-    auto flush_run = [&]() {
-        // merge the lanes' (max, sum) per head and store at the run's first sub-chunk
-        if (run_g < 0) return;
+    __device__ __forceinline__ void flush(const RuleArgs& a, int lane) {
+        if (g < 0) return;
 #pragma unroll
         for (int i = 0; i < G; ++i) {
-            float2 acc = make_float2(sm[i], ss[i]);
+            float2 acc = make_float2(m[i], s[i]);
 #pragma unroll
             for (int o = 16; o; o >>= 1)
                 acc = lse_merge(acc, make_float2(__shfl_xor_sync(kFull, acc.x, o), __shfl_xor_sync(kFull, acc.y, o)));
-            if (lane == 0) a.part[((int64_t)run_l * Hq + run_g * G + i) * a.n_sub + run_sub0] = acc;
+            if (lane == 0) a.part[((int64_t)l * a.Hq + g * G + i) * a.n_sub + sub0] = acc;
         }
-        run_g = -1;
-    };
+        g = -1;
+    }
 
-    for (int item = item0; item < item1; ++item) {
-        const int l = item / items_per_layer, ci = item % items_per_layer;
-        if (l != cur_l) {
-            __syncthreads();
-            for (int idx = threadIdx.x; idx < Hq * D / 4; idx += blockDim.x)
-                reinterpret_cast<float4*>(Ms)[idx] = __ldg(reinterpret_cast<const float4*>(a.M + (int64_t)l * Hq * D) + idx);
-            __syncthreads();
-            cur_l = l;
-        }
-        const char* layer = reinterpret_cast<const char*>(a.k_pool) + (size_t)l * a.layer_stride * ES;
-        for (int task = warp; task < tasks; task += kWarps) {
-            const int g = task % Hkv;
-            const int sub = ci * a.R + task / Hkv;
-            if (sub >= a.n_sub) continue;
-            if (run_g != g || run_l != l) {
-                flush_run();
-                run_g = g;
-                run_l = l;
-                run_sub0 = sub;
+    // Enter sub-chunk `sub` of (layer ll, kv head gg): continue the run or start a new one.
+    __device__ __forceinline__ void enter(const RuleArgs& a, int ll, int gg, int sub, int lane) {
+        if (g != gg || l != ll) {
+            flush(a, lane);
+            g = gg;
+            l = ll;
+            sub0 = sub;
 #pragma unroll
-                for (int i = 0; i < G; ++i) {
-                    sm[i] = -INFINITY;
-                    ss[i] = 0.f;
-                }
-            } else if (lane < G) {
-                // sub-chunks merged into the run's first entry carry an empty partial
-                a.part[((int64_t)l * Hq + g * G + lane) * a.n_sub + sub] = make_float2(-INFINITY, 0.f);
+            for (int i = 0; i < G; ++i) {
+                m[i] = -INFINITY;
+                s[i] = 0.f;
             }
-            // the lane's two tokens
-            const char* row[2];
-            bool cand[2];
+        } else if (lane < G) {
+            a.part[((int64_t)l * a.Hq + g * G + lane) * a.n_sub + sub] = make_float2(-INFINITY, 0.f);
+        }
+    }
+};
+
+// The (layer, kv head, sub-chunk) tasks a warp takes within its block's items,
+// in order; next() is false when the warp has none left.
+struct TaskCursor {
+    int item, t, l, g, sub;
+
+    __device__ __forceinline__ bool next(const RuleArgs& a, int item1, int warp, int tasks, int per_layer) {
+        if (warp >= tasks) return false;
+        for (;;) {
+            t += kWarps;
+            if (t >= tasks) {
+                t = warp;
+                ++item;
+            }
+            if (item >= item1) return false;
+            l = item / per_layer;
+            g = t % a.Hkv;
+            sub = (item % per_layer) * a.R + t / a.Hkv;
+            if (sub < a.n_sub) return true;
+        }
+    }
+};
+
+// Slot-map entries of a task's tokens, lane t holding tokens t, t + 32, ...;
+// -1 for tokens that are past N or forced (no row is read for them).  The
+// values are only loaded here, and checked where they are used, so that the
+// loads overlap the task before.
+__device__ __forceinline__ void task_slots(const RuleArgs& a, int sub, int lane, int (&slot)[kTPL]) {
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int j = sub * kSub + u * 32 + lane;
-                cand[u] = j < a.N && !is_forced(j, a.pi, a.q_s, a.q_e);
-                row[u] = nullptr;
-                if (cand[u]) {
-                    const int64_t slot = a.slot_map ? (int64_t)__ldg(a.slot_map + j) : (int64_t)j;
-                    if (slot < 0 || slot >= a.n_slots) {
-                        atomicOr(a.dev_err, (unsigned)KVSEL_DEV_BAD_SLOT);  // read as a zero row
-                    } else {
-                        row[u] = layer + ((size_t)slot * a.slot_stride + (size_t)g * D) * ES;
+    for (int u = 0; u < kTPL; ++u) {
+        const int j = sub * kSub + u * 32 + lane;
+        slot[u] = -1;
+        if (j < a.N && !is_forced(j, a.pi, a.q_s, a.q_e)) slot[u] = a.slot_map ? __ldg(a.slot_map + j) : j;
+    }
+}
+
+// One warp task = (layer l, kv head g, 32*kTPL tokens): lane t owns tokens t,
+// t+32, ... for all D dims of head g and all G query heads sharing it.  The
+// warp keeps the G rows of M it needs in its own slice of shared memory, and
+// every lane reads the same M entries, so the reads are broadcasts; K comes
+// straight from the pool in 32-byte pieces.  A warp streams through its tasks
+// without a block barrier: the last loads of a task already fetch the first
+// pieces of the next one, whose slot-map entries were loaded a task ahead.
+template <int G, bool BF16>
+__global__ void __launch_bounds__(kWarps * 32, KVSEL_RULE_MINB) rule_logits_kernel(const RuleArgs a) {
+    extern __shared__ __align__(16) float Msm[];  // [kWarps][G][D]
+    constexpr int ES = BF16 ? 2 : 4;
+    constexpr int DPP = 32 / ES;                  // dims per 32-byte piece
+    constexpr int BATCH = KVSEL_RULE_BATCH;       // pieces per token in flight (rolling)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Hq = a.Hq, D = a.D;
+    float* Ms = Msm + warp * G * D;
+    const int n_pieces = D / DPP;
+    const bool stream = n_pieces % BATCH == 0;    // pieces of consecutive tasks line up in the ring
+    const int tasks = a.Hkv * a.R;
+    const int item1 = min(a.n_items, (blockIdx.x + 1) * a.items_per_block);
+    const int per_layer = (a.n_sub + a.R - 1) / a.R;
+    const uint64_t pol_z = kvsel_ptx::policy_evict_last();
+
+    TaskCursor cur{blockIdx.x * a.items_per_block, warp - kWarps, 0, 0, 0};
+    if (!cur.next(a, item1, warp, tasks, per_layer)) return;
+    TaskCursor nxt = cur;
+    bool have_nxt = nxt.next(a, item1, warp, tasks, per_layer);
+    int slot_cur[kTPL], slot_nxt[kTPL];
+    task_slots(a, cur.sub, lane, slot_cur);
+    if (have_nxt) task_slots(a, nxt.sub, lane, slot_nxt);
+
+    auto row_of = [&](const TaskCursor& tk, int slot) -> const char* {
+        if (slot < 0 || slot >= a.n_slots) return nullptr;
+        return reinterpret_cast<const char*>(a.k_pool) +
+               ((size_t)tk.l * a.layer_stride + (size_t)slot * a.slot_stride + (size_t)tk.g * D) * ES;
+    };
+    const char* row[kTPL];
+    uint32_t raw[kTPL][BATCH][8];
+    auto load_first = [&]() {
+#pragma unroll
+        for (int u = 0; u < kTPL; ++u)
+#pragma unroll
+            for (int q = 0; q < BATCH; ++q) {
+                if (row[u] && q < n_pieces) {
+                    ldg32(row[u] + (size_t)q * 32, raw[u][q], a.aligned32);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) raw[u][q][k] = 0u;
+                }
+            }
+    };
+#pragma unroll
+    for (int u = 0; u < kTPL; ++u) row[u] = row_of(cur, slot_cur[u]);
+    load_first();
+
+    RunStats<G> run;
+    int m_l = -1, m_g = -1;
+    for (;;) {
+        run.enter(a, cur.l, cur.g, cur.sub, lane);
+        if (m_l != cur.l || m_g != cur.g) {
+            __syncwarp();
+            const float4* src = reinterpret_cast<const float4*>(a.M + ((int64_t)cur.l * Hq + cur.g * G) * D);
+            for (int idx = lane; idx < G * D / 4; idx += 32) reinterpret_cast<float4*>(Ms)[idx] = __ldg(src + idx);
+            __syncwarp();
+            m_l = cur.l;
+            m_g = cur.g;
+        }
+        float2 acc[kTPL][G];
+#pragma unroll
+        for (int u = 0; u < kTPL; ++u)
+#pragma unroll
+            for (int i = 0; i < G; ++i) acc[u][i] = make_float2(0.f, 0.f);
+        // Rolling prefetch: slot q of raw holds piece p0 + q; right after it is
+        // consumed it is refilled with piece p0 + BATCH + q, of this task or,
+        // past its last piece, of the next task.
+        for (int p0 = 0; p0 < n_pieces; p0 += BATCH) {
+#pragma unroll
+            for (int q = 0; q < BATCH; ++q) {
+                if (p0 + q >= n_pieces) break;
+                const int d0 = (p0 + q) * DPP;
+#pragma unroll
+                for (int w = 0; w < 8; w += (BF16 ? 2 : 4)) {
+                    // 4 dims of K for each of the lane's tokens
+                    float2 k01[kTPL], k23[kTPL];
+#pragma unroll
+                    for (int u = 0; u < kTPL; ++u) {
+                        if constexpr (BF16) {
+                            k01[u] = bf16x2_to_float2(raw[u][q][w]);
+                            k23[u] = bf16x2_to_float2(raw[u][q][w + 1]);
+                        } else {
+                            k01[u] = make_float2(__uint_as_float(raw[u][q][w]), __uint_as_float(raw[u][q][w + 1]));
+                            k23[u] = make_float2(__uint_as_float(raw[u][q][w + 2]), __uint_as_float(raw[u][q][w + 3]));
+                        }
+                    }
+                    const int d = d0 + (BF16 ? 2 * w : w);
+#pragma unroll
+                    for (int i = 0; i < G; ++i) {
+                        const float4 m4 = *reinterpret_cast<const float4*>(&Ms[i * D + d]);
+                        const float2 m01 = make_float2(m4.x, m4.y), m23 = make_float2(m4.z, m4.w);
+#pragma unroll
+                        for (int u = 0; u < kTPL; ++u) {
+                            acc[u][i] = __ffma2_rn(m01, k01[u], acc[u][i]);
+                            acc[u][i] = __ffma2_rn(m23, k23[u], acc[u][i]);
+                        }
                     }
                 }
-            }
-            float2 acc[2][G];
+                const int pn = p0 + BATCH + q;
+                if (pn < n_pieces) {
 #pragma unroll
-            for (int u = 0; u < 2; ++u)
+                    for (int u = 0; u < kTPL; ++u)
+                        if (row[u]) ldg32(row[u] + (size_t)pn * 32, raw[u][q], a.aligned32);
+                } else if (stream && have_nxt) {
 #pragma unroll
-                for (int i = 0; i < G; ++i) acc[u][i] = make_float2(0.f, 0.f);
-            for (int p0 = 0; p0 < n_pieces; p0 += BATCH) {
-                uint32_t raw[2][BATCH][8];
-#pragma unroll
-                for (int u = 0; u < 2; ++u)
-#pragma unroll
-                    for (int q = 0; q < BATCH; ++q) {
-                        if (row[u] && p0 + q < n_pieces) {
-                            ldg32(row[u] + (size_t)(p0 + q) * 32, raw[u][q], a.aligned32);
+                    for (int u = 0; u < kTPL; ++u) {
+                        const char* r2 = row_of(nxt, slot_nxt[u]);
+                        if (r2) {
+                            ldg32(r2 + (size_t)(pn - n_pieces) * 32, raw[u][q], a.aligned32);
                         } else {
 #pragma unroll
                             for (int k = 0; k < 8; ++k) raw[u][q][k] = 0u;
                         }
                     }
-#pragma unroll
-                for (int q = 0; q < BATCH; ++q) {
-                    if (p0 + q >= n_pieces) break;
-                    const int d0 = (p0 + q) * DPP;
-#pragma unroll
-                    for (int w = 0; w < 8; w += (BF16 ? 2 : 4)) {
-                        // 4 dims of K for both tokens
-                        float2 k01[2], k23[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            if constexpr (BF16) {
-                                k01[u] = bf16x2_to_float2(raw[u][q][w]);
-                                k23[u] = bf16x2_to_float2(raw[u][q][w + 1]);
-                            } else {
-                                k01[u] = make_float2(__uint_as_float(raw[u][q][w]), __uint_as_float(raw[u][q][w + 1]));
-                                k23[u] = make_float2(__uint_as_float(raw[u][q][w + 2]), __uint_as_float(raw[u][q][w + 3]));
-                            }
-                        }
-                        const int d = d0 + (BF16 ? 2 * w : w);
-#pragma unroll
-                        for (int i = 0; i < G; ++i) {
-                            const float4 m4 = *reinterpret_cast<const float4*>(&Ms[(g * G + i) * D + d]);
-                            const float2 m01 = make_float2(m4.x, m4.y), m23 = make_float2(m4.z, m4.w);
-#pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                acc[u][i] = __ffma2_rn(m01, k01[u], acc[u][i]);
-                                acc[u][i] = __ffma2_rn(m23, k23[u], acc[u][i]);
-                            }
-                        }
-                    }
-                }
-            }
-            // logits: coalesced along tokens; statistics per lane
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int j = sub * kSub + u * 32 + lane;
-                if (j < a.N) {
-#pragma unroll
-                    for (int i = 0; i < G; ++i) {
-                        const float z = cand[u] ? (acc[u][i].x + acc[u][i].y) * a.scale : -INFINITY;
-                        store_f32_hint(a.z + ((int64_t)l * Hq + g * G + i) * a.N + j, z, pol_z);
-                        if (cand[u]) stat_add(z, sm[i], ss[i]);
-                    }
                 }
             }
         }
+        // logits: coalesced along tokens; statistics per lane
+#pragma unroll
+        for (int u = 0; u < kTPL; ++u) {
+            const int j = cur.sub * kSub + u * 32 + lane;
+            if (j < a.N) {
+                const bool cand = !is_forced(j, a.pi, a.q_s, a.q_e);
+                if (cand && !row[u]) atomicOr(a.dev_err, (unsigned)KVSEL_DEV_BAD_SLOT);  // read as a zero row
+#pragma unroll
+                for (int i = 0; i < G; ++i) {
+                    const float z = cand ? (acc[u][i].x + acc[u][i].y) * a.scale : -INFINITY;
+                    store_f32_hint(a.z + ((int64_t)cur.l * Hq + cur.g * G + i) * a.N + j, z, pol_z);
+                    if (cand) stat_add(z, run.m[i], run.s[i]);
+                }
+            }
+        }
+        if (!have_nxt) break;
+        cur = nxt;
+#pragma unroll
+        for (int u = 0; u < kTPL; ++u) {
+            slot_cur[u] = slot_nxt[u];
+            row[u] = row_of(cur, slot_cur[u]);
+        }
+        have_nxt = nxt.next(a, item1, warp, tasks, per_layer);
+        if (have_nxt) task_slots(a, nxt.sub, lane, slot_nxt);
+        if (!stream) load_first();
     }
-    flush_run();
+    run.flush(a, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -487,8 +573,8 @@ cudaError_t launch_rule_scores(kvsel_ctx* ctx, const void* k_pool, int dtype, co
     const int items_per_layer = (a.n_sub + a.R - 1) / a.R;
     a.n_items = L * items_per_layer;
     const int G = Hq / Hkv;
-    const size_t smem = sizeof(float) * (size_t)Hq * D;
-    int blocks_per_sm = 2;
+    const size_t smem = sizeof(float) * (size_t)kWarps * G * D;  // each warp's slice of M
+    const int blocks_per_sm = KVSEL_RULE_MINB;
     const int grid_max = blocks_per_sm * ctx->num_sms;
     a.items_per_block = (a.n_items + grid_max - 1) / grid_max;
     const int grid = (a.n_items + a.items_per_block - 1) / a.items_per_block;

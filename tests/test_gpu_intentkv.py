@@ -130,7 +130,9 @@ def test_rule_scores_ragged_and_degenerate(ctx, N, pi, qs, qe):
     assert_scores_close(f64(rule), ref, what="rule_j degenerate")
 
 
-@pytest.mark.parametrize("G,Hkv,D", [(1, 4, 64), (3, 2, 128), (5, 1, 256), (8, 2, 32), (2, 3, 16)])
+@pytest.mark.parametrize("G,Hkv,D", [(1, 4, 64), (3, 2, 128), (5, 1, 256), (8, 2, 32), (2, 3, 16),
+                                     (1, 8, 128), (2, 4, 128), (4, 8, 128), (5, 8, 128), (6, 2, 128),
+                                     (7, 1, 128), (8, 16, 128), (4, 16, 128)])
 def test_rule_scores_shapes(ctx, G, Hkv, D):
     L, N = 2, 333
     Hq = G * Hkv
