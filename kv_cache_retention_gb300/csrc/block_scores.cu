@@ -8,26 +8,31 @@
 // For one (layer l, kv head g) the G = Hq/Hkv query heads' rows form one
 // contiguous [G*M][128] bf16 matrix Q_lg and the index one [Bcap][128] matrix
 // K_lg.  The logits S = Q_lg K_lg^T are never stored; two passes recompute them
-// on the tensor cores, each reducing along the axis its epilogue threads own:
-//   row pass:    A = 128 query rows (TMEM lanes), B = 256 candidate blocks per
-//                tile; each lane keeps an online (max, sum 2^x) over its row
+// on the tensor cores.  In both, A = 128 query rows (one per TMEM lane and
+// epilogue thread) and B = 256 candidate blocks (accumulator columns):
+//   row pass:    a unit is (l,g, 128 query rows); B tiles stream.  Each lane
+//                sums 2^(x - ref) over its row, ref being a reference that only
+//                moves when a tile's sum passes 2^64
 //                -> lse2[r] = log2 sum_{b in C} 2^(S[r,b] log2e/sqrt(d))
-//   column pass: A = 128 candidate blocks (TMEM lanes), B = 256 query rows per
-//                tile; each lane sums 2^(S[b,r] log2e/sqrt(d) - lse2[r]) over
-//                all rows of the group -> mass[lg][b], complete per CTA
+//   column pass: a unit is (l,g, 256 candidate blocks); A tiles stream.  Each
+//                lane holds lse2 of its row in a register and adds
+//                2^(x - lse2[r]) into one accumulator per column; at the end of
+//                the unit the columns are summed across lanes (a butterfly
+//                reduce-scatter) and across the four lane quarters
+//                -> mass[lg][b], complete per CTA
 //   finalize:    R[b] = sum_lg mass[lg][b] / (L*Hq), in fixed (l,g) order.
 //
 // Kernel structure (one persistent CTA per SM, 576 threads):
-//   warp 0      TMA producer: A tile per unit, B tiles through a 2-stage ring
-//               (128-byte swizzled, K-major, no multicast)
+//   warp 0      TMA producer: the unit's fixed tile, then the streamed tiles
+//               (A ring of 2 x 32 KB, B ring of 2 x 64 KB; 128-byte swizzled,
+//               K-major, no multicast)
 //   warp 1      allocates 512 TMEM columns; lane 0 issues tcgen05.mma
 //               (kind::f16, bf16 x bf16 -> fp32, M=128 N=256 K=16, 8 per tile)
 //               into one of two 256-column accumulators and commits to
 //               mbarriers that free the smem stage and hand the accumulator on
 //   warps 2-17  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
 //               32*(w%4)..+31; four column slices of 64), exp2 on the MUFU,
-//               packed fp32 adds; the accumulator is handed back as soon as it
-//               is in registers
+//               packed fp32 arithmetic
 // Every mbarrier wait is bounded (1 s of globaltimer); on a timeout the CTA
 // flags KVSEL_ERR_TIMEOUT in the device error word, drains its own copies and
 // MMAs, frees TMEM and returns.
@@ -41,29 +46,45 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kD = 128;
-constexpr int BM = 128;                         // A rows per unit = TMEM lanes
-constexpr int BN = 256;                         // B rows per tile = accumulator columns
-constexpr int kABytes = BM * kD * 2;            // 32 KB: two 64-column K blocks of 16 KB
-constexpr int kBBytes = BN * kD * 2;            // 64 KB: two K blocks of 32 KB
-constexpr int kNA = 2, kNB = 2, kNAcc = 2;
-constexpr int kTmemCols = 512;
+constexpr int BM = 128;                         // TMEM lanes = query rows per MMA
+constexpr int kRowBytes = kD * 2;               // one bf16 row of 128 dims
+constexpr int kStageBytes = 192 * 1024;         // operand buffers of either pass
+
+// Operand tiling of a pass.  The fixed operand is loaded once per unit (kNF
+// buffers), the streamed one once per tile (a ring of kNS stages).
+//   row pass:    fixed A = 128 query rows, streamed B = 256 candidate blocks
+//   column pass: fixed B = 256 candidate blocks, streamed A = 128 query rows
+template <int MODE>
+struct Tiling {
+    static constexpr int kFRows = MODE == 0 ? 128 : 256, kSRows = MODE == 0 ? 256 : 128;
+    static constexpr int kNF = MODE == 0 ? 2 : 1, kNS = MODE == 0 ? 2 : 4;
+    static constexpr int kFBytes = kFRows * kRowBytes, kSBytes = kSRows * kRowBytes;
+    static_assert(kNF * kFBytes + kNS * kSBytes == kStageBytes, "operand buffers");
+};
+constexpr int kMaxStages = 4;
+constexpr int kNAcc = 2;                        // accumulator buffers
+constexpr int kAccCols = 256;                   // TMEM columns per accumulator buffer
+constexpr int kTmemCols = kNAcc * kAccCols;
 constexpr int kEpiWarps = 16;                   // 4 TMEM lane quarters x kSlices column slices
 constexpr int kSlices = kEpiWarps / 4;
-constexpr int kSliceCols = BN / kSlices;        // accumulator columns per epilogue thread and tile
+constexpr int kSliceCols = kAccCols / kSlices;  // accumulator columns per epilogue thread and tile
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr uint64_t kWaitNs = 1000000000ull;     // 1 s per wait
-constexpr uint32_t kSuspendNs = 20000;          // try_wait may park the thread this long (woken on completion)
+#ifndef KVSEL_SUSPEND_NS
+#define KVSEL_SUSPEND_NS 20000
+#endif
+constexpr uint32_t kSuspendNs = KVSEL_SUSPEND_NS;  // try_wait may park the thread this long (woken on completion)
 
-// instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, N=256, M=128
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
+// instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M=128
+__host__ __device__ constexpr uint32_t idesc(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
 
 struct TcArgs {
-    int mode;          // 0 row pass, 1 column pass
     int n_units;
     int units_per_lg;
-    int n_bt;          // B tiles per unit
+    int n_it;          // streamed tiles per unit
     int rows_g;        // G*M
     int rows_pad;      // rows_g rounded up to a multiple of 4 (row stride of lse2)
     int c0, c1;        // candidate blocks [c0, c1)
@@ -76,15 +97,14 @@ struct TcArgs {
 };
 
 struct __align__(8) SmemTail {
-    float colv[kNAcc][BN];        // column pass: lse2 of the tile's query rows (bulk-copied)
-    float red[kSlices][BM][2];    // merge of the column slices at unit end
-    uint64_t full_a[kNA], empty_a[kNA], full_b[kNB], empty_b[kNB], acc_full[kNAcc], acc_empty[kNAcc];
-    uint64_t lse_full[kNAcc], lse_empty[kNAcc];  // column pass: colv ring, one slot per accumulator
+    float red[kSlices][BM][2];    // row pass: (ref, sum) per slice; column pass: [kSlices][4][64] column sums
+    uint64_t full_f[2], empty_f[2], full_s[kMaxStages], empty_s[kMaxStages], acc_full[kNAcc], acc_empty[kNAcc];
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
 };
-constexpr size_t kSmemBytes = (size_t)kNA * kABytes + (size_t)kNB * kBBytes + sizeof(SmemTail) + 1024;
+static_assert(kSlices * BM * 2 == kSlices * 4 * kSliceCols, "column pass reuses the row pass merge buffer");
+constexpr size_t kSmemBytes = (size_t)kStageBytes + sizeof(SmemTail) + 1024;
 
 // ---- PTX wrappers ----------------------------------------------------------
 
@@ -154,48 +174,6 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// Plain bulk copy global -> shared (16-byte aligned, size a multiple of 16).
-__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     saddr(dst)),
-                 "l"(src), "r"(bytes), "r"(saddr(bar))
-                 : "memory");
-}
-
-// 2^x on the FMA pipe, for a share of the exponentials (the MUFU computes the
-// rest): x = n + f with n = rint(x) (added to 1.5*2^23 and subtracted back),
-// |f| <= 1/2; 2^f = e^(f ln 2) by its Taylor series to degree 5 (truncation
-// below 3.4e-6 relative); 2^n goes into the exponent field.  x is clamped at
-// -125, so x = -inf gives ~2e-38 instead of 0 (far below anything summed here).
-__device__ __forceinline__ float2 exp2_fma(float2 x) {
-    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-    constexpr float c1 = 0.693147182464599609375f, c2 = 0.2402265071868896484375f, c3 = 0.0555041097104549407958984375f,
-                    c4 = 0.009618128649890422821044921875f, c5 = 0.001333355787210166454315185546875f;
-    x = make_float2(fmaxf(x.x, -125.f), fmaxf(x.y, -125.f));
-    const float2 t = __fadd2_rn(x, make_float2(kMagic, kMagic));
-    const float2 n = __fadd2_rn(t, make_float2(-kMagic, -kMagic));
-    const float2 f = __fadd2_rn(x, make_float2(-n.x, -n.y));
-    float2 p = __ffma2_rn(make_float2(c5, c5), f, make_float2(c4, c4));
-    p = __ffma2_rn(p, f, make_float2(c3, c3));
-    p = __ffma2_rn(p, f, make_float2(c2, c2));
-    p = __ffma2_rn(p, f, make_float2(c1, c1));
-    p = __ffma2_rn(p, f, make_float2(1.f, 1.f));
-    const int ex = (__float_as_int(t.x) - __float_as_int(kMagic)) << 23;
-    const int ey = (__float_as_int(t.y) - __float_as_int(kMagic)) << 23;
-    return make_float2(__int_as_float(__float_as_int(p.x) + ex), __int_as_float(__float_as_int(p.y) + ey));
-}
-
-// Exponentials of a pair: pairs with index < kPolyPairs (of 16 per 32-column
-// chunk) go to the FMA pipe, the rest to the MUFU.
-#ifndef KVSEL_POLY_PAIRS
-#define KVSEL_POLY_PAIRS 0
-#endif
-constexpr int kPolyPairs = KVSEL_POLY_PAIRS;
-__device__ __forceinline__ float2 exp2_pair(float2 x, int pair) {
-    if (pair < kPolyPairs) return exp2_fma(x);
-    return make_float2(ex2(x.x), ex2(x.y));
-}
-
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
     return (uint64_t)((addr & 0x3FFFFu) >> 4)   // start address
            | ((uint64_t)1 << 16)                // leading byte offset (unused with 128B swizzle)
@@ -204,11 +182,12 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
            | ((uint64_t)2 << 61);               // 128-byte swizzle
 }
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc_v,
+                                          uint32_t accum) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
             d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accum)
+        "l"(adesc), "l"(bdesc), "r"(idesc_v), "r"(accum)
         : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -231,6 +210,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -251,63 +240,81 @@ __device__ __forceinline__ bool epi_bar_and(bool v) {
     return r != 0;
 }
 
-// Column-pass accumulation of one slice: s2 += 2^(v*scale - lse[col]); with MASK,
-// columns >= nvalid are skipped (their lse slots may hold stale data).
-template <bool MASK>
-__device__ __forceinline__ void col_accumulate(const float (&v)[kSliceCols / 32][32], const float* cv, float scale,
-                                               int nvalid, float2 (&s2)[4]) {
-    const float2 sc = make_float2(scale, scale);
+// ---- epilogue helpers -----------------------------------------------------
+
+// Sum of 2^(v*scale - ref) over one 32-column chunk into four packed accumulators.
+__device__ __forceinline__ void row_terms(const float (&v)[32], float2 sc, float2 nr, float2 (&t2)[4]) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        const float2 x = __ffma2_rn(make_float2(v[i], v[i + 1]), sc, nr);
+        t2[(i >> 1) & 3] = __fadd2_rn(t2[(i >> 1) & 3], make_float2(ex2(x.x), ex2(x.y)));
+    }
+}
+
+// Largest value of a 64-column slice, as a tree of three-input maxima.
+__device__ __forceinline__ float slice_max(const float (&v)[kSliceCols / 32][32]) {
+    float m[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m[j] = -INFINITY;
 #pragma unroll
     for (int c = 0; c < kSliceCols / 32; ++c)
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(cv + c * 32 + i);
-            float2 x0 = __ffma2_rn(make_float2(v[c][i], v[c][i + 1]), sc, make_float2(-l4.x, -l4.y));
-            float2 x1 = __ffma2_rn(make_float2(v[c][i + 2], v[c][i + 3]), sc, make_float2(-l4.z, -l4.w));
-            if (MASK) {
-                const int col = c * 32 + i;
-                if (col >= nvalid) x0.x = -INFINITY;
-                if (col + 1 >= nvalid) x0.y = -INFINITY;
-                if (col + 2 >= nvalid) x1.x = -INFINITY;
-                if (col + 3 >= nvalid) x1.y = -INFINITY;
-            }
-            s2[(i >> 2) & 3] = __fadd2_rn(s2[(i >> 2) & 3], exp2_pair(x0, i >> 1));
-            s2[((i >> 2) + 2) & 3] = __fadd2_rn(s2[((i >> 2) + 2) & 3], exp2_pair(x1, (i >> 1) + 1));
+        for (int i = 0; i < 32; i += 2) m[(i >> 1) & 7] = max3(m[(i >> 1) & 7], v[c][i], v[c][i + 1]);
+    return max3(max3(m[0], m[1], m[2]), max3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+}
+
+// Column sums of a warp: on entry lane l holds f[c] = its row's value for column
+// c (0..63); on exit f[0], f[1] hold the sums over the warp's 32 rows of columns
+// 2l and 2l+1.  Five butterfly levels; at each the lane keeps the half of its
+// columns selected by one lane bit and sends the other half to its partner.
+__device__ __forceinline__ void column_reduce(float (&f)[64], int lane) {
+#pragma unroll
+    for (int s = 16, n = 32; s >= 1; s >>= 1, n >>= 1) {
+        const bool up = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+            const float keep = up ? f[n + i] : f[i];
+            const float send = up ? f[i] : f[n + i];
+            f[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
         }
+    }
 }
 
 // ---- the kernel -----------------------------------------------------------
 
+// MODE 0: row pass, MODE 1: column pass (operand roles in Tiling).  Either
+// way one tile is one 128 x 256 accumulator: TMEM lane = query row, column =
+// candidate block.
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-    block_scores_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, const TcArgs a) {
+    block_scores_tc(const __grid_constant__ CUtensorMap mapF, const __grid_constant__ CUtensorMap mapS, const TcArgs a) {
+    using T = Tiling<MODE>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t* sA = smem;                                   // [kNA][kABytes]
-    uint8_t* sB = smem + kNA * kABytes;                   // [kNB][kBBytes]
-    SmemTail& t = *reinterpret_cast<SmemTail*>(sB + kNB * kBBytes);
+    uint8_t* sF = smem;                                   // [kNF][kFBytes]
+    uint8_t* sS = smem + T::kNF * T::kFBytes;             // [kNS][kSBytes]
+    SmemTail& t = *reinterpret_cast<SmemTail*>(smem + kStageBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int* abort_flag = &t.abort_flag;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kNA; ++i) {
-            mbar_init(&t.full_a[i], 1);
-            mbar_init(&t.empty_a[i], 1);
+        for (int i = 0; i < T::kNF; ++i) {
+            mbar_init(&t.full_f[i], 1);
+            mbar_init(&t.empty_f[i], 1);
         }
-        for (int i = 0; i < kNB; ++i) {
-            mbar_init(&t.full_b[i], 1);
-            mbar_init(&t.empty_b[i], 1);
+        for (int i = 0; i < T::kNS; ++i) {
+            mbar_init(&t.full_s[i], 1);
+            mbar_init(&t.empty_s[i], 1);
         }
         for (int i = 0; i < kNAcc; ++i) {
             mbar_init(&t.acc_full[i], 1);
             mbar_init(&t.acc_empty[i], kEpiWarps);  // one arrival per epilogue warp
-            mbar_init(&t.lse_full[i], 1);
-            mbar_init(&t.lse_empty[i], kEpiWarps);
         }
         mbar_init(&t.mma_done, 1);
         t.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapA)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapB)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapF)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapS)) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&t.tmem_base)),
@@ -323,83 +330,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
-            uint32_t a_it = 0, b_it = 0;
+            uint32_t f_it = 0, s_it = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
-                const int lg = u / a.units_per_lg, ta = u % a.units_per_lg;
-                int ya, yb0;
-                if (a.mode == 0) {
-                    ya = lg * a.rows_g + ta * BM;
-                    yb0 = lg * a.Bcap + a.c0;
-                } else {
-                    ya = lg * a.Bcap + a.c0 + ta * BM;
-                    yb0 = lg * a.rows_g;
-                }
-                const int sa = a_it % kNA;
-                if (!(ok = wait_phase(&t.empty_a[sa], ((a_it / kNA) & 1) ^ 1, abort_flag, a.err))) break;
-                mbar_expect_tx(&t.full_a[sa], kABytes);
-                tma_load_2d(&mapA, &t.full_a[sa], sA + sa * kABytes, 0, ya);
-                tma_load_2d(&mapA, &t.full_a[sa], sA + sa * kABytes + kABytes / 2, 64, ya);
-                ++a_it;
-                for (int tb = 0; tb < a.n_bt; ++tb) {
-                    const int sb = b_it % kNB;
-                    if (!(ok = wait_phase(&t.empty_b[sb], ((b_it / kNB) & 1) ^ 1, abort_flag, a.err))) break;
-                    mbar_expect_tx(&t.full_b[sb], kBBytes);
-                    tma_load_2d(&mapB, &t.full_b[sb], sB + sb * kBBytes, 0, yb0 + tb * BN);
-                    tma_load_2d(&mapB, &t.full_b[sb], sB + sb * kBBytes + kBBytes / 2, 64, yb0 + tb * BN);
-                    if (a.mode == 1) {
-                        // the log-sum-exps of this tile's query rows, one slot per accumulator
-                        const int k = b_it % kNAcc;
-                        if (!(ok = wait_phase(&t.lse_empty[k], ((b_it / kNAcc) & 1) ^ 1, abort_flag, a.err))) break;
-                        const int r0 = tb * BN;
-                        const uint32_t bytes = 4u * (uint32_t)min(BN, a.rows_pad - r0);
-                        mbar_expect_tx(&t.lse_full[k], bytes);
-                        bulk_copy(&t.colv[k][0], a.lse2 + (int64_t)lg * a.rows_pad + r0, bytes, &t.lse_full[k]);
-                    }
-                    ++b_it;
+                const int lg = u / a.units_per_lg, o = u % a.units_per_lg;
+                const int fs = f_it % T::kNF;
+                const int yf = MODE == 0 ? lg * a.rows_g + o * T::kFRows : lg * a.Bcap + a.c0 + o * T::kFRows;
+                if (!(ok = wait_phase(&t.empty_f[fs], ((f_it / T::kNF) & 1) ^ 1, abort_flag, a.err))) break;
+                mbar_expect_tx(&t.full_f[fs], T::kFBytes);
+                tma_load_2d(&mapF, &t.full_f[fs], sF + fs * T::kFBytes, 0, yf);
+                tma_load_2d(&mapF, &t.full_f[fs], sF + fs * T::kFBytes + T::kFBytes / 2, 64, yf);
+                ++f_it;
+                for (int i = 0; i < a.n_it; ++i) {
+                    const int st = s_it % T::kNS;
+                    const int ys = MODE == 0 ? lg * a.Bcap + a.c0 + i * T::kSRows : lg * a.rows_g + i * T::kSRows;
+                    if (!(ok = wait_phase(&t.empty_s[st], ((s_it / T::kNS) & 1) ^ 1, abort_flag, a.err))) break;
+                    mbar_expect_tx(&t.full_s[st], T::kSBytes);
+                    tma_load_2d(&mapS, &t.full_s[st], sS + st * T::kSBytes, 0, ys);
+                    tma_load_2d(&mapS, &t.full_s[st], sS + st * T::kSBytes + T::kSBytes / 2, 64, ys);
+                    ++s_it;
                 }
             }
             // drain: wait until every copy this thread started has landed
-            for (uint32_t i = (b_it > (uint32_t)kNB ? b_it - kNB : 0); i < b_it; ++i)
-                drain_phase(&t.full_b[i % kNB], (i / kNB) & 1);
-            for (uint32_t i = (a_it > (uint32_t)kNA ? a_it - kNA : 0); i < a_it; ++i)
-                drain_phase(&t.full_a[i % kNA], (i / kNA) & 1);
-            if (a.mode == 1)
-                for (uint32_t i = (b_it > (uint32_t)kNAcc ? b_it - kNAcc : 0); i < b_it; ++i)
-                    drain_phase(&t.lse_full[i % kNAcc], (i / kNAcc) & 1);
+            for (uint32_t i = (s_it > (uint32_t)T::kNS ? s_it - T::kNS : 0); i < s_it; ++i)
+                drain_phase(&t.full_s[i % T::kNS], (i / T::kNS) & 1);
+            for (uint32_t i = (f_it > (uint32_t)T::kNF ? f_it - T::kNF : 0); i < f_it; ++i)
+                drain_phase(&t.full_f[i % T::kNF], (i / T::kNF) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
-            uint32_t a_it = 0, b_it = 0, acc_it = 0;
+            uint32_t f_it = 0, s_it = 0, acc_it = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
-                const int sa = a_it % kNA;
-                if (!(ok = wait_phase(&t.full_a[sa], (a_it / kNA) & 1, abort_flag, a.err))) break;
+                const int fs = f_it % T::kNF;
+                if (!(ok = wait_phase(&t.full_f[fs], (f_it / T::kNF) & 1, abort_flag, a.err))) break;
                 tc_fence_after();
-                const uint32_t a_base = saddr(sA + sa * kABytes);
-                for (int tb = 0; tb < a.n_bt; ++tb) {
-                    const int sb = b_it % kNB;
+                const uint32_t f_base = saddr(sF + fs * T::kFBytes);
+                for (int i = 0; i < a.n_it; ++i) {
+                    const int st = s_it % T::kNS;
                     const int k = acc_it % kNAcc;
-                    if (!(ok = wait_phase(&t.full_b[sb], (b_it / kNB) & 1, abort_flag, a.err))) break;
+                    if (!(ok = wait_phase(&t.full_s[st], (s_it / T::kNS) & 1, abort_flag, a.err))) break;
                     if (!(ok = wait_phase(&t.acc_empty[k], ((acc_it / kNAcc) & 1) ^ 1, abort_flag, a.err))) break;
                     tc_fence_after();
-                    const uint32_t b_base = saddr(sB + sb * kBBytes);
-                    const uint32_t d_tmem = tmem_base + (uint32_t)(k * BN);
+                    const uint32_t s_base = saddr(sS + st * T::kSBytes);
+                    // A = the 128-row operand, B = the 256-row one
+                    const uint32_t a_base = MODE == 0 ? f_base : s_base, b_base = MODE == 0 ? s_base : f_base;
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(k * kAccCols);
 #pragma unroll
                     for (int kk = 0; kk < kD / 16; ++kk) {
                         const uint32_t off = (uint32_t)((kk & 3) * 32);
-                        const uint64_t ad = sw128_desc(a_base + (kk >> 2) * (kABytes / 2) + off);
-                        const uint64_t bd = sw128_desc(b_base + (kk >> 2) * (kBBytes / 2) + off);
-                        umma_bf16(d_tmem, ad, bd, kk > 0 ? 1u : 0u);
+                        const uint64_t ad = sw128_desc(a_base + (kk >> 2) * (BM * 128) + off);
+                        const uint64_t bd = sw128_desc(b_base + (kk >> 2) * (kAccCols * 128) + off);
+                        umma_bf16(d_tmem, ad, bd, idesc(kAccCols), kk > 0 ? 1u : 0u);
                     }
-                    umma_commit(&t.empty_b[sb]);
+                    umma_commit(&t.empty_s[st]);
                     umma_commit(&t.acc_full[k]);
-                    ++b_it;
+                    ++s_it;
                     ++acc_it;
                 }
-                if (ok) umma_commit(&t.empty_a[sa]);
-                ++a_it;
+                if (ok) umma_commit(&t.empty_f[fs]);
+                ++f_it;
             }
             // drain: every MMA issued by this thread completes before TMEM is freed
             umma_commit(&t.mma_done);
@@ -410,21 +401,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ew = warp - 2;                 // 0 .. kEpiWarps-1
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
         const int slice = ew >> 2;               // column slice
-        const int r_local = q * 32 + lane;       // TMEM lane = A row of the unit
+        const int r_local = q * 32 + lane;       // TMEM lane = query row of the tile
         const int etid = ew * 32 + lane;
+        const float2 sc = make_float2(a.scale, a.scale);
         uint32_t acc_it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
-            const int lg = u / a.units_per_lg, ta = u % a.units_per_lg;
-            float m_run = -INFINITY;
+            const int lg = u / a.units_per_lg, o = u % a.units_per_lg;
+            const float* lse_lg = a.lse2 + (int64_t)lg * a.rows_pad;
+            // row pass: reference and sum of this lane's row over its slice
+            float ref = -INFINITY;
             float2 s2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                             make_float2(0.f, 0.f)};
-            for (int tb = 0; tb < a.n_bt; ++tb) {
+            // column pass: this lane's row's share of each of its slice's 64 columns,
+            // and lse2 of its row in the next two tiles (loaded ahead)
+            float2 cs[kSliceCols / 2];
+            float lse_n0 = INFINITY, lse_n1 = INFINITY;
+            if (MODE == 1) {
+#pragma unroll
+                for (int j = 0; j < kSliceCols / 2; ++j) cs[j] = make_float2(0.f, 0.f);
+                if (r_local < a.rows_pad) lse_n0 = __ldg(lse_lg + r_local);
+                if (BM + r_local < a.rows_pad && a.n_it > 1) lse_n1 = __ldg(lse_lg + BM + r_local);
+            }
+            for (int i = 0; i < a.n_it; ++i) {
                 const int k = acc_it % kNAcc;
                 // a timed-out wait makes this thread skip its work; the epilogue warps
                 // agree on giving up at the end of the unit
                 if (ok) ok = wait_phase(&t.acc_full[k], (acc_it / kNAcc) & 1, abort_flag, a.err);
-                if (ok && a.mode == 1) ok = wait_phase(&t.lse_full[k], (acc_it / kNAcc) & 1, abort_flag, a.err);
                 ok = __all_sync(0xffffffffu, ok);  // warp-uniform: TMEM loads are warp-collective
                 if (!ok) {
                     ++acc_it;
@@ -432,70 +435,84 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t taddr =
-                    tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(k * BN + slice * kSliceCols);
-                float v[kSliceCols / 32][32];
+                    tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(k * kAccCols + slice * kSliceCols);
+                if (MODE == 0) {
+                    float v[kSliceCols / 32][32];
 #pragma unroll
-                for (int c = 0; c < kSliceCols / 32; ++c) tmem_ld32(taddr + 32 * c, v[c]);
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&t.acc_empty[k]);  // this warp's part of the accumulator is read
-                if (a.mode == 0) {
-                    // row pass: online (max, sum 2^x) over this slice's columns
-                    const int col0 = a.c0 + tb * BN + slice * kSliceCols;  // block id of the slice's column 0
-                    const int nvalid = a.c1 - col0;                        // columns >= nvalid are masked
+                    for (int c = 0; c < kSliceCols / 32; ++c) tmem_ld32(taddr + 32 * c, v[c]);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&t.acc_empty[k]);  // this warp's part of the accumulator is read
+                    // columns past the candidate range (last tile only) are masked
+                    const int nvalid = a.c1 - (a.c0 + i * kAccCols + slice * kSliceCols);
                     if (nvalid < kSliceCols) {
 #pragma unroll
                         for (int c = 0; c < kSliceCols / 32; ++c)
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (c * 32 + i >= nvalid) v[c][i] = -INFINITY;
+                            for (int j = 0; j < 32; ++j)
+                                if (c * 32 + j >= nvalid) v[c][j] = -INFINITY;
                     }
-                    float mx = -INFINITY;
+                    if (ref == -INFINITY) ref = slice_max(v) * a.scale;  // first tile with a finite logit
+                    if (ref != -INFINITY) {
+                        float2 t2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                        make_float2(0.f, 0.f)};
 #pragma unroll
-                    for (int c = 0; c < kSliceCols / 32; ++c)
+                        for (int c = 0; c < kSliceCols / 32; ++c) row_terms(v[c], sc, make_float2(-ref, -ref), t2);
+                        const float big = fmaxf(max3(t2[0].x, t2[0].y, t2[1].x), max3(t2[1].y, t2[2].x, t2[2].y));
+                        if (!(fmaxf(big, fmaxf(t2[3].x, t2[3].y)) <= 0x1p64f)) {
+                            // a logit far above the reference: move it to this tile's
+                            // maximum, rescale the sum and take the tile again
+                            const float r_new = fmaxf(ref, slice_max(v) * a.scale);
+                            const float f = ex2(ref - r_new);
 #pragma unroll
-                        for (int i = 0; i < 32; i += 2) mx = max3(mx, v[c][i], v[c][i + 1]);
-                    const float m_new = fmaxf(m_run, mx * a.scale);
-                    if (m_new != -INFINITY) {
-                        if (m_new > m_run) {
-                            const float f = ex2(m_run - m_new);
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) s2[j] = make_float2(s2[j].x * f, s2[j].y * f);
-                            m_run = m_new;
-                        }
-                        const float2 sc = make_float2(a.scale, a.scale), nm = make_float2(-m_run, -m_run);
-#pragma unroll
-                        for (int c = 0; c < kSliceCols / 32; ++c)
-#pragma unroll
-                            for (int i = 0; i < 32; i += 2) {
-                                const float2 x = __ffma2_rn(make_float2(v[c][i], v[c][i + 1]), sc, nm);
-                                s2[(i >> 1) & 3] = __fadd2_rn(s2[(i >> 1) & 3], exp2_pair(x, i >> 1));
+                            for (int j = 0; j < 4; ++j) {
+                                s2[j] = make_float2(s2[j].x * f, s2[j].y * f);
+                                t2[j] = make_float2(0.f, 0.f);
                             }
+                            ref = r_new;
+#pragma unroll
+                            for (int c = 0; c < kSliceCols / 32; ++c) row_terms(v[c], sc, make_float2(-ref, -ref), t2);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) s2[j] = __fadd2_rn(s2[j], t2[j]);
                     }
                 } else {
-                    // column pass: sum over this slice's query rows of 2^(x - lse2[row]);
-                    // rows past the group (last tile only) contribute nothing
-                    const int nvalid = a.rows_g - (tb * BN + slice * kSliceCols);
-                    const float* cv = &t.colv[k][slice * kSliceCols];
-                    if (nvalid >= kSliceCols)
-                        col_accumulate<false>(v, cv, a.scale, nvalid, s2);
-                    else
-                        col_accumulate<true>(v, cv, a.scale, nvalid, s2);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&t.lse_empty[k]);  // colv slot k may be refilled
+                    // column pass: rows past rows_pad read +inf and add nothing
+                    const float lse = lse_n0;
+                    lse_n0 = lse_n1;
+                    const int r2 = (i + 2) * BM + r_local;
+                    lse_n1 = (i + 2 < a.n_it && r2 < a.rows_pad) ? __ldg(lse_lg + r2) : INFINITY;
+                    const float2 nl = make_float2(-lse, -lse);
+#pragma unroll
+                    for (int c = 0; c < kSliceCols / 16; ++c) {
+                        float v[16];
+                        tmem_ld16(taddr + 16 * c, v);
+                        tmem_ld_wait();
+                        if (c == kSliceCols / 16 - 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&t.acc_empty[k]);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; j += 2) {
+                            const float2 x = __ffma2_rn(make_float2(v[j], v[j + 1]), sc, nl);
+                            cs[c * 8 + j / 2] = __fadd2_rn(cs[c * 8 + j / 2], make_float2(ex2(x.x), ex2(x.y)));
+                        }
+                    }
                 }
                 ++acc_it;
             }
             if (!(ok = epi_bar_and(ok))) break;
-            // merge the column slices of each lane, in slice order
-            const float s_part = (s2[0].x + s2[0].y) + (s2[1].x + s2[1].y) + (s2[2].x + s2[2].y) + (s2[3].x + s2[3].y);
-            t.red[slice][r_local][0] = m_run;
-            t.red[slice][r_local][1] = s_part;
-            epi_bar();
-            if (slice == 0) {
-                if (a.mode == 0) {
-                    const int row = ta * BM + r_local;
+            if (MODE == 0) {
+                // merge the column slices of each row, in slice order
+                const float s_part =
+                    (s2[0].x + s2[0].y) + (s2[1].x + s2[1].y) + (s2[2].x + s2[2].y) + (s2[3].x + s2[3].y);
+                t.red[slice][r_local][0] = ref;
+                t.red[slice][r_local][1] = s_part;
+                epi_bar();
+                if (slice == 0) {
+                    const int row = o * BM + r_local;
                     if (row >= a.rows_g && row < a.rows_pad) a.lse2[(int64_t)lg * a.rows_pad + row] = INFINITY;
                     if (row < a.rows_g) {
                         float m = -INFINITY;
@@ -508,14 +525,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         a.lse2[(int64_t)lg * a.rows_pad + row] = sum > 0.f ? m + __log2f(sum) : -INFINITY;
                     }
-                } else {
-                    const int b = a.c0 + ta * BM + r_local;
-                    if (b < a.c1) {
-                        float sum = 0.f;
+                }
+            } else {
+                // sum each column over the warp's rows, then over the four lane quarters
+                float f[kSliceCols];
 #pragma unroll
-                        for (int j = 0; j < kSlices; ++j) sum += t.red[j][r_local][1];
-                        a.mass[(int64_t)lg * a.n_blocks + b] = sum;
-                    }
+                for (int j = 0; j < kSliceCols / 2; ++j) {
+                    f[2 * j] = cs[j].x;
+                    f[2 * j + 1] = cs[j].y;
+                }
+                column_reduce(f, lane);
+                float* red = &t.red[0][0][0];  // [kSlices][4][kSliceCols]
+                red[(slice * 4 + q) * kSliceCols + 2 * lane] = f[0];
+                red[(slice * 4 + q) * kSliceCols + 2 * lane + 1] = f[1];
+                epi_bar();
+                if (etid < kAccCols) {
+                    const int sl = etid / kSliceCols, cc = etid % kSliceCols;
+                    const float* rc = red + sl * 4 * kSliceCols + cc;
+                    const float sum = ((rc[0] + rc[kSliceCols]) + rc[2 * kSliceCols]) + rc[3 * kSliceCols];
+                    const int b = a.c0 + o * kAccCols + etid;
+                    if (b < a.c1) a.mass[(int64_t)lg * a.n_blocks + b] = sum;
                 }
             }
             epi_bar();
@@ -599,13 +628,13 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
     float* mass = R_partial ? R_partial : reinterpret_cast<float*>(w);
 
     if (ncand > 0) {
-        CUtensorMap qA, qB, iA, iB;
+        CUtensorMap q128, i256;
         const uint64_t q_rows = (uint64_t)L * Hq * M, i_rows = (uint64_t)LH * Bcap;
-        if (!make_map(&qA, q, q_rows, BM) || !make_map(&qB, q, q_rows, BN) || !make_map(&iA, index, i_rows, BM) ||
-            !make_map(&iB, index, i_rows, BN))
-            return cudaErrorInvalidValue;
-        cudaError_t e = cudaFuncSetAttribute(block_scores_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (!make_map(&q128, q, q_rows, BM) || !make_map(&i256, index, i_rows, kAccCols)) return cudaErrorInvalidValue;
+        cudaError_t e = cudaFuncSetAttribute(block_scores_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(block_scores_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         TcArgs a;
         a.rows_g = rows_g;
@@ -618,20 +647,18 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
         a.lse2 = lse2;
         a.mass = mass;
         a.err = ctx->dev_err;
-        // row pass
-        a.mode = 0;
+        // row pass: a unit per 128 query rows, the candidate blocks streamed 256 at a time
         a.units_per_lg = (rows_g + BM - 1) / BM;
         a.n_units = LH * a.units_per_lg;
-        a.n_bt = (ncand + BN - 1) / BN;
+        a.n_it = (ncand + kAccCols - 1) / kAccCols;
         int grid = a.n_units < ctx->num_sms ? a.n_units : ctx->num_sms;
-        block_scores_tc<<<grid, kThreads, kSmemBytes, s>>>(qA, iB, a);
-        // column pass
-        a.mode = 1;
-        a.units_per_lg = (ncand + BM - 1) / BM;
+        block_scores_tc<0><<<grid, kThreads, kSmemBytes, s>>>(q128, i256, a);
+        // column pass: a unit per 256 candidate blocks, the query rows streamed 128 at a time
+        a.units_per_lg = (ncand + kAccCols - 1) / kAccCols;
         a.n_units = LH * a.units_per_lg;
-        a.n_bt = (rows_g + BN - 1) / BN;
+        a.n_it = (rows_g + BM - 1) / BM;
         grid = a.n_units < ctx->num_sms ? a.n_units : ctx->num_sms;
-        block_scores_tc<<<grid, kThreads, kSmemBytes, s>>>(iA, qB, a);
+        block_scores_tc<1><<<grid, kThreads, kSmemBytes, s>>>(i256, q128, a);
     }
     bs_finalize<<<(n_blocks + 255) / 256, 256, 0, s>>>(mass, mass, R, LH, n_blocks, c0, c1,
                                                        1.0f / ((float)L * (float)Hq));

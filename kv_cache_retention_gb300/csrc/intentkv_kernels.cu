@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(kWarps * 32, KVSEL_RULE_MINB) rule_logits_kern
     const int per_layer = (a.n_sub + a.R - 1) / a.R;
     const uint64_t pol_z = kvsel_ptx::policy_evict_last();
 
-    TaskCursor cur{blockIdx.x * a.items_per_block, warp - kWarps, 0, 0, 0};
+    TaskCursor cur{(int)blockIdx.x * a.items_per_block, warp - kWarps, 0, 0, 0};
     if (!cur.next(a, item1, warp, tasks, per_layer)) return;
     TaskCursor nxt = cur;
     bool have_nxt = nxt.next(a, item1, warp, tasks, per_layer);
