@@ -320,8 +320,9 @@ def ours(args, rank, world, local_rank):
 # DRAM bytes (read + write) per call from an ncu capture of the current kernel code, scaled to the
 # bench workload; an entry is removed whenever its kernel changes.  Source: profiles/*.md.
 PROFILED_TRAFFIC = {
-    # block_scores_tc, 4-layer capture (357.4 + 359.5 MB for the two passes) x 16 layers groups
-    # (no current capture: the kernel changed since the last one)
+    # block_scores_tc, 4-layer capture of both passes (357.2 + 361.5 MB), x16 for 64 layers;
+    # profiles/block_scores_tc_ws1m_L4.md
+    "block_scores": 16 * (357.154816 + 361.484032) * 1e6,
 }
 
 
@@ -440,6 +441,110 @@ def profile_case(args):
     print(json.dumps({"profile_case": name, "layers": args.profile_layers, "ms_per_call": ms}), flush=True)
 
 
+def all_configs(args):
+    """One JSON line per workload: per-call device times of its select step
+    (CUDA events, mean over --steps after --warmup), rows/s and the roofline
+    fraction of its bandwidth- or tensor-bound calls.  Token workloads run the
+    IntentKV step, block workloads the KVMEM step (full Mean-K build when the
+    workload is not incremental; the scatter then reads the raw K of the
+    selected blocks)."""
+    import torch
+
+    import kv_cache_retention_gb300 as kv
+    from kv_cache_retention_gb300 import synth
+
+    torch.cuda.set_device(0)
+    ctx = kv.Context(0)
+    peaks = _peaks()
+
+    def timed(calls):
+        for _ in range(args.warmup):
+            for _, fn in calls:
+                fn()
+        torch.cuda.synchronize()
+        ev = {}
+        for _ in range(args.steps):
+            for name, fn in calls:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                ev.setdefault(name, []).append((a, b))
+        torch.cuda.synchronize()
+        ctx.check_device()
+        return {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in ev.items()}
+
+    def frac(bound, amount, ms):
+        if bound == "hbm":
+            ach = amount / (ms / 1e3) / 1e9
+            return {"achieved_GBs": ach, "frac_hbm": ach / peaks["hbm_gbs"]}
+        ach = amount / (ms / 1e3) / 1e12
+        return {"achieved_TFLOPs": ach, "frac_tensor_sustained": ach / peaks["bf16_tflops_sustained"]}
+
+    for name, tw in synth.TOKEN.items():
+        t = synth.token_inputs(tw, "cuda")
+        M = torch.zeros((tw.L, tw.Hq, tw.D), device="cuda")
+        for i in range(tw.turns - 1):
+            ctx.memory_update(t["turns"][i], tw.lam, M, first_turn=(i == 0))
+        q_last = t["turns"][tw.turns - 1].contiguous()
+        rule = torch.empty(tw.N, device="cuda")
+        keep = torch.empty(tw.N, device="cuda", dtype=torch.uint8)
+        keep_idx = torch.empty(tw.N, device="cuda", dtype=torch.int32)
+        smap = t["slot_map"] if t["slot_map"] is not None else torch.arange(tw.N, device="cuda", dtype=torch.int32)
+        slot_out = torch.empty(tw.N, device="cuda", dtype=torch.int32)
+        calls = [
+            ("memory_update", lambda: ctx.memory_update(q_last, tw.lam, M)),
+            ("rule_scores", lambda: ctx.rule_scores(t["pool"], M, tw.L, tw.Hq, tw.Hkv, tw.N, tw.D, tw.pi, tw.q_s,
+                                                    tw.q_e, rule, slot_map=t["slot_map"], n_slots=tw.N)),
+            ("topk_retain", lambda: ctx.topk_retain(rule, tw.pi, tw.q_s, tw.q_e, tw.C, keep=keep, keep_idx=keep_idx)),
+            ("redirect_slots", lambda: ctx.redirect_slots(smap, keep, tw.dead_slot, slot_out)),
+        ]
+        ms = timed(calls)
+        es = 2 if tw.dtype == "bf16" else 4
+        rows = tw.L * tw.Hkv * tw.n_cand
+        line = {"workload": tw.name, "kind": "IntentKV token step", "us_per_select_step": 1e3 * sum(ms.values()),
+                "rows_scored_per_s": rows / (sum(ms.values()) / 1e3), "ms": ms,
+                "rule_scores": frac("hbm", tw.L * tw.n_cand * tw.Hkv * tw.D * es + tw.N * 4, ms["rule_scores"])}
+        print(json.dumps(line), flush=True)
+        del t, M
+        torch.cuda.empty_cache()
+
+    for name, bw in synth.BLOCK.items():
+        b = synth.block_inputs(bw, "cuda")
+        R = torch.empty(bw.n_blocks, device="cuda")
+        ids = torch.empty(bw.n_sel, device="cuda", dtype=torch.int32)
+        n_top = min(bw.k, bw.n_cand)
+        if bw.incremental:
+            src_block, dst_page, dst_pos0 = synth.scatter_plan_incremental(bw, b["page_perm"])
+            build = lambda: ctx.meank_build(b["raw"], bw.block, b["index"], first_block=bw.first_new_block)  # noqa: E731
+            scatter = lambda: ctx.rerope_scatter(b["staging"], src_block, dst_page, dst_pos0, b["pool"],  # noqa: E731
+                                                 bw.rope_base)
+            built_tokens, moved_blocks = bw.new_tokens, n_top
+        else:
+            dst_page, dst_pos0 = synth.scatter_plan_full(bw, b["page_perm"])
+            build = lambda: ctx.meank_build(b["raw"], bw.block, b["index"])  # noqa: E731
+            scatter = lambda: ctx.rerope_scatter(b["raw"], ids, dst_page, dst_pos0, b["pool"], bw.rope_base)  # noqa: E731
+            built_tokens, moved_blocks = bw.n_blocks * bw.block, bw.n_sel
+        calls = [
+            ("meank_build", build),
+            ("block_scores", lambda: ctx.block_scores(b["q"], b["index"], bw.n_blocks, bw.n_sink, bw.n_recent, R)),
+            ("select_blocks", lambda: ctx.select_blocks(R, bw.n_sink, bw.n_recent, bw.k, ids)),
+            ("rerope_scatter", scatter),
+        ]
+        ms = timed(calls)
+        rows = bw.L * bw.Hkv * bw.n_cand
+        build_bytes = bw.L * bw.Hkv * (built_tokens + built_tokens // bw.block) * bw.D * 2
+        line = {"workload": bw.name, "kind": "KVMEM block step", "us_per_select_step": 1e3 * sum(ms.values()),
+                "rows_scored_per_s": rows / (sum(ms.values()) / 1e3), "ms": ms,
+                "meank_build": frac("hbm", build_bytes, ms["meank_build"]),
+                "block_scores": frac("tensor", 2 * bw.L * bw.Hq * bw.M * bw.n_cand * bw.D, ms["block_scores"]),
+                "rerope_scatter": frac("hbm", 2 * bw.L * bw.Hkv * moved_blocks * bw.block * bw.D * 2,
+                                       ms["rerope_scatter"])}
+        print(json.dumps(line), flush=True)
+        del b
+        torch.cuda.empty_cache()
+
+
 def run_step_only(ctx, s, name, ev):
     """Run only the call `name` of the step (for profiling captures)."""
     tw, bw = s["tw"], s["bw"]
@@ -476,7 +581,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-kernel", default=None, help="run only this call on a cut-down case (for ncu)")
     ap.add_argument("--profile-layers", type=int, default=4)
+    ap.add_argument("--all-configs", action="store_true", help="time the select step of every workload, one line each")
     args = ap.parse_args()
+    if args.all_configs:
+        all_configs(args)
+        return
     if args.profile_kernel:
         profile_case(args)
         return
