@@ -72,6 +72,10 @@ def _load():
             lib.orc_select_blocks.argtypes = [P, I, I, I, I, P]
             lib.orc_select_blocks.restype = I
             lib.orc_rerope_scatter.argtypes = [P, I64, I64, P, P, P, I, I, I, I, I, D, I, P, I]
+            lib.orc_workset_diff.argtypes = [P, P, I, P, I, I, I, P, P, P, P, P, P, P, P]
+            lib.orc_workset_diff.restype = I
+            lib.orc_restore_blocks.argtypes = [P, P, I64, I64, P, P, P, I, I, I, I, I, D, I, P, P, I]
+            lib.orc_rerope_shift.argtypes = [P, I, P, P, I, I, I, I, I, D, I]
             _lib = lib
     return _lib
 
@@ -254,4 +258,70 @@ def rerope_scatter(k_src, src_block, dst_page, dst_pos0, pool, page, rope_base,
     lib.orc_rerope_scatter(_ptr(k), int(src_layer_stride), int(src_head_stride), _ptr(sb), _ptr(dp),
                            _ptr(d0), sb.size, L, Hkv, D, page, float(rope_base), int(rope_style),
                            _ptr(out), P)
+    return out
+
+
+def workset_diff(prev_ids, prev_pages, new_ids, P, page):
+    """Differential working-set update (KVMEM restore path).
+
+    Returns a dict with new_pages, shift [n_new]; in_rank, in_page (incoming);
+    mv_rank, mv_shift (retained blocks whose position moved); out_page
+    (released pages).  Raises ValueError when the pool has too few free pages."""
+    lib = _load()
+    pi = _c(prev_ids, np.int32)
+    pp = _c(prev_pages, np.int32)
+    ni = _c(new_ids, np.int32)
+    n_prev, n_new = pi.size, ni.size
+    new_pages = np.zeros(max(n_new, 1), np.int32)
+    shift = np.zeros(max(n_new, 1), np.int32)
+    in_rank = np.zeros(max(n_new, 1), np.int32)
+    in_page = np.zeros(max(n_new, 1), np.int32)
+    mv_rank = np.zeros(max(n_new, 1), np.int32)
+    mv_shift = np.zeros(max(n_new, 1), np.int32)
+    out_page = np.zeros(max(n_prev, 1), np.int32)
+    counts = np.zeros(3, np.int32)
+    rc = lib.orc_workset_diff(_ptr(pi), _ptr(pp), n_prev, _ptr(ni), n_new, int(P), int(page), _ptr(new_pages),
+                              _ptr(shift), _ptr(in_rank), _ptr(in_page), _ptr(mv_rank), _ptr(mv_shift),
+                              _ptr(out_page), _ptr(counts))
+    if rc != 0:
+        raise ValueError("workset_diff: not enough free pages")
+    n_in, n_mv, n_out = (int(c) for c in counts)
+    return {"new_pages": new_pages[:n_new].copy(), "shift": shift[:n_new].copy(),
+            "in_rank": in_rank[:n_in].copy(), "in_page": in_page[:n_in].copy(),
+            "mv_rank": mv_rank[:n_mv].copy(), "mv_shift": mv_shift[:n_mv].copy(),
+            "out_page": out_page[:n_out].copy()}
+
+
+def restore_blocks(k_src, v_src, src_block, dst_page, dst_pos0, k_pool, v_pool, page, rope_base,
+                   rope_style=ROPE_NEOX):
+    """Incoming-block restore: K re-rotated to its compact position, V copied.
+
+    k_src, v_src: bf16 bits [L,Hkv,T,D]; pools bf16 bits [L,P,page,Hkv,D].
+    Returns new (k_pool, v_pool)."""
+    lib = _load()
+    k = _c(k_src, np.uint16)
+    v = _c(v_src, np.uint16)
+    assert k.shape == v.shape
+    ko = np.array(k_pool, dtype=np.uint16, copy=True)
+    vo = np.array(v_pool, dtype=np.uint16, copy=True)
+    L, Hkv, T, D = k.shape
+    P = ko.shape[1]
+    sb = _c(src_block, np.int32)
+    dp = _c(dst_page, np.int32)
+    d0 = _c(dst_pos0, np.int32)
+    lib.orc_restore_blocks(_ptr(k), _ptr(v), Hkv * T * D, T * D, _ptr(sb), _ptr(dp), _ptr(d0), sb.size, L, Hkv, D,
+                           page, float(rope_base), int(rope_style), _ptr(ko), _ptr(vo), P)
+    return ko, vo
+
+
+def rerope_shift(pool, pages, shifts, page, rope_base, rope_style=ROPE_NEOX):
+    """Turn every row of the listed pages by shifts[i] positions; returns a new pool."""
+    lib = _load()
+    out = np.array(pool, dtype=np.uint16, copy=True)
+    L, P, pg, Hkv, D = out.shape
+    assert pg == page
+    pg_ = _c(pages, np.int32)
+    sh = _c(shifts, np.int32)
+    lib.orc_rerope_shift(_ptr(out), P, _ptr(pg_), _ptr(sh), pg_.size, L, Hkv, D, page, float(rope_base),
+                         int(rope_style))
     return out

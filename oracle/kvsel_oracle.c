@@ -436,3 +436,137 @@ void orc_rerope_scatter(const uint16_t* k_src, int64_t src_layer_stride, int64_t
                 }
     free(row);
 }
+
+/* ------------------------------------------------------------------------ */
+/* KVMEM: differential working-set update                                    */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * KVMEM, section "engineering: tiered movement, page-table aliasing and
+ * position-consistent rebuild": only blocks that are selected now (W_t) but
+ * not resident in the GPU page pool (G_{t-1}) are moved in; the retained /
+ * incoming / outgoing split follows the same set difference.
+ *
+ * Readings (the pages give no formula for the split or the page choice):
+ *  - G_{t-1} is the previous working set: prev_ids[n_prev] ascending, block
+ *    prev_ids[r] held in page prev_pages[r] at compact position r * page.
+ *  - retained = W_t n G_{t-1} keep their page; incoming = W_t \ G_{t-1} take
+ *    the free pages of the pool [0, P) -- every page not held by a retained
+ *    block -- in ascending page order, incoming blocks in ascending block id;
+ *    outgoing = G_{t-1} \ W_t release their pages.
+ *  - the new working set new_ids[n_new] is ascending; block new_ids[r] sits at
+ *    compact position r * page, so a retained block whose rank moved from r'
+ *    to r must be turned by shift = (r - r') * page positions.
+ * Outputs: new_pages[r]; shift[r] (0 for incoming); in_rank / in_page: the
+ * incoming ranks ascending and their pages; mv_rank / mv_shift: retained ranks
+ * with a non-zero shift; out_page: the released pages, ascending by block id;
+ * counts[0..2] = (n_incoming, n_moved, n_outgoing).  Returns 0, or -1 when the
+ * pool has too few free pages.
+ */
+int orc_workset_diff(const int32_t* prev_ids, const int32_t* prev_pages, int n_prev, const int32_t* new_ids,
+                     int n_new, int P, int page, int32_t* new_pages, int32_t* shift, int32_t* in_rank,
+                     int32_t* in_page, int32_t* mv_rank, int32_t* mv_shift, int32_t* out_page, int32_t* counts) {
+    uint8_t* held = (uint8_t*)calloc((size_t)(P > 0 ? P : 1), 1);
+    int n_in = 0, n_mv = 0, n_out = 0;
+    /* retained entries: linear search of the previous set */
+    for (int r = 0; r < n_new; ++r) {
+        int found = -1;
+        for (int q = 0; q < n_prev; ++q)
+            if (prev_ids[q] == new_ids[r]) found = q;
+        if (found >= 0) {
+            new_pages[r] = prev_pages[found];
+            shift[r] = (r - found) * page;
+            held[prev_pages[found]] = 1;
+            if (shift[r] != 0) {
+                mv_rank[n_mv] = r;
+                mv_shift[n_mv] = shift[r];
+                ++n_mv;
+            }
+        } else {
+            new_pages[r] = -1;
+            shift[r] = 0;
+        }
+    }
+    /* incoming entries take the free pages in ascending order */
+    int next_free = 0;
+    for (int r = 0; r < n_new; ++r) {
+        if (new_pages[r] >= 0) continue;
+        while (next_free < P && held[next_free]) ++next_free;
+        if (next_free >= P) {
+            free(held);
+            return -1;
+        }
+        new_pages[r] = next_free;
+        held[next_free] = 1;
+        in_rank[n_in] = r;
+        in_page[n_in] = next_free;
+        ++n_in;
+    }
+    /* outgoing entries: previous blocks absent from the new set */
+    for (int q = 0; q < n_prev; ++q) {
+        int kept = 0;
+        for (int r = 0; r < n_new; ++r)
+            if (new_ids[r] == prev_ids[q]) kept = 1;
+        if (!kept) out_page[n_out++] = prev_pages[q];
+    }
+    counts[0] = n_in;
+    counts[1] = n_mv;
+    counts[2] = n_out;
+    free(held);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* KVMEM: restore of incoming blocks (re-RoPE'd K, copied V)                  */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * KVMEM, same section: K is rebuilt from the position-free raw K at the new
+ * compact position; V carries no position and is copied as it is.  K is
+ * exactly orc_rerope_scatter's output; for entry i and token t < page the V
+ * row v_src[l*v_layer_stride + g*v_head_stride + (src_block[i]*page + t)*D + :]
+ * is copied bit for bit to v_pool[l][dst_page[i]][t][g][:].
+ */
+void orc_restore_blocks(const uint16_t* k_src, const uint16_t* v_src, int64_t src_layer_stride,
+                        int64_t src_head_stride, const int32_t* src_block, const int32_t* dst_page,
+                        const int32_t* dst_pos0, int n, int L, int Hkv, int D, int page, double rope_base,
+                        int rope_style, uint16_t* k_pool, uint16_t* v_pool, int P) {
+    orc_rerope_scatter(k_src, src_layer_stride, src_head_stride, src_block, dst_page, dst_pos0, n, L, Hkv, D, page,
+                       rope_base, rope_style, k_pool, P);
+    for (int i = 0; i < n; ++i)
+        for (int l = 0; l < L; ++l)
+            for (int t = 0; t < page; ++t)
+                for (int g = 0; g < Hkv; ++g) {
+                    int64_t sb = (int64_t)l * src_layer_stride + (int64_t)g * src_head_stride +
+                                 ((int64_t)src_block[i] * page + t) * D;
+                    int64_t ob = ((((int64_t)l * P + dst_page[i]) * page + t) * Hkv + g) * D;
+                    for (int d = 0; d < D; ++d) v_pool[ob + d] = v_src[sb + d];
+                }
+}
+
+/* ------------------------------------------------------------------------ */
+/* KVMEM: moving a retained block to its new compact position                */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * A retained block keeps its page (page-table aliasing) but its compact
+ * position moves by shift[i] positions.  RoPE rotations by angles a and b
+ * compose to the rotation by a + b, so the stored K (rotated to its old
+ * position) is turned by shift[i] more positions in place: every row of
+ * pool[l][pages[i]][t][g][:] becomes bf16(R(shift[i]) * row), one rounding.
+ * A negative shift turns backwards.
+ */
+void orc_rerope_shift(uint16_t* pool, int P, const int32_t* pages, const int32_t* shifts, int n, int L, int Hkv,
+                      int D, int page, double rope_base, int rope_style) {
+    double* row = (double*)malloc(sizeof(double) * (size_t)D);
+    for (int i = 0; i < n; ++i)
+        for (int l = 0; l < L; ++l)
+            for (int t = 0; t < page; ++t)
+                for (int g = 0; g < Hkv; ++g) {
+                    int64_t ob = ((((int64_t)l * P + pages[i]) * page + t) * Hkv + g) * D;
+                    for (int d = 0; d < D; ++d) row[d] = orc_bf16_to_double(pool[ob + d]);
+                    orc_rope_rotate(row, D, (double)shifts[i], rope_base, rope_style, 0);
+                    for (int d = 0; d < D; ++d) pool[ob + d] = orc_double_to_bf16(row[d]);
+                }
+    free(row);
+}
