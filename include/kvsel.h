@@ -244,6 +244,68 @@ int kvsel_rerope_scatter(kvsel_ctx* ctx, const void* k_src, int64_t src_layer_st
                          int D, int page, double rope_base, int rope_style, void* pool, int P,
                          void* stream);
 
+/*
+ * Differential working-set update (KVMEM, section "engineering: tiered
+ * movement, page-table aliasing and position-consistent rebuild"): of the new
+ * working set W_t only the blocks that are not resident in the page pool are
+ * moved in.  G_{t-1} is the previous working set prev_ids[n_prev] (ascending
+ * block ids), block prev_ids[r] held in page prev_pages[r] at compact
+ * position r*page; W_t is new_ids[n_new] (ascending), block new_ids[r] at
+ * compact position r*page.
+ *   retained (in both):   new_pages[r] = its old page; shift[r] = (r - old rank)*page
+ *   incoming (new only):  new_pages[r] = the free pages of [0, P) -- every page
+ *                         not held by a retained block -- in ascending order,
+ *                         incoming blocks in ascending id; shift[r] = 0
+ *   outgoing (prev only): its page is released
+ * Outputs (device, int32): new_pages, shift [n_new]; in_rank, in_page [<= n_new]
+ * (the incoming ranks ascending, their pages); mv_rank, mv_shift [<= n_new]
+ * (retained ranks whose shift is non-zero); out_page [<= n_prev] (released
+ * pages, ascending block id); counts[3] = (n_incoming, n_moved, n_outgoing).
+ * Nothing is synchronised: counts stay on the device (see n_dev below).
+ * Requires n_prev, n_new <= P <= 2^20 and P*page < 2^24.  A set that is not
+ * strictly ascending, a previous page outside [0, P) or held twice, or a pool
+ * with too few free pages sets the device error word (kvsel_check_device).
+ */
+int kvsel_workset_diff(kvsel_ctx* ctx, const int32_t* prev_ids, const int32_t* prev_pages, int n_prev,
+                       const int32_t* new_ids, int n_new, int P, int page, int32_t* new_pages,
+                       int32_t* shift, int32_t* in_rank, int32_t* in_page, int32_t* mv_rank,
+                       int32_t* mv_shift, int32_t* out_page, int32_t* counts, void* stream);
+
+/*
+ * Restore of incoming blocks (same KVMEM section): K rebuilt from the raw,
+ * position-free K at the new compact position, exactly as
+ * kvsel_rerope_scatter; V, which carries no position, copied bit for bit.
+ * v_src has k_src's layout and strides; v_pool has pool's layout.  For
+ * entry i < n, token t < page, layer l, kv head g:
+ *   k_pool[l][dst_page[i]][t][g][:] = bf16(RoPE(k_src row, dst_pos0[i] + t))
+ *   v_pool[l][dst_page[i]][t][g][:] = v_src row
+ * n_dev: NULL, or a device int32 count <= n: entries >= *n_dev are skipped, so
+ * that a launch sized for n can follow kvsel_workset_diff without a host sync.
+ * Checks, limits and errors as kvsel_rerope_scatter; both pools must be
+ * 16-byte aligned.
+ */
+int kvsel_restore_blocks(kvsel_ctx* ctx, const void* k_src, const void* v_src, int64_t src_layer_stride,
+                         int64_t src_head_stride, int src_tokens, const int32_t* src_block,
+                         const int32_t* dst_page, const int32_t* dst_pos0, int n, const int32_t* n_dev,
+                         int L, int Hkv, int D, int page, double rope_base, int rope_style, void* k_pool,
+                         void* v_pool, int P, void* stream);
+
+/*
+ * Move retained blocks to their new compact positions in place (page-table
+ * aliasing keeps the page; the K rows must follow the position): every row
+ * pool[l][pages[i]][t][g][:] becomes bf16(R(shifts[i]) * row), the RoPE
+ * rotation by shifts[i] positions (negative: backwards).  Rotations compose,
+ * so a row rotated to position p lands on position p + shifts[i].
+ *   pool    bf16 [L][P][page][Hkv][D], 16-byte aligned
+ *   pages, shifts  int32 [n]; |shift| < 2^24, page < P, else the entry is
+ *           skipped and the device error word is set
+ *   n_dev   NULL or a device count <= n, as in kvsel_restore_blocks
+ * Requires D in {16,32,64,128,256}.  Entries should name distinct pages.
+ */
+int kvsel_rerope_shift(kvsel_ctx* ctx, void* pool, int P, const int32_t* pages, const int32_t* shifts, int n,
+                       const int32_t* n_dev, int L, int Hkv, int D, int page, double rope_base,
+                       int rope_style, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -51,6 +51,10 @@ SIGNATURES = {
     "kvsel_block_scores": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "kvsel_select_blocks": (_I, [_P, _P, _I, _I, _I, _I, _P, _IP, _P]),
     "kvsel_rerope_scatter": (_I, [_P, _P, _I64, _I64, _I, _P, _P, _P, _I, _I, _I, _I, _I, _D, _I, _P, _I, _P]),
+    "kvsel_workset_diff": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "kvsel_restore_blocks": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _D, _I, _P, _P,
+                                  _I, _P]),
+    "kvsel_rerope_shift": (_I, [_P, _P, _I, _P, _P, _I, _P, _I, _I, _I, _I, _D, _I, _P]),
 }
 
 
@@ -151,6 +155,24 @@ def kvsel_rerope_scatter(ctx, k_src, src_layer_stride, src_head_stride, src_toke
                          n, L, Hkv, D, page, rope_base, rope_style, pool, P, stream):
     return _lib.kvsel_rerope_scatter(ctx, k_src, src_layer_stride, src_head_stride, src_tokens, src_block, dst_page,
                                      dst_pos0, n, L, Hkv, D, page, rope_base, rope_style, pool, P, stream)
+
+
+def kvsel_workset_diff(ctx, prev_ids, prev_pages, n_prev, new_ids, n_new, P, page, new_pages, shift, in_rank,
+                       in_page, mv_rank, mv_shift, out_page, counts, stream):
+    return _lib.kvsel_workset_diff(ctx, prev_ids, prev_pages, n_prev, new_ids, n_new, P, page, new_pages, shift,
+                                   in_rank, in_page, mv_rank, mv_shift, out_page, counts, stream)
+
+
+def kvsel_restore_blocks(ctx, k_src, v_src, src_layer_stride, src_head_stride, src_tokens, src_block, dst_page,
+                         dst_pos0, n, n_dev, L, Hkv, D, page, rope_base, rope_style, k_pool, v_pool, P, stream):
+    return _lib.kvsel_restore_blocks(ctx, k_src, v_src, src_layer_stride, src_head_stride, src_tokens, src_block,
+                                     dst_page, dst_pos0, n, n_dev, L, Hkv, D, page, rope_base, rope_style, k_pool,
+                                     v_pool, P, stream)
+
+
+def kvsel_rerope_shift(ctx, pool, P, pages, shifts, n, n_dev, L, Hkv, D, page, rope_base, rope_style, stream):
+    return _lib.kvsel_rerope_shift(ctx, pool, P, pages, shifts, n, n_dev, L, Hkv, D, page, rope_base, rope_style,
+                                   stream)
 
 
 # ---------------------------------------------------------------------------
@@ -294,3 +316,56 @@ class Context:
                                          _ptr(dst_pos0, torch.int32, "dst_pos0"), n, L, Hkv, D, page,
                                          float(rope_base), int(rope_style), _ptr(pool, torch.bfloat16, "pool"), P,
                                          self._stream(stream)))
+
+    def workset_diff(self, prev_ids, prev_pages, new_ids, P, page, out=None, stream=None):
+        """Retained / incoming / outgoing split of a new working set (int32 CUDA tensors).
+
+        Returns a dict of device tensors: new_pages, shift, in_rank, in_page,
+        mv_rank, mv_shift (length n_new, valid prefixes given by counts), out_page
+        (length n_prev) and counts = (n_incoming, n_moved, n_outgoing).  Nothing
+        is synchronised; read counts on the host only when the sizes are needed."""
+        torch = _torch()
+        n_prev, n_new = prev_ids.numel(), new_ids.numel()
+        dev = new_ids.device if n_new else prev_ids.device
+        if out is None:
+            out = {k: torch.empty(max(n_new, 1), dtype=torch.int32, device=dev)
+                   for k in ("new_pages", "shift", "in_rank", "in_page", "mv_rank", "mv_shift")}
+            out["out_page"] = torch.empty(max(n_prev, 1), dtype=torch.int32, device=dev)
+            out["counts"] = torch.zeros(3, dtype=torch.int32, device=dev)
+        i32 = torch.int32
+        self._check(kvsel_workset_diff(
+            self.handle, _ptr(prev_ids, i32, "prev_ids") if n_prev else None,
+            _ptr(prev_pages, i32, "prev_pages") if n_prev else None, n_prev,
+            _ptr(new_ids, i32, "new_ids") if n_new else None, n_new, int(P), int(page),
+            _ptr(out["new_pages"], i32), _ptr(out["shift"], i32), _ptr(out["in_rank"], i32),
+            _ptr(out["in_page"], i32), _ptr(out["mv_rank"], i32), _ptr(out["mv_shift"], i32),
+            _ptr(out["out_page"], i32), _ptr(out["counts"], i32), self._stream(stream)))
+        return out
+
+    def restore_blocks(self, k_src, v_src, src_block, dst_page, dst_pos0, k_pool, v_pool, rope_base,
+                       rope_style=ROPE_NEOX, n=None, n_dev=None, stream=None):
+        """k_src, v_src: bf16 [L][Hkv][T][D] (contiguous, same shape); pools bf16 [L][P][page][Hkv][D]."""
+        torch = _torch()
+        L, Hkv, T, D = k_src.shape
+        if tuple(v_src.shape) != tuple(k_src.shape) or tuple(v_pool.shape) != tuple(k_pool.shape):
+            raise ValueError("restore_blocks: V source and pool must match K's shapes")
+        _, P, page, _, _ = k_pool.shape
+        n = src_block.numel() if n is None else n
+        bf = torch.bfloat16
+        self._check(kvsel_restore_blocks(self.handle, _ptr(k_src, bf, "k_src"), _ptr(v_src, bf, "v_src"), Hkv * T * D,
+                                         T * D, T, _ptr(src_block, torch.int32, "src_block"),
+                                         _ptr(dst_page, torch.int32, "dst_page"),
+                                         _ptr(dst_pos0, torch.int32, "dst_pos0"), n,
+                                         _ptr(n_dev, torch.int32, "n_dev"), L, Hkv, D, page, float(rope_base),
+                                         int(rope_style), _ptr(k_pool, bf, "k_pool"), _ptr(v_pool, bf, "v_pool"), P,
+                                         self._stream(stream)))
+
+    def rerope_shift(self, pool, pages, shifts, rope_base, rope_style=ROPE_NEOX, n=None, n_dev=None, stream=None):
+        """Turn the rows of the listed pages of pool (bf16 [L][P][page][Hkv][D]) by shifts[i] positions."""
+        torch = _torch()
+        L, P, page, Hkv, D = pool.shape
+        n = pages.numel() if n is None else n
+        self._check(kvsel_rerope_shift(self.handle, _ptr(pool, torch.bfloat16, "pool"), P,
+                                       _ptr(pages, torch.int32, "pages"), _ptr(shifts, torch.int32, "shifts"), n,
+                                       _ptr(n_dev, torch.int32, "n_dev"), L, Hkv, D, page, float(rope_base),
+                                       int(rope_style), self._stream(stream)))

@@ -22,6 +22,7 @@ SOURCES = [
     "kvmem_kernels.cu",
     "block_scores.cu",
     "rule_scores_noalloc.cu",
+    "workset_kernels.cu",
 ]
 HEADERS = ["kvsel_internal.h", os.path.join("..", "..", "include", "kvsel.h")]
 

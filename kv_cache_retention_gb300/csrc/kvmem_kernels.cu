@@ -165,12 +165,20 @@ __global__ void __launch_bounds__(256) meank_kernel(const __nv_bfloat16* __restr
 // destination page; each source row is contiguous too.
 constexpr int kLayerGroup = 8;
 
+// Incoming-block restore.  WITH_V also copies the block's V rows (V carries no
+// position) to the same page of v_pool in the same pass.  n_dev, when given, is
+// a device-side entry count: CTAs past it return at once, so a launch sized
+// for the largest count needs no host round trip.
+template <bool WITH_V>
 __global__ void __launch_bounds__(256) rerope_kernel(const __nv_bfloat16* __restrict__ k_src, int64_t sls, int64_t shs,
                                                      int src_tokens, const int32_t* __restrict__ src_block,
                                                      const int32_t* __restrict__ dst_page,
-                                                     const int32_t* __restrict__ dst_pos0, int L, int Hkv, int D,
-                                                     int page, const float2* tlo, const float2* thi, int style,
-                                                     __nv_bfloat16* __restrict__ pool, int P, unsigned* dev_err) {
+                                                     const int32_t* __restrict__ dst_pos0, const int32_t* n_dev,
+                                                     int L, int Hkv, int D, int page, const float2* tlo,
+                                                     const float2* thi, int style, __nv_bfloat16* __restrict__ pool,
+                                                     const __nv_bfloat16* __restrict__ v_src,
+                                                     __nv_bfloat16* __restrict__ v_pool, int P, unsigned* dev_err) {
+    if (n_dev && (int)blockIdx.x >= __ldg(n_dev)) return;
     extern __shared__ float2 cs[];  // [page][D/2]
     const int i = blockIdx.x;
     const int l0 = blockIdx.y * kLayerGroup, l1 = min(L, l0 + kLayerGroup);
@@ -226,6 +234,76 @@ __global__ void __launch_bounds__(256) rerope_kernel(const __nv_bfloat16* __rest
             }
             __stcs(reinterpret_cast<uint4*>(drow + 8 * ca), pack8(xa));
             __stcs(reinterpret_cast<uint4*>(drow + 8 * cb), pack8(xb));
+            if constexpr (WITH_V) {
+                // V: the same two 16-byte chunks of the V row, copied as they are
+                const __nv_bfloat16* vrow = v_src + (srow - k_src);
+                __nv_bfloat16* vdst = v_pool + (drow - pool);
+                __stcs(reinterpret_cast<uint4*>(vdst + 8 * ca), __ldcs(reinterpret_cast<const uint4*>(vrow + 8 * ca)));
+                __stcs(reinterpret_cast<uint4*>(vdst + 8 * cb), __ldcs(reinterpret_cast<const uint4*>(vrow + 8 * cb)));
+            }
+        }
+    }
+}
+
+// In-place move of retained blocks: every row of page pages[i] is turned by
+// shifts[i] positions (negative: backwards), one rounding to bf16.  Grid: one
+// CTA per (entry, group of kLayerGroup layers); the D/2 (cos, sin) pairs of the
+// shift are computed once per CTA.
+__global__ void __launch_bounds__(256) shift_kernel(__nv_bfloat16* __restrict__ pool, int P,
+                                                    const int32_t* __restrict__ pages,
+                                                    const int32_t* __restrict__ shifts, const int32_t* n_dev, int L,
+                                                    int Hkv, int D, int page, const float2* tlo, const float2* thi,
+                                                    int style, unsigned* dev_err) {
+    __shared__ float2 cs[128];  // [D/2]
+    if (n_dev && (int)blockIdx.x >= __ldg(n_dev)) return;
+    const int i = blockIdx.x;
+    const int l0 = blockIdx.y * kLayerGroup, l1 = min(L, l0 + kLayerGroup);
+    const int pg = __ldg(pages + i), sh = __ldg(shifts + i);
+    const int mag = sh < 0 ? -sh : sh;
+    const bool ok_page = pg >= 0 && pg < P, ok_shift = mag < KVSEL_MAX_POS;
+    if (!(ok_page && ok_shift)) {
+        if (threadIdx.x == 0 && blockIdx.y == 0)
+            atomicOr(dev_err, (ok_page ? 0u : (unsigned)KVSEL_DEV_BAD_PAGE) | (ok_shift ? 0u : (unsigned)KVSEL_DEV_BAD_POSITION));
+        return;
+    }
+    const int half = D / 2;
+    for (int idx = threadIdx.x; idx < half; idx += blockDim.x) {
+        const float2 c = rope_cs(tlo, thi, half, mag, idx);
+        cs[idx] = make_float2(c.x, sh < 0 ? -c.y : c.y);  // a backward turn negates the sine
+    }
+    __syncthreads();
+    const int PR = D >> 4;
+    const int total = page * Hkv * PR;
+    for (int l = l0; l < l1; ++l) {
+        __nv_bfloat16* base = pool + ((int64_t)l * P + pg) * (int64_t)page * Hkv * D;
+        for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+            const int cp = idx % PR, r = idx / PR;
+            __nv_bfloat16* row = base + (int64_t)r * D;
+            const int ca = cp, cb = cp + PR;
+            float xa[8], xb[8];
+            unpack8(*reinterpret_cast<const uint4*>(row + 8 * ca), xa);
+            unpack8(*reinterpret_cast<const uint4*>(row + 8 * cb), xb);
+            if (style == KVSEL_ROPE_NEOX) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float2 c = cs[8 * cp + k];
+                    const float a = xa[k], b = xb[k];
+                    xa[k] = fmaf(a, c.x, -b * c.y);
+                    xb[k] = fmaf(b, c.x, a * c.y);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; k += 2) {
+                    const float2 c1 = cs[4 * ca + k / 2], c2 = cs[4 * cb + k / 2];
+                    const float a1 = xa[k], b1 = xa[k + 1], a2 = xb[k], b2 = xb[k + 1];
+                    xa[k] = fmaf(a1, c1.x, -b1 * c1.y);
+                    xa[k + 1] = fmaf(b1, c1.x, a1 * c1.y);
+                    xb[k] = fmaf(a2, c2.x, -b2 * c2.y);
+                    xb[k + 1] = fmaf(b2, c2.x, a2 * c2.y);
+                }
+            }
+            *reinterpret_cast<uint4*>(row + 8 * ca) = pack8(xa);
+            *reinterpret_cast<uint4*>(row + 8 * cb) = pack8(xb);
         }
     }
 }
@@ -253,17 +331,28 @@ cudaError_t launch_meank(const void* k_src, int L, int Hkv, int T, int D, int bl
 }
 
 cudaError_t launch_rerope(const void* k_src, int64_t sls, int64_t shs, int src_tokens, const int32_t* src_block,
-                          const int32_t* dst_page, const int32_t* dst_pos0, int n, int L, int Hkv, int D, int page,
-                          const kvsel_ctx::RopeTab* tab, int rope_style, void* pool, int P, unsigned* dev_err,
-                          cudaStream_t s) {
+                          const int32_t* dst_page, const int32_t* dst_pos0, int n, const int32_t* n_dev, int L,
+                          int Hkv, int D, int page, const kvsel_ctx::RopeTab* tab, int rope_style, void* pool,
+                          const void* v_src, void* v_pool, int P, unsigned* dev_err, cudaStream_t s) {
     const dim3 grid((unsigned)n, (unsigned)((L + kLayerGroup - 1) / kLayerGroup));
     const size_t smem = sizeof(float2) * (size_t)page * (D / 2);
+    auto kern = v_src ? rerope_kernel<true> : rerope_kernel<false>;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(rerope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    rerope_kernel<<<grid, 256, smem, s>>>(static_cast<const __nv_bfloat16*>(k_src), sls, shs, src_tokens,
-                                                 src_block, dst_page, dst_pos0, L, Hkv, D, page, tab->lo, tab->hi,
-                                                 rope_style, static_cast<__nv_bfloat16*>(pool), P, dev_err);
+    kern<<<grid, 256, smem, s>>>(static_cast<const __nv_bfloat16*>(k_src), sls, shs, src_tokens, src_block, dst_page,
+                                 dst_pos0, n_dev, L, Hkv, D, page, tab->lo, tab->hi, rope_style,
+                                 static_cast<__nv_bfloat16*>(pool), static_cast<const __nv_bfloat16*>(v_src),
+                                 static_cast<__nv_bfloat16*>(v_pool), P, dev_err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_shift(void* pool, int P, const int32_t* pages, const int32_t* shifts, int n, const int32_t* n_dev,
+                         int L, int Hkv, int D, int page, const kvsel_ctx::RopeTab* tab, int rope_style,
+                         unsigned* dev_err, cudaStream_t s) {
+    const dim3 grid((unsigned)n, (unsigned)((L + kLayerGroup - 1) / kLayerGroup));
+    shift_kernel<<<grid, 256, 0, s>>>(static_cast<__nv_bfloat16*>(pool), P, pages, shifts, n_dev, L, Hkv, D, page,
+                                      tab->lo, tab->hi, rope_style, dev_err);
     return cudaGetLastError();
 }

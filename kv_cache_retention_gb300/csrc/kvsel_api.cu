@@ -146,11 +146,13 @@ int kvsel_check_device(kvsel_ctx* ctx, void* stream) {
     if (!word) return KVSEL_OK;
     cudaMemset(ctx->dev_err, 0, sizeof(unsigned));
     if (word & KVSEL_DEV_TIMEOUT) return fail(ctx, KVSEL_ERR_TIMEOUT, "a bounded device wait gave up (tensor-core pipeline)");
-    return fail(ctx, KVSEL_ERR_DEVICE_CHECK, "device check failed:%s%s%s%s",
+    return fail(ctx, KVSEL_ERR_DEVICE_CHECK, "device check failed:%s%s%s%s%s%s",
                 (word & KVSEL_DEV_BAD_SLOT) ? " slot out of range" : "",
                 (word & KVSEL_DEV_BAD_POSITION) ? " position out of range" : "",
                 (word & KVSEL_DEV_BAD_BLOCK) ? " source block out of range" : "",
-                (word & KVSEL_DEV_BAD_PAGE) ? " page out of range" : "");
+                (word & KVSEL_DEV_BAD_PAGE) ? " page out of range" : "",
+                (word & KVSEL_DEV_BAD_SET) ? " working set not ascending or page held twice" : "",
+                (word & KVSEL_DEV_POOL_FULL) ? " too few free pages" : "");
 }
 
 int kvsel_memory_update(kvsel_ctx* ctx, const void* q_rows, int q_dtype, int L, int Hq, int R, int D,
@@ -302,8 +304,74 @@ int kvsel_rerope_scatter(kvsel_ctx* ctx, const void* k_src, int64_t src_layer_st
     const kvsel_ctx::RopeTab* tab = kvsel_rope_tables(ctx, D, rope_base, s);
     if (!tab) return fail(ctx, KVSEL_ERR_CUDA, "rerope_scatter: rope table allocation failed");
     return launched(ctx, launch_rerope(k_src, src_layer_stride, src_head_stride, src_tokens, src_block, dst_page, dst_pos0,
-                                       n, L, Hkv, D, page, tab, rope_style, pool, P, ctx->dev_err, s),
+                                       n, nullptr, L, Hkv, D, page, tab, rope_style, pool, nullptr, nullptr, P,
+                                       ctx->dev_err, s),
                     "rerope_scatter launch");
+}
+
+int kvsel_workset_diff(kvsel_ctx* ctx, const int32_t* prev_ids, const int32_t* prev_pages, int n_prev,
+                       const int32_t* new_ids, int n_new, int P, int page, int32_t* new_pages, int32_t* shift,
+                       int32_t* in_rank, int32_t* in_page, int32_t* mv_rank, int32_t* mv_shift, int32_t* out_page,
+                       int32_t* counts, void* stream) {
+    int rc = enter(ctx);
+    if (rc) return rc;
+    if (n_prev < 0 || n_new < 0 || P <= 0 || page <= 0) return fail(ctx, KVSEL_ERR_SHAPE, "workset_diff: bad sizes");
+    if (P > (1 << 20)) return fail(ctx, KVSEL_ERR_UNSUPPORTED, "workset_diff: P=%d > 2^20 pages", P);
+    if (n_prev > P || n_new > P) return fail(ctx, KVSEL_ERR_SHAPE, "workset_diff: a working set larger than the pool");
+    if ((int64_t)P * page >= KVSEL_MAX_POS) return fail(ctx, KVSEL_ERR_SHAPE, "workset_diff: P*page must stay below 2^24 positions");
+    if ((n_prev > 0 && (!prev_ids || !prev_pages || !out_page)) ||
+        (n_new > 0 && (!new_ids || !new_pages || !shift || !in_rank || !in_page || !mv_rank || !mv_shift)) || !counts)
+        return fail(ctx, KVSEL_ERR_INVALID_ARG, "workset_diff: null pointer");
+    return launched(ctx, launch_workset_diff(prev_ids, prev_pages, n_prev, new_ids, n_new, P, page, new_pages, shift,
+                                             in_rank, in_page, mv_rank, mv_shift, out_page, counts, ctx->dev_err,
+                                             (cudaStream_t)stream),
+                    "workset_diff launch");
+}
+
+int kvsel_restore_blocks(kvsel_ctx* ctx, const void* k_src, const void* v_src, int64_t src_layer_stride,
+                         int64_t src_head_stride, int src_tokens, const int32_t* src_block, const int32_t* dst_page,
+                         const int32_t* dst_pos0, int n, const int32_t* n_dev, int L, int Hkv, int D, int page,
+                         double rope_base, int rope_style, void* k_pool, void* v_pool, int P, void* stream) {
+    int rc = enter(ctx);
+    if (rc) return rc;
+    if (!k_src || !v_src || !src_block || !dst_page || !dst_pos0 || !k_pool || !v_pool)
+        return fail(ctx, KVSEL_ERR_INVALID_ARG, "restore_blocks: null pointer");
+    if (n < 0 || L <= 0 || Hkv <= 0 || page <= 0 || P <= 0 || src_tokens < 0) return fail(ctx, KVSEL_ERR_SHAPE, "restore_blocks: bad sizes");
+    if (!pow2_head_dim(D)) return fail(ctx, KVSEL_ERR_UNSUPPORTED, "restore_blocks: D=%d unsupported", D);
+    if ((int64_t)page * D > 16384) return fail(ctx, KVSEL_ERR_UNSUPPORTED, "restore_blocks: page*D=%lld > 16384", (long long)page * D);
+    if (rope_style != KVSEL_ROPE_NEOX && rope_style != KVSEL_ROPE_INTERLEAVED) return fail(ctx, KVSEL_ERR_INVALID_ARG, "restore_blocks: bad rope_style");
+    if (!(rope_base > 1.0)) return fail(ctx, KVSEL_ERR_INVALID_ARG, "restore_blocks: rope_base must be > 1");
+    if (src_head_stride < (int64_t)src_tokens * D || src_layer_stride < 0) return fail(ctx, KVSEL_ERR_SHAPE, "restore_blocks: head stride < src_tokens*D");
+    if (!aligned16(k_src) || !aligned16(v_src) || !aligned16(k_pool) || !aligned16(v_pool) || (src_layer_stride * 2) % 16 ||
+        (src_head_stride * 2) % 16)
+        return fail(ctx, KVSEL_ERR_ALIGN, "restore_blocks: pointers and strides must be 16-byte aligned");
+    if (n == 0) return KVSEL_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    const kvsel_ctx::RopeTab* tab = kvsel_rope_tables(ctx, D, rope_base, s);
+    if (!tab) return fail(ctx, KVSEL_ERR_CUDA, "restore_blocks: rope table allocation failed");
+    return launched(ctx, launch_rerope(k_src, src_layer_stride, src_head_stride, src_tokens, src_block, dst_page, dst_pos0,
+                                       n, n_dev, L, Hkv, D, page, tab, rope_style, k_pool, v_src, v_pool, P,
+                                       ctx->dev_err, s),
+                    "restore_blocks launch");
+}
+
+int kvsel_rerope_shift(kvsel_ctx* ctx, void* pool, int P, const int32_t* pages, const int32_t* shifts, int n,
+                       const int32_t* n_dev, int L, int Hkv, int D, int page, double rope_base, int rope_style,
+                       void* stream) {
+    int rc = enter(ctx);
+    if (rc) return rc;
+    if (!pool || !pages || !shifts) return fail(ctx, KVSEL_ERR_INVALID_ARG, "rerope_shift: null pointer");
+    if (n < 0 || L <= 0 || Hkv <= 0 || page <= 0 || P <= 0) return fail(ctx, KVSEL_ERR_SHAPE, "rerope_shift: bad sizes");
+    if (!pow2_head_dim(D)) return fail(ctx, KVSEL_ERR_UNSUPPORTED, "rerope_shift: D=%d unsupported", D);
+    if (rope_style != KVSEL_ROPE_NEOX && rope_style != KVSEL_ROPE_INTERLEAVED) return fail(ctx, KVSEL_ERR_INVALID_ARG, "rerope_shift: bad rope_style");
+    if (!(rope_base > 1.0)) return fail(ctx, KVSEL_ERR_INVALID_ARG, "rerope_shift: rope_base must be > 1");
+    if (!aligned16(pool)) return fail(ctx, KVSEL_ERR_ALIGN, "rerope_shift: pool must be 16-byte aligned");
+    if (n == 0) return KVSEL_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    const kvsel_ctx::RopeTab* tab = kvsel_rope_tables(ctx, D, rope_base, s);
+    if (!tab) return fail(ctx, KVSEL_ERR_CUDA, "rerope_shift: rope table allocation failed");
+    return launched(ctx, launch_shift(pool, P, pages, shifts, n, n_dev, L, Hkv, D, page, tab, rope_style, ctx->dev_err, s),
+                    "rerope_shift launch");
 }
 
 }  // extern "C"

@@ -34,6 +34,8 @@ enum kvsel_devcheck : unsigned {
     KVSEL_DEV_BAD_POSITION = 1u << 1,
     KVSEL_DEV_BAD_BLOCK = 1u << 2,
     KVSEL_DEV_BAD_PAGE = 1u << 3,
+    KVSEL_DEV_BAD_SET = 1u << 4,   // a working set not ascending, or a page held twice
+    KVSEL_DEV_POOL_FULL = 1u << 5, // fewer free pages than incoming blocks
     KVSEL_DEV_TIMEOUT = 1u << 8,  // a bounded wait inside a kernel gave up
 };
 
@@ -73,10 +75,18 @@ cudaError_t launch_meank(const void* k_src, int L, int Hkv, int T, int D, int bl
                          const int32_t* src_pos, const kvsel_ctx::RopeTab* tab, int rope_style,
                          void* index, int Bcap, unsigned* dev_err, cudaStream_t s);
 
-cudaError_t launch_rerope(const void* k_src, int64_t sls, int64_t shs, int src_tokens,
-                          const int32_t* src_block, const int32_t* dst_page, const int32_t* dst_pos0,
-                          int n, int L, int Hkv, int D, int page, const kvsel_ctx::RopeTab* tab,
-                          int rope_style, void* pool, int P, unsigned* dev_err, cudaStream_t s);
+cudaError_t launch_rerope(const void* k_src, int64_t sls, int64_t shs, int src_tokens, const int32_t* src_block,
+                          const int32_t* dst_page, const int32_t* dst_pos0, int n, const int32_t* n_dev, int L,
+                          int Hkv, int D, int page, const kvsel_ctx::RopeTab* tab, int rope_style, void* pool,
+                          const void* v_src, void* v_pool, int P, unsigned* dev_err, cudaStream_t s);
+cudaError_t launch_shift(void* pool, int P, const int32_t* pages, const int32_t* shifts, int n, const int32_t* n_dev,
+                         int L, int Hkv, int D, int page, const kvsel_ctx::RopeTab* tab, int rope_style,
+                         unsigned* dev_err, cudaStream_t s);
+cudaError_t launch_workset_diff(const int32_t* prev_ids, const int32_t* prev_pages, int n_prev,
+                                const int32_t* new_ids, int n_new, int P, int page, int32_t* new_pages,
+                                int32_t* shift, int32_t* in_rank, int32_t* in_page, int32_t* mv_rank,
+                                int32_t* mv_shift, int32_t* out_page, int32_t* counts, unsigned* dev_err,
+                                cudaStream_t s);
 
 cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index, int L, int Hq, int Hkv,
                                 int M, int D, int n_blocks, int Bcap, int n_sink, int n_recent, float* R,
