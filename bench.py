@@ -545,6 +545,69 @@ def all_configs(args):
         torch.cuda.empty_cache()
 
 
+def restore_pipeline(args):
+    """Throughput of the packed, pipelined host -> device restore (kvsel_stage_restore) at the 1M-workspace
+    dims (L64 Hkv8 D128, 32-token blocks: 4 MiB of K+V per block): 256 blocks restored from a 384-block host
+    repository in shuffled order, per batch size, from pageable and from pinned memory; beside it the
+    host -> device link alone (one pinned copy of the same bytes) and the restore kernel alone (from device
+    memory)."""
+    import numpy as np
+    import torch
+
+    import kv_cache_retention_gb300 as kv
+
+    torch.cuda.set_device(0)
+    ctx = kv.Context(0)
+    L, Hkv, D, page, n_repo, n, P = 64, 8, 128, 32, 384, 256, 2180
+    g = torch.Generator().manual_seed(77)
+    seed_k = torch.randn((L, Hkv, 16 * page, D), generator=g).to(torch.bfloat16)
+    seed_v = torch.randn((L, Hkv, 16 * page, D), generator=g).to(torch.bfloat16)
+    hk = seed_k.repeat(1, 1, n_repo // 16, 1).contiguous()
+    hv = seed_v.repeat(1, 1, n_repo // 16, 1).contiguous()
+    rng = np.random.default_rng(5)
+    blocks = rng.choice(n_repo, n, replace=False).astype(np.int32)
+    pages = rng.choice(P, n, replace=False).astype(np.int32)
+    pos0 = (np.arange(n) * page).astype(np.int32)
+    kp = torch.zeros((L, P, page, Hkv, D), device="cuda", dtype=torch.bfloat16)
+    vp = torch.zeros_like(kp)
+    nbytes = 2 * L * Hkv * n * page * D * 2
+
+    def timed(fn, reps=3):
+        fn()
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            best = min(best, time.perf_counter() - t0)
+        return best
+
+    out = {"workload": "restore 256 of 384 host blocks, L64 Hkv8 D128, 32-token blocks (K+V 4 MiB per block)",
+           "bytes": nbytes, "staged": {}}
+    pk, pv = hk.pin_memory(), hv.pin_memory()
+    for mem, (k_src, v_src) in (("pageable", (hk, hv)), ("pinned", (pk, pv))):
+        for chunk in (4, 16, 64):
+            for threads in (8, 16):
+                sec = timed(lambda: ctx.stage_restore(k_src, v_src, blocks, pages, pos0, kp, vp, 1e6,
+                                                      chunk_blocks=chunk, gather_threads=threads,
+                                                      mode=kv.STAGE_PACKED))
+                out["staged"][f"{mem}_chunk{chunk}_threads{threads}"] = {"ms": 1e3 * sec, "GBs": nbytes / sec / 1e9}
+    sec = timed(lambda: ctx.stage_restore(pk, pv, blocks, pages, pos0, kp, vp, 1e6, mode=kv.STAGE_DIRECT))
+    out["direct_pinned"] = {"ms": 1e3 * sec, "GBs": nbytes / sec / 1e9}
+    ctx.check_device()
+    link_src = torch.empty(nbytes // 2, dtype=torch.bfloat16).pin_memory()
+    link_dst = torch.empty(nbytes // 2, dtype=torch.bfloat16, device="cuda")
+    sec = timed(lambda: link_dst.copy_(link_src, non_blocking=True))
+    out["link_h2d"] = {"ms": 1e3 * sec, "GBs": nbytes / sec / 1e9}
+    dk, dv = hk.cuda(), hv.cuda()
+    sb, dpg, d0 = (torch.as_tensor(a, device="cuda") for a in (blocks, pages, pos0))
+    sec = timed(lambda: ctx.restore_blocks(dk, dv, sb, dpg, d0, kp, vp, 1e6))
+    out["kernel_only"] = {"ms": 1e3 * sec, "GBs": 2 * nbytes / sec / 1e9, "note": "read + write bytes"}
+    ctx.check_device()
+    print(json.dumps(out), flush=True)
+
+
 def run_step_only(ctx, s, name, ev):
     """Run only the call `name` of the step (for profiling captures)."""
     tw, bw = s["tw"], s["bw"]
@@ -582,9 +645,13 @@ def main():
     ap.add_argument("--profile-kernel", default=None, help="run only this call on a cut-down case (for ncu)")
     ap.add_argument("--profile-layers", type=int, default=4)
     ap.add_argument("--all-configs", action="store_true", help="time the select step of every workload, one line each")
+    ap.add_argument("--restore-pipeline", action="store_true", help="throughput of the staged host -> device restore")
     args = ap.parse_args()
     if args.all_configs:
         all_configs(args)
+        return
+    if args.restore_pipeline:
+        restore_pipeline(args)
         return
     if args.profile_kernel:
         profile_case(args)

@@ -63,6 +63,9 @@ typedef enum { KVSEL_F32 = 0, KVSEL_BF16 = 1 } kvsel_dtype;
 /* RoPE pairing: NeoX / rotate-half pairs (i, i + D/2); interleaved (2i, 2i+1). */
 typedef enum { KVSEL_ROPE_NEOX = 0, KVSEL_ROPE_INTERLEAVED = 1 } kvsel_rope_style;
 
+/* How kvsel_stage_restore reaches the host repository (see there). */
+typedef enum { KVSEL_STAGE_AUTO = 0, KVSEL_STAGE_PACKED = 1, KVSEL_STAGE_DIRECT = 2 } kvsel_stage_mode;
+
 /* ------------------------------------------------------------------------ */
 /* context                                                                   */
 /* ------------------------------------------------------------------------ */
@@ -305,6 +308,42 @@ int kvsel_restore_blocks(kvsel_ctx* ctx, const void* k_src, const void* v_src, i
 int kvsel_rerope_shift(kvsel_ctx* ctx, void* pool, int P, const int32_t* pages, const int32_t* shifts, int n,
                        const int32_t* n_dev, int L, int Hkv, int D, int page, double rope_base,
                        int rope_style, void* stream);
+
+/*
+ * Packed and pipelined rematerialisation (KVMEM, same section): restores n
+ * blocks from a HOST repository into the GPU page pools, as
+ * kvsel_restore_blocks would from device memory.  The blocks lie scattered in
+ * the repository; each batch of chunk_blocks blocks is gathered by
+ * gather_threads CPU threads into one contiguous pinned buffer, copied to the
+ * device in one cudaMemcpyAsync on the context's copy stream, and restored by
+ * the K re-RoPE + V copy kernel on `stream`.  Two buffer slots alternate, so
+ * the gather of batch c+1, the copy of batch c and the kernel of batch c-1 run
+ * at the same time.
+ *   host_k, host_v  bf16 [L][Hkv][host_tokens][D] in host memory (pinned or
+ *                   pageable), strides in elements; block b is tokens
+ *                   [b*page, (b+1)*page)
+ *   blocks, dst_page, dst_pos0  HOST int32 [n]: repository block, pool page and
+ *                   first compact position of each entry; all are checked on
+ *                   the host before any work (KVSEL_ERR_SHAPE)
+ *   k_pool, v_pool  device bf16 [L][P][page][Hkv][D], 16-byte aligned
+ * Blocks the host until every batch is gathered and queued (at most two
+ * batches ahead of the GPU); the restore itself completes asynchronously on
+ * `stream`.  The context owns the staging buffers (two slots of the largest
+ * batch, pinned and device) and reuses them across calls.
+ * mode:
+ *   KVSEL_STAGE_AUTO    direct when both repositories are pinned and mapped
+ *                       (cudaHostAlloc / cudaHostRegister), packed otherwise
+ *   KVSEL_STAGE_PACKED  always the packed, pipelined path above
+ *   KVSEL_STAGE_DIRECT  the restore kernel reads the mapped repositories in
+ *                       place (on a Grace host over NVLink-C2C): no CPU gather,
+ *                       no staging copy; KVSEL_ERR_INVALID_ARG if not mapped
+ * Results are identical in every mode.
+ */
+int kvsel_stage_restore(kvsel_ctx* ctx, const void* host_k, const void* host_v, int64_t host_layer_stride,
+                        int64_t host_head_stride, int host_tokens, const int32_t* blocks,
+                        const int32_t* dst_page, const int32_t* dst_pos0, int n, int L, int Hkv, int D,
+                        int page, double rope_base, int rope_style, void* k_pool, void* v_pool, int P,
+                        int chunk_blocks, int gather_threads, int mode, void* stream);
 
 #ifdef __cplusplus
 }

@@ -32,6 +32,9 @@ F32 = 0
 BF16 = 1
 ROPE_NEOX = 0
 ROPE_INTERLEAVED = 1
+STAGE_AUTO = 0    # kvsel_stage_restore: direct when the repository is pinned, else packed
+STAGE_PACKED = 1  # gather into pinned batches, copy, restore (pipelined)
+STAGE_DIRECT = 2  # the restore kernel reads the pinned repository in place
 
 # name -> (restype, argtypes), mirroring include/kvsel.h
 _P, _I, _I64, _F, _D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_double
@@ -55,6 +58,8 @@ SIGNATURES = {
     "kvsel_restore_blocks": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _D, _I, _P, _P,
                                   _I, _P]),
     "kvsel_rerope_shift": (_I, [_P, _P, _I, _P, _P, _I, _P, _I, _I, _I, _I, _D, _I, _P]),
+    "kvsel_stage_restore": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _P, _P, _I, _I, _I, _I, _I, _D, _I, _P, _P, _I,
+                                 _I, _I, _I, _P]),
 }
 
 
@@ -173,6 +178,14 @@ def kvsel_restore_blocks(ctx, k_src, v_src, src_layer_stride, src_head_stride, s
 def kvsel_rerope_shift(ctx, pool, P, pages, shifts, n, n_dev, L, Hkv, D, page, rope_base, rope_style, stream):
     return _lib.kvsel_rerope_shift(ctx, pool, P, pages, shifts, n, n_dev, L, Hkv, D, page, rope_base, rope_style,
                                    stream)
+
+
+def kvsel_stage_restore(ctx, host_k, host_v, host_layer_stride, host_head_stride, host_tokens, blocks, dst_page,
+                        dst_pos0, n, L, Hkv, D, page, rope_base, rope_style, k_pool, v_pool, P, chunk_blocks,
+                        gather_threads, mode, stream):
+    return _lib.kvsel_stage_restore(ctx, host_k, host_v, host_layer_stride, host_head_stride, host_tokens, blocks,
+                                    dst_page, dst_pos0, n, L, Hkv, D, page, rope_base, rope_style, k_pool, v_pool,
+                                    P, chunk_blocks, gather_threads, mode, stream)
 
 
 # ---------------------------------------------------------------------------
@@ -359,6 +372,35 @@ class Context:
                                          _ptr(n_dev, torch.int32, "n_dev"), L, Hkv, D, page, float(rope_base),
                                          int(rope_style), _ptr(k_pool, bf, "k_pool"), _ptr(v_pool, bf, "v_pool"), P,
                                          self._stream(stream)))
+
+    def stage_restore(self, host_k, host_v, blocks, dst_page, dst_pos0, k_pool, v_pool, rope_base,
+                      rope_style=ROPE_NEOX, chunk_blocks=64, gather_threads=None, mode=None, stream=None):
+        """Restore blocks from a host repository (CPU bf16 tensors [L][Hkv][T][D], pinned or not) into the
+        device pools, through the packed, pipelined host -> device staging.  blocks, dst_page and dst_pos0
+        are host int32 arrays (numpy or CPU tensors)."""
+        import numpy as np
+        torch = _torch()
+        for name, t in (("host_k", host_k), ("host_v", host_v)):
+            if t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+                raise ValueError(f"{name}: expected a contiguous CPU bf16 tensor")
+        if tuple(host_v.shape) != tuple(host_k.shape) or tuple(v_pool.shape) != tuple(k_pool.shape):
+            raise ValueError("stage_restore: V repository and pool must match K's shapes")
+        L, Hkv, T, D = host_k.shape
+        _, P, page, _, _ = k_pool.shape
+        arrs = [np.ascontiguousarray(np.asarray(a.cpu() if hasattr(a, "cpu") else a, dtype=np.int32))
+                for a in (blocks, dst_page, dst_pos0)]
+        n = arrs[0].size
+        if any(a.size != n for a in arrs):
+            raise ValueError("stage_restore: blocks, dst_page and dst_pos0 differ in length")
+        ptrs = [a.ctypes.data_as(ctypes.c_void_p) for a in arrs]
+        if gather_threads is None:
+            gather_threads = min(16, os.cpu_count() or 1)
+        self._check(kvsel_stage_restore(self.handle, ctypes.c_void_p(host_k.data_ptr()),
+                                        ctypes.c_void_p(host_v.data_ptr()), Hkv * T * D, T * D, T, ptrs[0], ptrs[1],
+                                        ptrs[2], n, L, Hkv, D, page, float(rope_base), int(rope_style),
+                                        _ptr(k_pool, torch.bfloat16, "k_pool"), _ptr(v_pool, torch.bfloat16, "v_pool"),
+                                        P, int(chunk_blocks), int(gather_threads),
+                                        STAGE_AUTO if mode is None else int(mode), self._stream(stream)))
 
     def rerope_shift(self, pool, pages, shifts, rope_base, rope_style=ROPE_NEOX, n=None, n_dev=None, stream=None):
         """Turn the rows of the listed pages of pool (bf16 [L][P][page][Hkv][D]) by shifts[i] positions."""

@@ -23,6 +23,7 @@ SOURCES = [
     "block_scores.cu",
     "rule_scores_noalloc.cu",
     "workset_kernels.cu",
+    "stage_pipeline.cu",
 ]
 HEADERS = ["kvsel_internal.h", os.path.join("..", "..", "include", "kvsel.h")]
 

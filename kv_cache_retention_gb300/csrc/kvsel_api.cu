@@ -53,6 +53,20 @@ int launched(kvsel_ctx* ctx, cudaError_t e, const char* what) {
 
 }  // namespace
 
+int kvsel_enter(kvsel_ctx* ctx) { return enter(ctx); }
+
+int kvsel_fail(kvsel_ctx* ctx, int code, const char* fmt, ...) {
+    if (ctx) {
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(ctx->err, sizeof ctx->err, fmt, ap);
+        va_end(ap);
+    }
+    return code;
+}
+
+int kvsel_cuda_fail(kvsel_ctx* ctx, cudaError_t e, const char* what) { return cuda_fail(ctx, e, what); }
+
 void* kvsel_workspace(kvsel_ctx* ctx, size_t bytes) {
     if (bytes == 0) bytes = 256;
     if (bytes <= ctx->ws_bytes) return ctx->ws;
@@ -122,6 +136,7 @@ int kvsel_ctx_destroy(kvsel_ctx* ctx) {
     if (!ctx) return KVSEL_OK;
     cudaSetDevice(ctx->device);
     cudaDeviceSynchronize();
+    kvsel_stager_release(ctx);
     if (ctx->ws) cudaFree(ctx->ws);
     if (ctx->dev_err) cudaFree(ctx->dev_err);
     for (int i = 0; i < ctx->n_rope; ++i) {

@@ -25,6 +25,18 @@ struct kvsel_ctx {
     };
     RopeTab rope[8];
     int n_rope = 0;
+    // Host -> device staging of kvsel_stage_restore: two slots of a pinned and a
+    // device buffer, and a copy stream; grown on demand, freed with the context.
+    struct Stager {
+        struct Slot {
+            void* host = nullptr;
+            void* dev = nullptr;
+            cudaEvent_t copied = nullptr;    // the slot's last copy has left the host buffer
+            cudaEvent_t consumed = nullptr;  // the slot's last kernel has read the device buffer
+        } slot[2];
+        cudaStream_t copy_stream = nullptr;
+        size_t capacity = 0;
+    } stager;
     char err[512] = {0};
 };
 
@@ -44,6 +56,14 @@ enum kvsel_devcheck : unsigned {
 #define KVSEL_ROPE_LO (1 << KVSEL_ROPE_LO_BITS)
 #define KVSEL_ROPE_HI (1 << 14)
 #define KVSEL_MAX_POS (KVSEL_ROPE_LO * KVSEL_ROPE_HI)  // 2^24
+
+// Error helpers shared by the translation units that implement calls:
+// entry guard, formatted failure (sets the context's error string), CUDA failure.
+int kvsel_enter(kvsel_ctx* ctx);
+int kvsel_fail(kvsel_ctx* ctx, int code, const char* fmt, ...);
+int kvsel_cuda_fail(kvsel_ctx* ctx, cudaError_t e, const char* what);
+// Frees the staging buffers, events and copy stream of kvsel_stage_restore.
+void kvsel_stager_release(kvsel_ctx* ctx);
 
 // Returns a pointer into the context workspace of at least `bytes` (256-byte
 // aligned), growing it if needed; nullptr on allocation failure.

@@ -255,3 +255,77 @@ def test_restore_step_chain(ctx):
             # a pair's larger component reaches its smaller one, so the bound is in ulps of
             # the pair's norm
             _bf16_within(got_k[:, pg], ref[:, 0], 2, f"moved rank {r}", floor=_pair_mag(raw_rows))
+
+
+# --------------------------------------------------------------------------
+# packed, pipelined host -> device rematerialisation
+# --------------------------------------------------------------------------
+
+def _host_repo(L, Hkv, n_blocks, page, D, seed, pinned):
+    g = torch.Generator().manual_seed(seed)
+    k = torch.randn((L, Hkv, n_blocks * page, D), generator=g).to(torch.bfloat16)
+    v = torch.randn((L, Hkv, n_blocks * page, D), generator=g).to(torch.bfloat16)
+    if pinned:
+        k, v = k.pin_memory(), v.pin_memory()
+    return k, v
+
+
+@pytest.mark.parametrize("chunk,threads,pinned,mode", [(1, 1, False, kv.STAGE_AUTO), (7, 4, False, kv.STAGE_PACKED),
+                                                       (32, 8, True, kv.STAGE_PACKED), (500, 3, True, kv.STAGE_PACKED),
+                                                       (16, 2, True, kv.STAGE_DIRECT), (16, 2, True, kv.STAGE_AUTO)])
+def test_stage_restore_equals_device_restore(ctx, chunk, threads, pinned, mode):
+    """The staged restore from host memory writes exactly what restore_blocks writes from device memory."""
+    L, Hkv, D, page, nrepo, P = 3, 2, 128, 32, 90, 80
+    hk, hv = _host_repo(L, Hkv, nrepo, page, D, chunk, pinned)
+    rng = np.random.default_rng(chunk)
+    n = 60
+    blocks = rng.choice(nrepo, n, replace=False).astype(np.int32)
+    pages = rng.choice(P, n, replace=False).astype(np.int32)
+    pos0 = (rng.permutation(n) * page).astype(np.int32)
+    kp = torch.randn((L, P, page, Hkv, D), device="cuda").to(torch.bfloat16)
+    vp = torch.randn_like(kp)
+    kp2, vp2 = kp.clone(), vp.clone()
+    ctx.stage_restore(hk, hv, blocks, pages, pos0, kp, vp, 1e6, chunk_blocks=chunk, gather_threads=threads, mode=mode)
+    ctx.check_device()
+    ctx.restore_blocks(hk.cuda(), hv.cuda(), _i32(blocks), _i32(pages), _i32(pos0), kp2, vp2, 1e6)
+    ctx.check_device()
+    assert torch.equal(kp, kp2) and torch.equal(vp, vp2)
+    # and a sample against the oracle
+    ref_k, ref_v = oracle.restore_blocks(bits(hk), bits(hv), blocks[:3], pages[:3], pos0[:3],
+                                         np.zeros((L, P, page, Hkv, D), np.uint16),
+                                         np.zeros((L, P, page, Hkv, D), np.uint16), page, 1e6)
+    got_k, got_v = bits(kp), bits(vp)
+    for i in range(3):
+        assert np.array_equal(got_v[:, pages[i]], ref_v[:, pages[i]])
+        raw = bits(hk)[:, :, blocks[i] * page:(blocks[i] + 1) * page].transpose(0, 2, 1, 3)
+        _bf16_within(got_k[:, pages[i]], ref_k[:, pages[i]], 2, f"staged entry {i}", floor=_pair_floor(raw))
+
+
+def test_stage_restore_repeated_calls_and_growth(ctx):
+    """Consecutive calls reuse the staging slots (and grow them) without disturbing queued work."""
+    L, Hkv, D, page, nrepo, P = 2, 2, 64, 16, 40, 40
+    hk, hv = _host_repo(L, Hkv, nrepo, page, D, 99, False)
+    kp = torch.zeros((L, P, page, Hkv, D), device="cuda", dtype=torch.bfloat16)
+    vp = torch.zeros_like(kp)
+    for step, chunk in enumerate((2, 2, 9, 3)):
+        blocks = np.arange(step * 10, step * 10 + 10, dtype=np.int32)
+        ctx.stage_restore(hk, hv, blocks, blocks, blocks * page, kp, vp, 1e4, chunk_blocks=chunk, gather_threads=2)
+    ctx.check_device()
+    # block b went to page b: pool[l][b][t][g] = repository[l][g][b*page + t]
+    assert torch.equal(vp, hv.cuda().permute(0, 2, 1, 3).reshape(L, P, page, Hkv, D))
+
+
+def test_stage_restore_host_checks(ctx):
+    L, Hkv, D, page = 1, 1, 64, 8
+    hk, hv = _host_repo(L, Hkv, 4, page, D, 1, False)
+    kp = torch.zeros((L, 3, page, Hkv, D), device="cuda", dtype=torch.bfloat16)
+    vp = torch.zeros_like(kp)
+    for blocks, pages, pos in (([4], [0], [0]), ([0], [3], [0]), ([0], [0], [2 ** 24 - 4])):
+        with pytest.raises(kv.KvselError):
+            ctx.stage_restore(hk, hv, np.array(blocks, np.int32), np.array(pages, np.int32), np.array(pos, np.int32),
+                              kp, vp, 1e4)
+    assert torch.all(kp == 0) and torch.all(vp == 0)
+    with pytest.raises(kv.KvselError, match="pinned"):  # direct mode on pageable memory is refused on the host
+        ctx.stage_restore(hk, hv, np.array([0], np.int32), np.array([0], np.int32), np.array([0], np.int32), kp, vp,
+                          1e4, mode=kv.STAGE_DIRECT)
+    ctx.check_device()
