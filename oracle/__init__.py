@@ -76,6 +76,8 @@ def _load():
             lib.orc_workset_diff.restype = I
             lib.orc_restore_blocks.argtypes = [P, P, I64, I64, P, P, P, I, I, I, I, I, D, I, P, P, I]
             lib.orc_rerope_shift.argtypes = [P, I, P, P, I, I, I, I, I, D, I]
+            lib.orc_span_keep.argtypes = [P, P, I, P, I, P, I, P]
+            lib.orc_span_keep.restype = I
             _lib = lib
     return _lib
 
@@ -325,3 +327,16 @@ def rerope_shift(pool, pages, shifts, page, rope_base, rope_style=ROPE_NEOX):
     lib.orc_rerope_shift(_ptr(out), P, _ptr(pg_), _ptr(sh), pg_.size, L, Hkv, D, page, float(rope_base),
                          int(rope_style))
     return out
+
+
+def span_keep(span_start, span_end, del_ids, N, keep_in=None):
+    """SideQuest cursor eviction: keep mask with the listed cursors' spans cleared.
+
+    Returns (keep_out uint8 [N], number of ids outside the cursor table)."""
+    lib = _load()
+    ss, se = _c(span_start, np.int32), _c(span_end, np.int32)
+    di = _c(del_ids, np.int32)
+    ki = None if keep_in is None else _c(keep_in, np.uint8)
+    out = np.zeros(max(N, 1), np.uint8)
+    bad = lib.orc_span_keep(_ptr(ss), _ptr(se), ss.size, _ptr(di), di.size, _ptr(ki), int(N), _ptr(out))
+    return out[:N].copy(), int(bad)

@@ -570,3 +570,34 @@ void orc_rerope_shift(uint16_t* pool, int P, const int32_t* pages, const int32_t
                 }
     free(row);
 }
+
+/* ------------------------------------------------------------------------ */
+/* SideQuest: cursor-span eviction as a keep mask                            */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * "SideQuest" page, method overview and Figure 1: the auxiliary thread names
+ * the cursors to delete ({del_cursors: [ids]}); the main thread then clears
+ * those cursors' KV entries.  Cursor c spans positions [span_start[c],
+ * span_end[c]) (readings: half-open spans, clipped to [0, N); spans may
+ * overlap).  The result ANDs into an existing keep mask (keep_in, or all ones
+ * when keep_in is NULL), so it composes with a retention policy and feeds the
+ * dead-slot redirect:
+ *   keep_out[j] = keep_in[j] && j lies in no span of a listed cursor.
+ * Returns the number of listed ids outside [0, n_cursors) (they are ignored).
+ */
+int orc_span_keep(const int32_t* span_start, const int32_t* span_end, int n_cursors, const int32_t* del_ids,
+                  int n_del, const uint8_t* keep_in, int N, uint8_t* keep_out) {
+    int bad = 0;
+    for (int j = 0; j < N; ++j) keep_out[j] = keep_in ? (keep_in[j] != 0) : 1;
+    for (int d = 0; d < n_del; ++d) {
+        int c = del_ids[d];
+        if (c < 0 || c >= n_cursors) {
+            ++bad;
+            continue;
+        }
+        for (int j = span_start[c]; j < span_end[c]; ++j)
+            if (j >= 0 && j < N) keep_out[j] = 0;
+    }
+    return bad;
+}

@@ -1,8 +1,9 @@
 """Pins of the oracle's KVMEM restore path (differential working-set update,
-incoming-block restore, in-place position shift) against what the page and the
-mathematics fix: a hand-worked example, set-partition invariants, degenerate
-cases, an exact V copy checked by indexing, and the composition law of
-rotations.  CPU only."""
+incoming-block restore, in-place position shift) and of SideQuest's
+cursor-span eviction mask against what the pages and the mathematics fix:
+hand-worked examples, set-partition invariants, degenerate cases, an exact V
+copy checked by indexing, the composition law of rotations, and span clearing
+re-done with numpy slices.  CPU only."""
 import json
 import os
 
@@ -168,3 +169,38 @@ def test_rerope_shift_laws(style):
     moved = _f64(oracle.rerope_shift(one, np.array([0], np.int32), np.array([s], np.int32), 1, 1e6, style)[0, 0, 0, 0])
     direct = oracle.rope_rotate(raw, p + s, 1e6, style)
     assert np.allclose(moved, direct, rtol=0, atol=2.0 ** -6 * np.abs(direct).max())
+
+
+# --------------------------------------------------------------------------
+# SideQuest cursor-span eviction
+# --------------------------------------------------------------------------
+
+def test_span_keep_golden():
+    g = json.load(open(os.path.join(GOLDEN, "span_keep_small.json")))
+    out, bad = oracle.span_keep(g["span_start"], g["span_end"], g["del_ids"], g["N"], g["keep_in"])
+    assert out.tolist() == g["keep_out"] and bad == g["bad_ids"]
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_span_keep_invariants(seed):
+    rng = np.random.default_rng(seed)
+    N, n_cur = int(rng.integers(1, 3000)), int(rng.integers(1, 60))
+    start = rng.integers(-20, N + 20, n_cur).astype(np.int32)
+    end = (start + rng.integers(0, 200, n_cur)).astype(np.int32)
+    dels = rng.choice(n_cur + 5, int(rng.integers(0, n_cur)), replace=False).astype(np.int32)
+    keep_in = (rng.random(N) < 0.8).astype(np.uint8)
+    out, bad = oracle.span_keep(start, end, dels, N, keep_in)
+    cleared = np.zeros(N, bool)
+    for c in dels:
+        if c < n_cur:
+            cleared[max(start[c], 0):max(min(end[c], N), 0)] = True
+    assert np.array_equal(out.astype(bool), keep_in.astype(bool) & ~cleared)
+    assert bad == int((dels >= n_cur).sum())
+    # deleting nothing keeps the mask; with no mask given, everything outside the spans is kept
+    same, _ = oracle.span_keep(start, end, np.zeros(0, np.int32), N, keep_in)
+    assert np.array_equal(same, keep_in)
+    ones, _ = oracle.span_keep(start, end, dels, N)
+    assert np.array_equal(ones.astype(bool), ~cleared)
+    # the deletion order does not matter
+    perm, _ = oracle.span_keep(start, end, dels[::-1].copy(), N, keep_in)
+    assert np.array_equal(perm, out)
