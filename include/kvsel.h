@@ -248,6 +248,21 @@ int kvsel_rerope_scatter(kvsel_ctx* ctx, const void* k_src, int64_t src_layer_st
                          void* stream);
 
 /*
+ * Cursor-span eviction ("SideQuest" page, method overview and Figure 1): the
+ * auxiliary thread lists the cursors whose KV entries the main thread clears.
+ *   keep_out[j] = keep_in[j] (1 when keep_in is NULL) AND no listed cursor c has
+ *                 span_start[c] <= j < span_end[c]
+ * Spans are half-open and may overlap or run past [0, N); keep_out may alias
+ * keep_in, so the call can clear spans from an IntentKV keep mask in place
+ * before kvsel_redirect_slots.  Listed ids outside [0, n_cursors) are ignored
+ * and set the device error word.
+ *   span_start, span_end  int32 [n_cursors]; del_ids int32 [n_del]; masks u8 [N]
+ */
+int kvsel_span_keep(kvsel_ctx* ctx, const int32_t* span_start, const int32_t* span_end, int n_cursors,
+                    const int32_t* del_ids, int n_del, const uint8_t* keep_in, int N, uint8_t* keep_out,
+                    void* stream);
+
+/*
  * Differential working-set update (KVMEM, section "engineering: tiered
  * movement, page-table aliasing and position-consistent rebuild"): of the new
  * working set W_t only the blocks that are not resident in the page pool are

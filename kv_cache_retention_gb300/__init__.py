@@ -54,6 +54,7 @@ SIGNATURES = {
     "kvsel_block_scores": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "kvsel_select_blocks": (_I, [_P, _P, _I, _I, _I, _I, _P, _IP, _P]),
     "kvsel_rerope_scatter": (_I, [_P, _P, _I64, _I64, _I, _P, _P, _P, _I, _I, _I, _I, _I, _D, _I, _P, _I, _P]),
+    "kvsel_span_keep": (_I, [_P, _P, _P, _I, _P, _I, _P, _I, _P, _P]),
     "kvsel_workset_diff": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "kvsel_restore_blocks": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _D, _I, _P, _P,
                                   _I, _P]),
@@ -160,6 +161,10 @@ def kvsel_rerope_scatter(ctx, k_src, src_layer_stride, src_head_stride, src_toke
                          n, L, Hkv, D, page, rope_base, rope_style, pool, P, stream):
     return _lib.kvsel_rerope_scatter(ctx, k_src, src_layer_stride, src_head_stride, src_tokens, src_block, dst_page,
                                      dst_pos0, n, L, Hkv, D, page, rope_base, rope_style, pool, P, stream)
+
+
+def kvsel_span_keep(ctx, span_start, span_end, n_cursors, del_ids, n_del, keep_in, N, keep_out, stream):
+    return _lib.kvsel_span_keep(ctx, span_start, span_end, n_cursors, del_ids, n_del, keep_in, N, keep_out, stream)
 
 
 def kvsel_workset_diff(ctx, prev_ids, prev_pages, n_prev, new_ids, n_new, P, page, new_pages, shift, in_rank,
@@ -329,6 +334,17 @@ class Context:
                                          _ptr(dst_pos0, torch.int32, "dst_pos0"), n, L, Hkv, D, page,
                                          float(rope_base), int(rope_style), _ptr(pool, torch.bfloat16, "pool"), P,
                                          self._stream(stream)))
+
+    def span_keep(self, span_start, span_end, del_ids, N, keep_out, keep_in=None, stream=None):
+        """Clear the listed cursors' spans from a keep mask (uint8 CUDA tensors; keep_out may be keep_in)."""
+        torch = _torch()
+        n_cur, n_del = span_start.numel(), del_ids.numel()
+        i32 = torch.int32
+        self._check(kvsel_span_keep(self.handle, _ptr(span_start, i32, "span_start") if n_cur else None,
+                                    _ptr(span_end, i32, "span_end") if n_cur else None, n_cur,
+                                    _ptr(del_ids, i32, "del_ids") if n_del else None, n_del,
+                                    _ptr(keep_in, torch.uint8, "keep_in"), int(N),
+                                    _ptr(keep_out, torch.uint8, "keep_out"), self._stream(stream)))
 
     def workset_diff(self, prev_ids, prev_pages, new_ids, P, page, out=None, stream=None):
         """Retained / incoming / outgoing split of a new working set (int32 CUDA tensors).

@@ -477,6 +477,59 @@ __global__ void redirect_kernel(const int32_t* __restrict__ slot_in, const uint8
         slot_out[j] = keep[j] ? slot_in[j] : dead;
 }
 
+// SideQuest cursor eviction ("SideQuest" page, method overview, Figure 1): the
+// listed cursors' half-open spans [span_start, span_end) are cleared from a keep
+// mask.  Each CTA holds the listed spans in shared memory (in chunks of kSpanChunk)
+// and each thread tests its positions against all of them; keep_out may alias
+// keep_in.  Ids outside the cursor table are ignored and flagged.
+constexpr int kSpanChunk = 2048;
+
+__global__ void __launch_bounds__(256) span_keep_kernel(const int32_t* __restrict__ span_start,
+                                                        const int32_t* __restrict__ span_end, int n_cursors,
+                                                        const int32_t* __restrict__ del_ids, int n_del,
+                                                        const uint8_t* keep_in, int N, uint8_t* keep_out,
+                                                        unsigned* dev_err) {
+    __shared__ int2 spans[kSpanChunk];
+    const int stride = gridDim.x * blockDim.x;
+    const int j0 = blockIdx.x * blockDim.x + threadIdx.x;
+    // positions of this thread: j0, j0 + stride, ... (at most kPer of them)
+    constexpr int kPer = 8;
+    bool keep[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int j = j0 + u * stride;
+        keep[u] = j < N && (keep_in ? keep_in[j] != 0 : true);
+    }
+    for (int c0 = 0; c0 < n_del; c0 += kSpanChunk) {
+        const int nc = min(kSpanChunk, n_del - c0);
+        __syncthreads();
+        for (int d = threadIdx.x; d < nc; d += blockDim.x) {
+            const int c = __ldg(del_ids + c0 + d);
+            int2 sp = make_int2(0, 0);  // empty span for an unknown id
+            if (c >= 0 && c < n_cursors) {
+                sp = make_int2(__ldg(span_start + c), __ldg(span_end + c));
+            } else if (blockIdx.x == 0) {
+                atomicOr(dev_err, (unsigned)KVSEL_DEV_BAD_BLOCK);
+            }
+            spans[d] = sp;
+        }
+        __syncthreads();
+        for (int d = 0; d < nc; ++d) {
+            const int2 sp = spans[d];
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int j = j0 + u * stride;
+                if (j >= sp.x && j < sp.y) keep[u] = false;
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int j = j0 + u * stride;
+        if (j < N) keep_out[j] = keep[u] ? 1 : 0;
+    }
+}
+
 template <int G, bool BF16>
 cudaError_t launch_logits(const RuleArgs& a, int grid, size_t smem, cudaStream_t s) {
     if (smem > 48 * 1024) {
@@ -586,6 +639,15 @@ cudaError_t launch_rule_scores(kvsel_ctx* ctx, const void* k_pool, int dtype, co
     if (smem3 > 48 * 1024)
         cudaFuncSetAttribute(rule_accum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);
     rule_accum_kernel<<<(N + 31) / 32, 256, smem3, s>>>(a.z, lse2, (int)rows, N, pi, q_s, q_e, rule);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_span_keep(const int32_t* span_start, const int32_t* span_end, int n_cursors, const int32_t* del_ids,
+                             int n_del, const uint8_t* keep_in, int N, uint8_t* keep_out, unsigned* dev_err,
+                             cudaStream_t s) {
+    // every position is covered: grid * 256 threads * 8 positions >= N
+    const int grid = (N + 256 * 8 - 1) / (256 * 8);
+    span_keep_kernel<<<grid, 256, 0, s>>>(span_start, span_end, n_cursors, del_ids, n_del, keep_in, N, keep_out, dev_err);
     return cudaGetLastError();
 }
 

@@ -164,7 +164,7 @@ int kvsel_check_device(kvsel_ctx* ctx, void* stream) {
     return fail(ctx, KVSEL_ERR_DEVICE_CHECK, "device check failed:%s%s%s%s%s%s",
                 (word & KVSEL_DEV_BAD_SLOT) ? " slot out of range" : "",
                 (word & KVSEL_DEV_BAD_POSITION) ? " position out of range" : "",
-                (word & KVSEL_DEV_BAD_BLOCK) ? " source block out of range" : "",
+                (word & KVSEL_DEV_BAD_BLOCK) ? " source block or cursor id out of range" : "",
                 (word & KVSEL_DEV_BAD_PAGE) ? " page out of range" : "",
                 (word & KVSEL_DEV_BAD_SET) ? " working set not ascending or page held twice" : "",
                 (word & KVSEL_DEV_POOL_FULL) ? " too few free pages" : "");
@@ -237,6 +237,19 @@ int kvsel_redirect_slots(kvsel_ctx* ctx, const int32_t* slot_in, const uint8_t* 
     if (N < 0) return fail(ctx, KVSEL_ERR_SHAPE, "redirect_slots: negative N");
     if (N == 0) return KVSEL_OK;
     return launched(ctx, launch_redirect(slot_in, keep, N, dead_slot, slot_out, (cudaStream_t)stream), "redirect_slots launch");
+}
+
+int kvsel_span_keep(kvsel_ctx* ctx, const int32_t* span_start, const int32_t* span_end, int n_cursors,
+                    const int32_t* del_ids, int n_del, const uint8_t* keep_in, int N, uint8_t* keep_out, void* stream) {
+    int rc = enter(ctx);
+    if (rc) return rc;
+    if (N < 0 || n_cursors < 0 || n_del < 0) return fail(ctx, KVSEL_ERR_SHAPE, "span_keep: negative size");
+    if (!keep_out || (n_del > 0 && !del_ids) || (n_cursors > 0 && (!span_start || !span_end)))
+        return fail(ctx, KVSEL_ERR_INVALID_ARG, "span_keep: null pointer");
+    if (N == 0) return KVSEL_OK;
+    return launched(ctx, launch_span_keep(span_start, span_end, n_cursors, del_ids, n_del, keep_in, N, keep_out,
+                                          ctx->dev_err, (cudaStream_t)stream),
+                    "span_keep launch");
 }
 
 int kvsel_meank_build(kvsel_ctx* ctx, const void* k_src, int L, int Hkv, int T, int D, int block, int first_block,

@@ -102,6 +102,9 @@ cudaError_t launch_rerope(const void* k_src, int64_t sls, int64_t shs, int src_t
 cudaError_t launch_shift(void* pool, int P, const int32_t* pages, const int32_t* shifts, int n, const int32_t* n_dev,
                          int L, int Hkv, int D, int page, const kvsel_ctx::RopeTab* tab, int rope_style,
                          unsigned* dev_err, cudaStream_t s);
+cudaError_t launch_span_keep(const int32_t* span_start, const int32_t* span_end, int n_cursors, const int32_t* del_ids,
+                             int n_del, const uint8_t* keep_in, int N, uint8_t* keep_out, unsigned* dev_err,
+                             cudaStream_t s);
 cudaError_t launch_workset_diff(const int32_t* prev_ids, const int32_t* prev_pages, int n_prev,
                                 const int32_t* new_ids, int n_new, int P, int page, int32_t* new_pages,
                                 int32_t* shift, int32_t* in_rank, int32_t* in_page, int32_t* mv_rank,

@@ -329,3 +329,54 @@ def test_stage_restore_host_checks(ctx):
         ctx.stage_restore(hk, hv, np.array([0], np.int32), np.array([0], np.int32), np.array([0], np.int32), kp, vp,
                           1e4, mode=kv.STAGE_DIRECT)
     ctx.check_device()
+
+
+# --------------------------------------------------------------------------
+# SideQuest cursor-span eviction: bit-exact
+# --------------------------------------------------------------------------
+
+def test_span_keep_golden(ctx):
+    g = json.load(open(os.path.join(GOLDEN, "span_keep_small.json")))
+    keep_in = torch.tensor(g["keep_in"], dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(keep_in)
+    ctx.span_keep(_i32(g["span_start"]), _i32(g["span_end"]), _i32(g["del_ids"]), g["N"], out, keep_in=keep_in)
+    with pytest.raises(kv.KvselError, match="cursor id"):  # id 7 is not a cursor
+        ctx.check_device()
+    assert out.cpu().tolist() == g["keep_out"]
+
+
+@pytest.mark.parametrize("seed,N,n_cur,n_del", [(0, 92160, 500, 120), (1, 32768, 6000, 5000), (2, 1, 3, 3),
+                                               (3, 70001, 40, 0), (4, 4096, 2, 2)])
+def test_span_keep_parity(ctx, seed, N, n_cur, n_del):
+    rng = np.random.default_rng(seed)
+    start = rng.integers(-50, N + 50, n_cur).astype(np.int32)
+    end = (start + rng.integers(0, 2000, n_cur)).astype(np.int32)
+    dels = rng.choice(n_cur, n_del, replace=False).astype(np.int32)
+    keep_in = (rng.random(N) < 0.7).astype(np.uint8)
+    ref, bad = oracle.span_keep(start, end, dels, N, keep_in)
+    assert bad == 0
+    k = torch.as_tensor(keep_in, device="cuda")
+    ctx.span_keep(_i32(start), _i32(end), _i32(dels), N, k, keep_in=k)  # in place
+    ctx.check_device()
+    assert np.array_equal(k.cpu().numpy(), ref)
+    ones = torch.empty(N, dtype=torch.uint8, device="cuda")
+    ctx.span_keep(_i32(start), _i32(end), _i32(dels), N, ones)
+    ctx.check_device()
+    assert np.array_equal(ones.cpu().numpy(), oracle.span_keep(start, end, dels, N)[0])
+
+
+def test_span_keep_then_redirect(ctx):
+    """An IntentKV keep mask, cleared of the deleted cursors' spans, drives the dead-slot redirect."""
+    N, dead = 10000, 10000
+    rng = np.random.default_rng(8)
+    keep = (rng.random(N) < 0.5).astype(np.uint8)
+    start = np.array([100, 5000, 9990], np.int32)
+    end = np.array([300, 5100, 10010], np.int32)
+    slots = rng.permutation(N).astype(np.int32)
+    k = torch.as_tensor(keep, device="cuda")
+    ctx.span_keep(_i32(start), _i32(end), _i32([0, 2]), N, k, keep_in=k)
+    out = torch.empty(N, dtype=torch.int32, device="cuda")
+    ctx.redirect_slots(_i32(slots), k, dead, out)
+    ctx.check_device()
+    ref_keep, _ = oracle.span_keep(start, end, np.array([0, 2], np.int32), N, keep)
+    assert np.array_equal(out.cpu().numpy(), oracle.redirect_slots(slots, ref_keep, dead))
