@@ -608,6 +608,59 @@ def restore_pipeline(args):
     print(json.dumps(out), flush=True)
 
 
+def block_sweep(args):
+    """Mean-K block size sweep (beta = 16 / 32 / 64) at a fixed history and a fixed token budget: the
+    Mean-K workload's 262,144-token history (L64 Hq40 Hkv8 D128, 512 query tokens), keeping 128 sink and
+    2048 recent tokens plus the top 32,768 tokens' worth of blocks; full Mean-K build, R_b, working set and
+    re-RoPE scatter of the working set per beta (CUDA events, mean over --steps)."""
+    import dataclasses
+
+    import torch
+
+    import kv_cache_retention_gb300 as kv
+    from kv_cache_retention_gb300 import synth
+
+    torch.cuda.set_device(0)
+    ctx = kv.Context(0)
+    base = synth.BLOCK["meank262k"]
+    tokens = base.n_blocks * base.block
+    for beta in (16, 32, 64):
+        bw = dataclasses.replace(base, block=beta, n_blocks=tokens // beta, n_sink=128 // beta,
+                                 n_recent=2048 // beta, k=32768 // beta)
+        b = synth.block_inputs(bw, "cuda")
+        R = torch.empty(bw.n_blocks, device="cuda")
+        ids = torch.empty(bw.n_sel, device="cuda", dtype=torch.int32)
+        dst_page, dst_pos0 = synth.scatter_plan_full(bw, b["page_perm"])
+        calls = [
+            ("meank_build", lambda: ctx.meank_build(b["raw"], bw.block, b["index"])),
+            ("block_scores", lambda: ctx.block_scores(b["q"], b["index"], bw.n_blocks, bw.n_sink, bw.n_recent, R)),
+            ("select_blocks", lambda: ctx.select_blocks(R, bw.n_sink, bw.n_recent, bw.k, ids)),
+            ("rerope_scatter", lambda: ctx.rerope_scatter(b["raw"], ids, dst_page, dst_pos0, b["pool"], bw.rope_base)),
+        ]
+        for _ in range(args.warmup):
+            for _, fn in calls:
+                fn()
+        torch.cuda.synchronize()
+        ev = {}
+        for _ in range(args.steps):
+            for name, fn in calls:
+                a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record()
+                fn()
+                b0.record()
+                ev.setdefault(name, []).append((a0, b0))
+        torch.cuda.synchronize()
+        ctx.check_device()
+        ms = {k: sum(x.elapsed_time(y) for x, y in v) / len(v) for k, v in ev.items()}
+        index_bytes = bw.L * bw.Hkv * bw.n_blocks * bw.D * 2
+        print(json.dumps({"beta": beta, "blocks": bw.n_blocks, "candidates": bw.n_cand, "selected": bw.n_sel,
+                          "index_MB": index_bytes / 1e6, "ms": ms,
+                          "select_step_ms": ms["block_scores"] + ms["select_blocks"] + ms["rerope_scatter"]}),
+              flush=True)
+        del b
+        torch.cuda.empty_cache()
+
+
 def run_step_only(ctx, s, name, ev):
     """Run only the call `name` of the step (for profiling captures)."""
     tw, bw = s["tw"], s["bw"]
@@ -646,7 +699,11 @@ def main():
     ap.add_argument("--profile-layers", type=int, default=4)
     ap.add_argument("--all-configs", action="store_true", help="time the select step of every workload, one line each")
     ap.add_argument("--restore-pipeline", action="store_true", help="throughput of the staged host -> device restore")
+    ap.add_argument("--block-sweep", action="store_true", help="Mean-K block size sweep (16 / 32 / 64 tokens)")
     args = ap.parse_args()
+    if args.block_sweep:
+        block_sweep(args)
+        return
     if args.all_configs:
         all_configs(args)
         return

@@ -76,6 +76,21 @@ def test_memory_update_mode1_and_zero(ctx):
     assert torch.all(Mz == 0)
 
 
+def test_query_mode_ignores_the_session_memory(ctx):
+    """IntentKV's query mode scores with the current query encoding alone: an update with
+    first_turn set gives Enc(q_t)/|Enc(q_t)| whatever the session's memory held."""
+    w = synth.TOKEN["8b"]
+    turns = synth.token_inputs(synth.scaled(w, L=2, N=64, turns=2), "cuda")["turns"]
+    fresh = torch.zeros((2, w.Hq, w.D), device="cuda")
+    used = torch.randn((2, w.Hq, w.D), device="cuda")
+    ctx.memory_update(turns[1], w.lam, fresh, first_turn=True)
+    ctx.memory_update(turns[1], w.lam, used, first_turn=True)
+    assert torch.equal(fresh, used)
+    ref, _ = oracle.memory_update(_host(turns[1]), w.lam, first_turn=True)
+    assert_scores_close(f64(fresh), ref, what="query-mode M")
+    assert torch.allclose(fresh.norm(dim=-1), torch.ones(2, w.Hq, device="cuda"), atol=1e-5)
+
+
 def test_memory_update_ragged_dims(ctx):
     # D=72 (not a power of two), R=3, bf16 rows
     g = torch.Generator(device="cuda").manual_seed(7)
