@@ -661,6 +661,72 @@ def block_sweep(args):
         torch.cuda.empty_cache()
 
 
+def batch_sessions(args):
+    """A serving batch of 36 sessions (8B shape: L36 Hq32 Hkv8 D128, bf16 K in one shared pool of 16-slot
+    pages, N drawn from 1024-8192 per session, 64 query rows per turn, C = N/4): the IntentKV step
+    (QueryMemory update, rule scores, top-C*) as three batched calls, against the same sessions stepped
+    one by one with the single-session calls on the same stream (CUDA events, mean over --steps)."""
+    import numpy as np
+    import torch
+
+    import kv_cache_retention_gb300 as kv
+
+    torch.cuda.set_device(0)
+    ctx = kv.Context(0)
+    S, L, Hq, Hkv, D, page = 36, 36, 32, 8, 128, 16
+    rng = np.random.default_rng(36)
+    Ns = [int(n) for n in rng.integers(1024, 8193, S)]
+    n_slots = sum((n + page - 1) // page for n in Ns) * page
+    pool = torch.empty((L, n_slots, Hkv, D), device="cuda", dtype=torch.bfloat16).normal_()
+    perm = rng.permutation(n_slots // page)
+    smaps, Ms, qs, rules, keeps, forced, Cs = [], [], [], [], [], [], []
+    at = 0
+    for N in Ns:
+        np_ = (N + page - 1) // page
+        pages = perm[at:at + np_]
+        at += np_
+        j = np.arange(N)
+        smaps.append(torch.as_tensor((pages[j // page] * page + j % page).astype(np.int32), device="cuda"))
+        Ms.append(torch.nn.functional.normalize(torch.randn((L, Hq, D), device="cuda"), dim=-1))
+        qs.append(torch.randn((L, Hq, 64, D), device="cuda").to(torch.bfloat16))
+        rules.append(torch.empty(N, device="cuda"))
+        keeps.append(torch.empty(N, dtype=torch.uint8, device="cuda"))
+        forced.append((64, N - 256, N))
+        Cs.append(N // 4)
+
+    def batched():
+        ctx.memory_update_batch(qs, [0.3] * S, Ms)
+        ctx.rule_scores_batch(pool, Ms, L, Hq, Hkv, Ns, D, forced, rules, slot_maps=smaps, n_slots=n_slots)
+        ctx.topk_retain_batch(rules, forced, Cs, keeps)
+
+    def one_by_one():
+        for i in range(S):
+            ctx.memory_update(qs[i], 0.3, Ms[i])
+            ctx.rule_scores(pool, Ms[i], L, Hq, Hkv, Ns[i], D, *forced[i], rules[i], slot_map=smaps[i],
+                            n_slots=n_slots)
+            ctx.topk_retain(rules[i], *forced[i], Cs[i], keep=keeps[i])
+
+    out = {"workload": "36 sessions, L36 Hq32 Hkv8 D128, N 1024-8192 per session", "sessions": S,
+           "tokens": sum(Ns)}
+    rows = sum(L * Hkv * (N - 64 - 256) for N in Ns)
+    for name, fn in (("batched", batched), ("one_by_one", one_by_one)):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        for _ in range(args.steps):
+            fn()
+        b0.record()
+        torch.cuda.synchronize()
+        ms = a0.elapsed_time(b0) / args.steps
+        out[name] = {"ms": ms, "rows_per_s": rows / (ms / 1e3),
+                     "launches": 5 if name == "batched" else 5 * S}
+    ctx.check_device()
+    out["speedup"] = out["one_by_one"]["ms"] / out["batched"]["ms"]
+    print(json.dumps(out), flush=True)
+
+
 def run_step_only(ctx, s, name, ev):
     """Run only the call `name` of the step (for profiling captures)."""
     tw, bw = s["tw"], s["bw"]
@@ -700,7 +766,11 @@ def main():
     ap.add_argument("--all-configs", action="store_true", help="time the select step of every workload, one line each")
     ap.add_argument("--restore-pipeline", action="store_true", help="throughput of the staged host -> device restore")
     ap.add_argument("--block-sweep", action="store_true", help="Mean-K block size sweep (16 / 32 / 64 tokens)")
+    ap.add_argument("--batch-sessions", action="store_true", help="36-session batched IntentKV step vs one by one")
     args = ap.parse_args()
+    if args.batch_sessions:
+        batch_sessions(args)
+        return
     if args.block_sweep:
         block_sweep(args)
         return

@@ -248,6 +248,67 @@ int kvsel_rerope_scatter(kvsel_ctx* ctx, const void* k_src, int64_t src_layer_st
                          void* stream);
 
 /*
+ * Many sessions per call.  A serving batch holds many agent sessions (the
+ * pages' serving runs reach batches of 36) that share the model's shapes and
+ * one paged K pool but differ in N, slot map, query memory, forced set and
+ * budget.  The *_batch calls run the step of every session in one launch per
+ * kernel (grid.y = session) and give, session by session, exactly what the
+ * single-session call gives.  Session tables are host arrays; every pointer
+ * inside them is a device pointer.
+ */
+typedef struct {
+    const void* q_rows;      /* [L][Hq][R][D] post-RoPE query rows of the turn's span (q_dtype) */
+    int R;                   /* rows of the span */
+    float lambda;            /* decay rate */
+    int first_turn;          /* 1: M = Enc(q)/|Enc(q)| (also IntentKV's query mode) */
+    float* M;                /* [L][Hq][D] in/out */
+    float* A;                /* [L][Hq][D] in/out for norm_mode 1, else NULL */
+} kvsel_memory_session;
+
+/*
+ * kvsel_memory_update for S sessions in one launch (q_dtype, L, Hq, D and
+ * norm_mode shared; each session checked as the single call checks it).
+ */
+int kvsel_memory_update_batch(kvsel_ctx* ctx, int q_dtype, int L, int Hq, int D, int norm_mode,
+                              const kvsel_memory_session* sessions, int S, void* stream);
+
+typedef struct {
+    const int32_t* slot_map; /* [N] pool slot of each position, or NULL (identity) */
+    int N;                   /* positions of this session */
+    const float* M;          /* [L][Hq][D] query memory, 16-byte aligned */
+    int pi, q_s, q_e;        /* forced set [0, pi) U [q_s, q_e) */
+    float* rule;             /* [N] out, 16-byte aligned */
+} kvsel_rule_session;
+
+/*
+ * kvsel_rule_scores for S sessions in one launch per kernel.  k_pool, dtype,
+ * n_slots, strides and L, Hq, Hkv, D are shared, as in kvsel_rule_scores; each
+ * session is checked as the single call checks it.  Uses workspace:
+ * sum over sessions of (4*L*Hq*N + 8*L*Hq*ceil(N/64) + 4*L*Hq) bytes plus the
+ * session table.  1 <= S <= 65535.
+ */
+int kvsel_rule_scores_batch(kvsel_ctx* ctx, const void* k_pool, int k_dtype, int n_slots, int L, int Hq,
+                            int Hkv, int D, int64_t layer_stride, int64_t slot_stride,
+                            const kvsel_rule_session* sessions, int S, void* stream);
+
+typedef struct {
+    const float* rule;       /* [N] scores */
+    int N;
+    int pi, q_s, q_e;        /* forced set [0, pi) U [q_s, q_e) */
+    int C;                   /* budget */
+    uint8_t* keep;           /* [N] out or NULL */
+    int32_t* keep_idx;       /* [n_keep] out or NULL (not both NULL) */
+} kvsel_topk_session;
+
+/*
+ * kvsel_topk_retain for S sessions.  Sessions of N <= 131072 share one launch,
+ * one thread-block cluster each; larger ones take the single-CTA kernel.
+ * n_keep_host: NULL or a host int array [S] receiving each session's |keep|.
+ */
+int kvsel_topk_retain_batch(kvsel_ctx* ctx, const kvsel_topk_session* sessions, int S, int* n_keep_host,
+                            void* stream);
+
+/*
  * Cursor-span eviction ("SideQuest" page, method overview and Figure 1): the
  * auxiliary thread lists the cursors whose KV entries the main thread clears.
  *   keep_out[j] = keep_in[j] (1 when keep_in is NULL) AND no listed cursor c has

@@ -39,6 +39,24 @@ STAGE_DIRECT = 2  # the restore kernel reads the pinned repository in place
 # name -> (restype, argtypes), mirroring include/kvsel.h
 _P, _I, _I64, _F, _D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_double
 _IP = ctypes.POINTER(ctypes.c_int)
+class MemorySession(ctypes.Structure):
+    """kvsel_memory_session (include/kvsel.h)."""
+    _fields_ = [("q_rows", ctypes.c_void_p), ("R", ctypes.c_int), ("lam", ctypes.c_float),
+                ("first_turn", ctypes.c_int), ("M", ctypes.c_void_p), ("A", ctypes.c_void_p)]
+
+
+class RuleSession(ctypes.Structure):
+    """kvsel_rule_session (include/kvsel.h)."""
+    _fields_ = [("slot_map", ctypes.c_void_p), ("N", ctypes.c_int), ("M", ctypes.c_void_p), ("pi", ctypes.c_int),
+                ("q_s", ctypes.c_int), ("q_e", ctypes.c_int), ("rule", ctypes.c_void_p)]
+
+
+class TopkSession(ctypes.Structure):
+    """kvsel_topk_session (include/kvsel.h)."""
+    _fields_ = [("rule", ctypes.c_void_p), ("N", ctypes.c_int), ("pi", ctypes.c_int), ("q_s", ctypes.c_int),
+                ("q_e", ctypes.c_int), ("C", ctypes.c_int), ("keep", ctypes.c_void_p), ("keep_idx", ctypes.c_void_p)]
+
+
 SIGNATURES = {
     "kvsel_version": (_I, []),
     "kvsel_ctx_create": (_I, [_I, ctypes.POINTER(_P)]),
@@ -54,6 +72,9 @@ SIGNATURES = {
     "kvsel_block_scores": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "kvsel_select_blocks": (_I, [_P, _P, _I, _I, _I, _I, _P, _IP, _P]),
     "kvsel_rerope_scatter": (_I, [_P, _P, _I64, _I64, _I, _P, _P, _P, _I, _I, _I, _I, _I, _D, _I, _P, _I, _P]),
+    "kvsel_memory_update_batch": (_I, [_P, _I, _I, _I, _I, _I, _P, _I, _P]),
+    "kvsel_rule_scores_batch": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I64, _I64, _P, _I, _P]),
+    "kvsel_topk_retain_batch": (_I, [_P, _P, _I, _P, _P]),
     "kvsel_span_keep": (_I, [_P, _P, _P, _I, _P, _I, _P, _I, _P, _P]),
     "kvsel_workset_diff": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "kvsel_restore_blocks": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _D, _I, _P, _P,
@@ -161,6 +182,20 @@ def kvsel_rerope_scatter(ctx, k_src, src_layer_stride, src_head_stride, src_toke
                          n, L, Hkv, D, page, rope_base, rope_style, pool, P, stream):
     return _lib.kvsel_rerope_scatter(ctx, k_src, src_layer_stride, src_head_stride, src_tokens, src_block, dst_page,
                                      dst_pos0, n, L, Hkv, D, page, rope_base, rope_style, pool, P, stream)
+
+
+def kvsel_memory_update_batch(ctx, q_dtype, L, Hq, D, norm_mode, sessions, S, stream):
+    return _lib.kvsel_memory_update_batch(ctx, q_dtype, L, Hq, D, norm_mode, sessions, S, stream)
+
+
+def kvsel_rule_scores_batch(ctx, k_pool, k_dtype, n_slots, L, Hq, Hkv, D, layer_stride, slot_stride, sessions, S,
+                            stream):
+    return _lib.kvsel_rule_scores_batch(ctx, k_pool, k_dtype, n_slots, L, Hq, Hkv, D, layer_stride, slot_stride,
+                                        sessions, S, stream)
+
+
+def kvsel_topk_retain_batch(ctx, sessions, S, n_keep_host, stream):
+    return _lib.kvsel_topk_retain_batch(ctx, sessions, S, n_keep_host, stream)
 
 
 def kvsel_span_keep(ctx, span_start, span_end, n_cursors, del_ids, n_del, keep_in, N, keep_out, stream):
@@ -334,6 +369,64 @@ class Context:
                                          _ptr(dst_pos0, torch.int32, "dst_pos0"), n, L, Hkv, D, page,
                                          float(rope_base), int(rope_style), _ptr(pool, torch.bfloat16, "pool"), P,
                                          self._stream(stream)))
+
+    # batched sessions ------------------------------------------------------
+
+    def memory_update_batch(self, q_rows_list, lam_list, M_list, first_turn_list=None, norm_mode=0, A_list=None,
+                            stream=None):
+        """One QueryMemory turn for each session: q_rows_list[i] [L][Hq][R_i][D] (same dtype for all)."""
+        torch = _torch()
+        S = len(q_rows_list)
+        if S == 0:
+            return
+        q0 = q_rows_list[0]
+        L, Hq, _, D = q0.shape
+        dt = BF16 if q0.dtype == torch.bfloat16 else F32
+        arr = (MemorySession * S)()
+        for i, q in enumerate(q_rows_list):
+            if q.dtype != q0.dtype or tuple(q.shape[:2]) != (L, Hq) or q.shape[3] != D:
+                raise ValueError("memory_update_batch: sessions must share dtype, L, Hq and D")
+            ft = bool(first_turn_list[i]) if first_turn_list is not None else False
+            A = None if A_list is None else A_list[i]
+            arr[i] = MemorySession(_ptr(q, name="q_rows"), q.shape[2], float(lam_list[i]), int(ft),
+                                   _ptr(M_list[i], torch.float32, "M"), _ptr(A, torch.float32, "A"))
+        self._check(kvsel_memory_update_batch(self.handle, dt, L, Hq, D, int(norm_mode), arr, S, self._stream(stream)))
+
+    def rule_scores_batch(self, k_pool, M_list, L, Hq, Hkv, N_list, D, forced_list, rule_list, slot_maps=None,
+                          n_slots=None, layer_stride=None, slot_stride=None, stream=None):
+        """rule_scores for many sessions on one shared pool; forced_list[i] = (pi, q_s, q_e)."""
+        torch = _torch()
+        S = len(M_list)
+        dt = BF16 if k_pool.dtype == torch.bfloat16 else F32
+        if slot_stride is None:
+            slot_stride = Hkv * D
+        if n_slots is None:
+            n_slots = k_pool.numel() // (L * slot_stride)
+        if layer_stride is None:
+            layer_stride = n_slots * slot_stride
+        arr = (RuleSession * S)()
+        for i in range(S):
+            sm = None if slot_maps is None else slot_maps[i]
+            pi, qs, qe = forced_list[i]
+            arr[i] = RuleSession(_ptr(sm, torch.int32, "slot_map"), int(N_list[i]), _ptr(M_list[i], torch.float32, "M"),
+                                 int(pi), int(qs), int(qe), _ptr(rule_list[i], torch.float32, "rule"))
+        self._check(kvsel_rule_scores_batch(self.handle, _ptr(k_pool, None, "k_pool"), dt, int(n_slots), L, Hq, Hkv, D,
+                                            int(layer_stride), int(slot_stride), arr, S, self._stream(stream)))
+
+    def topk_retain_batch(self, rule_list, forced_list, C_list, keep_list=None, keep_idx_list=None, stream=None):
+        """topk_retain for many sessions; returns the host list of |keep| per session."""
+        torch = _torch()
+        S = len(rule_list)
+        arr = (TopkSession * S)()
+        for i, r in enumerate(rule_list):
+            pi, qs, qe = forced_list[i]
+            keep = None if keep_list is None else keep_list[i]
+            idx = None if keep_idx_list is None else keep_idx_list[i]
+            arr[i] = TopkSession(_ptr(r, torch.float32, "rule"), r.numel(), int(pi), int(qs), int(qe), int(C_list[i]),
+                                 _ptr(keep, torch.uint8, "keep"), _ptr(idx, torch.int32, "keep_idx"))
+        n_keep = (ctypes.c_int * max(S, 1))()
+        self._check(kvsel_topk_retain_batch(self.handle, arr, S, n_keep, self._stream(stream)))
+        return [int(n_keep[i]) for i in range(S)]
 
     def span_keep(self, span_start, span_end, del_ids, N, keep_out, keep_in=None, stream=None):
         """Clear the listed cursors' spans from a keep mask (uint8 CUDA tensors; keep_out may be keep_in)."""

@@ -21,6 +21,8 @@
 //      the logits (coalesced along j), reduced across warps in a fixed order.
 #include <cuda_bf16.h>
 
+#include <vector>
+
 #include "kvsel_internal.h"
 #include "ptx_sm100.cuh"
 
@@ -58,10 +60,29 @@ __device__ __forceinline__ bool is_forced(int j, int pi, int q_s, int q_e) {
 // QueryMemory (Eq. 2)
 // ---------------------------------------------------------------------------
 
+// One turn of one session, for the batched launch (grid.y = session).
+struct MemJob {
+    const void* q;
+    int R;
+    float decay;
+    int first_turn;
+    float* M;
+    float* A;
+};
+
 template <typename T>
 __global__ void __launch_bounds__(256) memory_update_kernel(const T* __restrict__ q, int R, int D, float decay,
                                                             int first_turn, int norm_mode, float* __restrict__ M,
-                                                            float* __restrict__ A) {
+                                                            float* __restrict__ A, const MemJob* __restrict__ batch) {
+    if (batch) {
+        const MemJob& b = batch[blockIdx.y];
+        q = static_cast<const T*>(b.q);
+        R = b.R;
+        decay = b.decay;
+        first_turn = b.first_turn;
+        M = b.M;
+        A = b.A;
+    }
     constexpr int VEC = 16 / sizeof(T);
     extern __shared__ float sm[];  // [rows_per_iter][D] partial sums, then U[D]
     __shared__ float red[32];
@@ -142,6 +163,8 @@ struct RuleArgs {
     int items_per_block;
     float* z;          // [L][Hq][N]
     float2* part;      // [L][Hq][n_sub]
+    float* lse2;       // [L][Hq]
+    float* rule;       // [N] out
     unsigned* dev_err;
     bool aligned32;    // pool base, layer and slot strides are 32-byte aligned
 };
@@ -270,8 +293,12 @@ __device__ __forceinline__ void task_slots(const RuleArgs& a, int sub, int lane,
 // straight from the pool in 32-byte pieces.  A warp streams through its tasks
 // without a block barrier: the last loads of a task already fetch the first
 // pieces of the next one, whose slot-map entries were loaded a task ahead.
-template <int G, bool BF16>
-__global__ void __launch_bounds__(kWarps * 32, KVSEL_RULE_MINB) rule_logits_kernel(const RuleArgs a) {
+// BATCHED: one launch for many sessions; grid.y is the session, batch[s] its
+// arguments, and CTAs past a session's last item find no task.
+template <int G, bool BF16, bool BATCHED>
+__global__ void __launch_bounds__(kWarps * 32, KVSEL_RULE_MINB)
+    rule_logits_kernel(const __grid_constant__ RuleArgs a_in, const RuleArgs* __restrict__ batch) {
+    const RuleArgs& a = BATCHED ? batch[blockIdx.y] : a_in;
     extern __shared__ __align__(16) float Msm[];  // [kWarps][G][D]
     constexpr int ES = BF16 ? 2 : 4;
     constexpr int DPP = 32 / ES;                  // dims per 32-byte piece
@@ -421,11 +448,15 @@ __global__ void __launch_bounds__(kWarps * 32, KVSEL_RULE_MINB) rule_logits_kern
 // Rule scores, pass 2 and 3
 // ---------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(256) rule_lse_kernel(const float2* __restrict__ part, int rows, int n_chunks,
-                                                       float* __restrict__ lse2) {
+template <bool BATCHED>
+__global__ void __launch_bounds__(256) rule_lse_kernel(const __grid_constant__ RuleArgs a_in,
+                                                       const RuleArgs* __restrict__ batch, int rows) {
+    const RuleArgs& a = BATCHED ? batch[blockIdx.y] : a_in;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (warp >= rows) return;
+    const int n_chunks = a.n_sub;
+    const float2* part = a.part;
     float2 acc = make_float2(-INFINITY, 0.f);
     for (int c = lane; c < n_chunks; c += 32) acc = lse_merge(acc, part[(int64_t)warp * n_chunks + c]);
 #pragma unroll
@@ -433,14 +464,21 @@ __global__ void __launch_bounds__(256) rule_lse_kernel(const float2* __restrict_
         float2 other = make_float2(__shfl_xor_sync(kFull, acc.x, o), __shfl_xor_sync(kFull, acc.y, o));
         acc = lse_merge(acc, other);
     }
-    if (lane == 0) lse2[warp] = acc.y > 0.f ? acc.x + log2f(acc.y) : -INFINITY;
+    if (lane == 0) a.lse2[warp] = acc.y > 0.f ? acc.x + log2f(acc.y) : -INFINITY;
 }
 
 // Block = 8 warps x 32 tokens; warp w sums its share of the (l,h) rows for its
 // lane's token; the 8 partial sums are added in warp order.
-__global__ void __launch_bounds__(256) rule_accum_kernel(const float* __restrict__ z, const float* __restrict__ lse2,
-                                                         int rows, int N, int pi, int q_s, int q_e,
-                                                         float* __restrict__ rule) {
+template <bool BATCHED>
+__global__ void __launch_bounds__(256) rule_accum_kernel(const __grid_constant__ RuleArgs a_in,
+                                                         const RuleArgs* __restrict__ batch, int rows) {
+    const RuleArgs& a = BATCHED ? batch[blockIdx.y] : a_in;
+    const int N = a.N;
+    if (BATCHED && (int)blockIdx.x * 32 >= N) return;  // past this session's tokens
+    const float* __restrict__ z = a.z;
+    const float* __restrict__ lse2 = a.lse2;
+    const int pi = a.pi, q_s = a.q_s, q_e = a.q_e;
+    float* __restrict__ rule = a.rule;
     extern __shared__ float s_lse[];  // [rows]
     __shared__ float red[8][32];
     for (int r = threadIdx.x; r < rows; r += blockDim.x) s_lse[r] = lse2[r];
@@ -530,28 +568,28 @@ __global__ void __launch_bounds__(256) span_keep_kernel(const int32_t* __restric
     }
 }
 
-template <int G, bool BF16>
-cudaError_t launch_logits(const RuleArgs& a, int grid, size_t smem, cudaStream_t s) {
+template <int G, bool BF16, bool BATCHED>
+cudaError_t launch_logits(const RuleArgs& a, const RuleArgs* batch, dim3 grid, size_t smem, cudaStream_t s) {
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(rule_logits_kernel<G, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(rule_logits_kernel<G, BF16, BATCHED>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    rule_logits_kernel<G, BF16><<<grid, kWarps * 32, smem, s>>>(a);
+    rule_logits_kernel<G, BF16, BATCHED><<<grid, kWarps * 32, smem, s>>>(a, batch);
     return cudaGetLastError();
 }
 
-template <bool BF16>
-cudaError_t dispatch_logits(int G, const RuleArgs& a, int grid, size_t smem, cudaStream_t s) {
+template <bool BF16, bool BATCHED>
+cudaError_t dispatch_logits(int G, const RuleArgs& a, const RuleArgs* batch, dim3 grid, size_t smem, cudaStream_t s) {
     switch (G) {
-        case 1: return launch_logits<1, BF16>(a, grid, smem, s);
-        case 2: return launch_logits<2, BF16>(a, grid, smem, s);
-        case 3: return launch_logits<3, BF16>(a, grid, smem, s);
-        case 4: return launch_logits<4, BF16>(a, grid, smem, s);
-        case 5: return launch_logits<5, BF16>(a, grid, smem, s);
-        case 6: return launch_logits<6, BF16>(a, grid, smem, s);
-        case 7: return launch_logits<7, BF16>(a, grid, smem, s);
-        case 8: return launch_logits<8, BF16>(a, grid, smem, s);
+        case 1: return launch_logits<1, BF16, BATCHED>(a, batch, grid, smem, s);
+        case 2: return launch_logits<2, BF16, BATCHED>(a, batch, grid, smem, s);
+        case 3: return launch_logits<3, BF16, BATCHED>(a, batch, grid, smem, s);
+        case 4: return launch_logits<4, BF16, BATCHED>(a, batch, grid, smem, s);
+        case 5: return launch_logits<5, BF16, BATCHED>(a, batch, grid, smem, s);
+        case 6: return launch_logits<6, BF16, BATCHED>(a, batch, grid, smem, s);
+        case 7: return launch_logits<7, BF16, BATCHED>(a, batch, grid, smem, s);
+        case 8: return launch_logits<8, BF16, BATCHED>(a, batch, grid, smem, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -573,12 +611,38 @@ cudaError_t launch_memory_update(const void* q, int dtype, int L, int Hq, int R,
         if (smem > 48 * 1024)
             cudaFuncSetAttribute(memory_update_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         memory_update_kernel<__nv_bfloat16><<<heads, 256, smem, s>>>(static_cast<const __nv_bfloat16*>(q), R, D, decay,
-                                                                      first_turn, norm_mode, M, A);
+                                                                      first_turn, norm_mode, M, A, nullptr);
     } else {
         if (smem > 48 * 1024)
             cudaFuncSetAttribute(memory_update_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         memory_update_kernel<float><<<heads, 256, smem, s>>>(static_cast<const float*>(q), R, D, decay, first_turn,
-                                                             norm_mode, M, A);
+                                                             norm_mode, M, A, nullptr);
+    }
+    return cudaGetLastError();
+}
+
+size_t memory_update_batch_workspace(int S) { return (size_t)S * sizeof(MemJob) + 256; }
+
+cudaError_t launch_memory_update_batch(int dtype, int L, int Hq, int D, int norm_mode, const kvsel_memory_session* sess,
+                                       int S, void* ws, cudaStream_t s) {
+    std::vector<MemJob> jobs((size_t)S);
+    for (int i = 0; i < S; ++i)
+        jobs[i] = MemJob{sess[i].q_rows, sess[i].R, expf(-sess[i].lambda), sess[i].first_turn, sess[i].M, sess[i].A};
+    MemJob* dev = static_cast<MemJob*>(ws);
+    cudaError_t e = cudaMemcpyAsync(dev, jobs.data(), (size_t)S * sizeof(MemJob), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return e;
+    const int vec = dtype == KVSEL_BF16 ? 8 : 4;
+    const int rpi = 256 / (D / vec);
+    const size_t smem = sizeof(float) * ((size_t)rpi * D + D);
+    const dim3 grid((unsigned)(L * Hq), (unsigned)S);
+    if (dtype == KVSEL_BF16) {
+        if (smem > 48 * 1024)
+            cudaFuncSetAttribute(memory_update_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        memory_update_kernel<__nv_bfloat16><<<grid, 256, smem, s>>>(nullptr, 0, D, 0.f, 0, norm_mode, nullptr, nullptr, dev);
+    } else {
+        if (smem > 48 * 1024)
+            cudaFuncSetAttribute(memory_update_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        memory_update_kernel<float><<<grid, 256, smem, s>>>(nullptr, 0, D, 0.f, 0, norm_mode, nullptr, nullptr, dev);
     }
     return cudaGetLastError();
 }
@@ -615,7 +679,8 @@ cudaError_t launch_rule_scores(kvsel_ctx* ctx, const void* k_pool, int dtype, co
     w += align256(rows * N * sizeof(float));
     a.part = reinterpret_cast<float2*>(w);
     w += align256(rows * a.n_sub * sizeof(float2));
-    float* lse2 = reinterpret_cast<float*>(w);
+    a.lse2 = reinterpret_cast<float*>(w);
+    a.rule = rule;
     a.dev_err = ctx->dev_err;
     {
         const int64_t es = dtype == KVSEL_BF16 ? 2 : 4;  // row offsets g*D*es are multiples of 32 for D >= 16
@@ -631,14 +696,96 @@ cudaError_t launch_rule_scores(kvsel_ctx* ctx, const void* k_pool, int dtype, co
     const int grid_max = blocks_per_sm * ctx->num_sms;
     a.items_per_block = (a.n_items + grid_max - 1) / grid_max;
     const int grid = (a.n_items + a.items_per_block - 1) / a.items_per_block;
-    cudaError_t e = dtype == KVSEL_BF16 ? dispatch_logits<true>(G, a, grid, smem, s)
-                                        : dispatch_logits<false>(G, a, grid, smem, s);
+    cudaError_t e = dtype == KVSEL_BF16 ? dispatch_logits<true, false>(G, a, nullptr, dim3(grid), smem, s)
+                                        : dispatch_logits<false, false>(G, a, nullptr, dim3(grid), smem, s);
     if (e != cudaSuccess) return e;
-    rule_lse_kernel<<<(int)((rows * 32 + 255) / 256), 256, 0, s>>>(a.part, (int)rows, a.n_sub, lse2);
+    rule_lse_kernel<false><<<(int)((rows * 32 + 255) / 256), 256, 0, s>>>(a, nullptr, (int)rows);
     const size_t smem3 = rows * sizeof(float);
     if (smem3 > 48 * 1024)
-        cudaFuncSetAttribute(rule_accum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);
-    rule_accum_kernel<<<(N + 31) / 32, 256, smem3, s>>>(a.z, lse2, (int)rows, N, pi, q_s, q_e, rule);
+        cudaFuncSetAttribute(rule_accum_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);
+    rule_accum_kernel<false><<<(N + 31) / 32, 256, smem3, s>>>(a, nullptr, (int)rows);
+    return cudaGetLastError();
+}
+
+size_t rule_scores_batch_workspace(int L, int Hq, const kvsel_rule_session* sess, int S) {
+    const size_t rows = (size_t)L * Hq;
+    size_t b = align256((size_t)S * sizeof(RuleArgs));
+    for (int i = 0; i < S; ++i) {
+        const int N = sess[i].N;
+        b += align256(rows * N * sizeof(float)) + align256(rows * rule_chunks(N) * sizeof(float2)) +
+             align256(rows * sizeof(float));
+    }
+    return b;
+}
+
+cudaError_t launch_rule_scores_batch(kvsel_ctx* ctx, const void* k_pool, int dtype, int n_slots, int L, int Hq,
+                                     int Hkv, int D, int64_t layer_stride, int64_t slot_stride,
+                                     const kvsel_rule_session* sess, int S, void* ws, cudaStream_t s) {
+    const size_t rows = (size_t)L * Hq;
+    char* w = static_cast<char*>(ws);
+    RuleArgs* dev_args = reinterpret_cast<RuleArgs*>(w);
+    w += align256((size_t)S * sizeof(RuleArgs));
+    const int64_t es = dtype == KVSEL_BF16 ? 2 : 4;
+    const bool aligned32 = reinterpret_cast<uintptr_t>(k_pool) % 32 == 0 && (layer_stride * es) % 32 == 0 &&
+                           (slot_stride * es) % 32 == 0;
+    const int R = Hkv >= kWarps ? 1 : kWarps / Hkv;
+    std::vector<RuleArgs> args((size_t)S);
+    int64_t total_items = 0;
+    int max_N = 0;
+    for (int i = 0; i < S; ++i) {
+        RuleArgs& a = args[i];
+        a.k_pool = k_pool;
+        a.slot_map = sess[i].slot_map;
+        a.n_slots = n_slots;
+        a.L = L;
+        a.Hq = Hq;
+        a.Hkv = Hkv;
+        a.N = sess[i].N;
+        a.D = D;
+        a.layer_stride = layer_stride;
+        a.slot_stride = slot_stride;
+        a.M = sess[i].M;
+        a.pi = sess[i].pi;
+        a.q_s = sess[i].q_s;
+        a.q_e = sess[i].q_e;
+        a.scale = kLog2e / sqrtf((float)D);
+        a.n_sub = rule_chunks(a.N);
+        a.R = R;
+        a.n_items = L * ((a.n_sub + R - 1) / R);
+        a.z = reinterpret_cast<float*>(w);
+        w += align256(rows * a.N * sizeof(float));
+        a.part = reinterpret_cast<float2*>(w);
+        w += align256(rows * a.n_sub * sizeof(float2));
+        a.lse2 = reinterpret_cast<float*>(w);
+        w += align256(rows * sizeof(float));
+        a.rule = sess[i].rule;
+        a.dev_err = ctx->dev_err;
+        a.aligned32 = aligned32;
+        total_items += a.n_items;
+        max_N = a.N > max_N ? a.N : max_N;
+    }
+    // every CTA gets the same number of items, sized to fill the GPU once over all sessions
+    const int64_t grid_max = (int64_t)KVSEL_RULE_MINB * ctx->num_sms;
+    const int ipb = (int)((total_items + grid_max - 1) / grid_max > 0 ? (total_items + grid_max - 1) / grid_max : 1);
+    int gx = 1;
+    for (auto& a : args) {
+        a.items_per_block = ipb;
+        const int g = (a.n_items + ipb - 1) / ipb;
+        gx = g > gx ? g : gx;
+    }
+    cudaError_t e = cudaMemcpyAsync(dev_args, args.data(), (size_t)S * sizeof(RuleArgs), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return e;
+    const int G = Hq / Hkv;
+    const size_t smem = sizeof(float) * (size_t)kWarps * G * D;
+    e = dtype == KVSEL_BF16 ? dispatch_logits<true, true>(G, args[0], dev_args, dim3(gx, S), smem, s)
+                            : dispatch_logits<false, true>(G, args[0], dev_args, dim3(gx, S), smem, s);
+    if (e != cudaSuccess) return e;
+    rule_lse_kernel<true><<<dim3((unsigned)((rows * 32 + 255) / 256), S), 256, 0, s>>>(args[0], dev_args, (int)rows);
+    const size_t smem3 = rows * sizeof(float);
+    if (smem3 > 48 * 1024)
+        cudaFuncSetAttribute(rule_accum_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);
+    if (max_N > 0)
+        rule_accum_kernel<true><<<dim3((max_N + 31) / 32, S), 256, smem3, s>>>(args[0], dev_args, (int)rows);
     return cudaGetLastError();
 }
 

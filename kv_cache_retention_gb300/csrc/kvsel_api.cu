@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "kvsel_internal.h"
 
@@ -185,6 +186,31 @@ int kvsel_memory_update(kvsel_ctx* ctx, const void* q_rows, int q_dtype, int L, 
     return launched(ctx, launch_memory_update(q_rows, q_dtype, L, Hq, R, D, lambda, first_turn, norm_mode, M, A, (cudaStream_t)stream), "memory_update launch");
 }
 
+int kvsel_memory_update_batch(kvsel_ctx* ctx, int q_dtype, int L, int Hq, int D, int norm_mode,
+                              const kvsel_memory_session* sessions, int S, void* stream) {
+    int rc = enter(ctx);
+    if (rc) return rc;
+    if (S < 0 || S > 65535 || (S > 0 && !sessions)) return fail(ctx, KVSEL_ERR_INVALID_ARG, "memory_update_batch: bad session table");
+    if (q_dtype != KVSEL_F32 && q_dtype != KVSEL_BF16) return fail(ctx, KVSEL_ERR_INVALID_ARG, "memory_update_batch: bad dtype");
+    if (norm_mode != 0 && norm_mode != 1) return fail(ctx, KVSEL_ERR_INVALID_ARG, "memory_update_batch: norm_mode must be 0 or 1");
+    if (L <= 0 || Hq <= 0 || D <= 0) return fail(ctx, KVSEL_ERR_SHAPE, "memory_update_batch: sizes must be positive");
+    if (D > 1024 || D % (q_dtype == KVSEL_BF16 ? 8 : 4)) return fail(ctx, KVSEL_ERR_UNSUPPORTED, "memory_update_batch: D=%d unsupported", D);
+    for (int i = 0; i < S; ++i) {
+        const kvsel_memory_session& x = sessions[i];
+        if (!x.q_rows || !x.M) return fail(ctx, KVSEL_ERR_INVALID_ARG, "memory_update_batch: session %d: null q_rows or M", i);
+        if (norm_mode == 1 && !x.A) return fail(ctx, KVSEL_ERR_INVALID_ARG, "memory_update_batch: session %d: norm_mode 1 needs A", i);
+        if (x.R <= 0) return fail(ctx, KVSEL_ERR_SHAPE, "memory_update_batch: session %d: R must be positive", i);
+        if (!(x.lambda >= 0.0f)) return fail(ctx, KVSEL_ERR_INVALID_ARG, "memory_update_batch: session %d: lambda must be >= 0", i);
+        if (!aligned16(x.q_rows) || !aligned16(x.M) || (x.A && !aligned16(x.A)))
+            return fail(ctx, KVSEL_ERR_ALIGN, "memory_update_batch: session %d: pointers must be 16-byte aligned", i);
+    }
+    if (S == 0) return KVSEL_OK;
+    void* ws = kvsel_workspace(ctx, memory_update_batch_workspace(S));
+    if (!ws) return fail(ctx, KVSEL_ERR_CUDA, "memory_update_batch: workspace allocation failed");
+    return launched(ctx, launch_memory_update_batch(q_dtype, L, Hq, D, norm_mode, sessions, S, ws, (cudaStream_t)stream),
+                    "memory_update_batch launch");
+}
+
 int kvsel_rule_scores(kvsel_ctx* ctx, const void* k_pool, int k_dtype, const int32_t* slot_map, int n_slots,
                       int L, int Hq, int Hkv, int N, int D, int64_t layer_stride, int64_t slot_stride,
                       const float* M, int pi, int q_s, int q_e, float* rule, void* stream) {
@@ -227,6 +253,67 @@ int kvsel_topk_retain(kvsel_ctx* ctx, const float* score, int N, int pi, int q_s
     if (N == 0) return KVSEL_OK;
     return launched(ctx, launch_topk(score, N, pi, q_s, q_e, (int)need, (int)nH, keep, keep_idx, (cudaStream_t)stream),
                     "topk_retain launch");
+}
+
+int kvsel_topk_retain_batch(kvsel_ctx* ctx, const kvsel_topk_session* sessions, int S, int* n_keep_host,
+                            void* stream) {
+    int rc = enter(ctx);
+    if (rc) return rc;
+    if (S < 0 || (S > 0 && !sessions)) return fail(ctx, KVSEL_ERR_INVALID_ARG, "topk_retain_batch: bad session table");
+    std::vector<int> need((size_t)S), n_cand((size_t)S);
+    for (int i = 0; i < S; ++i) {
+        const kvsel_topk_session& x = sessions[i];
+        if (!x.rule || (!x.keep && !x.keep_idx)) return fail(ctx, KVSEL_ERR_INVALID_ARG, "topk_retain_batch: session %d: null score or no output", i);
+        if (x.N < 0 || x.C < 0) return fail(ctx, KVSEL_ERR_SHAPE, "topk_retain_batch: session %d: negative N or C", i);
+        if (x.pi < 0 || x.pi > x.N || x.q_s < 0 || x.q_s > x.q_e || x.q_e > x.N)
+            return fail(ctx, KVSEL_ERR_SHAPE, "topk_retain_batch: session %d: forced ranges outside [0,N]", i);
+        const int64_t nF = forced_count(x.pi, x.q_s, x.q_e), nH = x.N - nF;
+        const int64_t cstar = x.C - nF > 0 ? x.C - nF : 0;
+        need[i] = (int)(cstar < nH ? cstar : nH);
+        n_cand[i] = (int)nH;
+        if (n_keep_host) n_keep_host[i] = (int)(nF + need[i]);
+    }
+    if (S == 0) return KVSEL_OK;
+    void* ws = kvsel_workspace(ctx, topk_batch_workspace(S));
+    if (!ws) return fail(ctx, KVSEL_ERR_CUDA, "topk_retain_batch: workspace allocation failed");
+    return launched(ctx, launch_topk_batch(sessions, need.data(), n_cand.data(), S, ws, (cudaStream_t)stream),
+                    "topk_retain_batch launch");
+}
+
+int kvsel_rule_scores_batch(kvsel_ctx* ctx, const void* k_pool, int k_dtype, int n_slots, int L, int Hq, int Hkv,
+                            int D, int64_t layer_stride, int64_t slot_stride, const kvsel_rule_session* sessions,
+                            int S, void* stream) {
+    int rc = enter(ctx);
+    if (rc) return rc;
+    if (!k_pool || (S > 0 && !sessions)) return fail(ctx, KVSEL_ERR_INVALID_ARG, "rule_scores_batch: null pointer");
+    if (S < 0 || S > 65535) return fail(ctx, KVSEL_ERR_SHAPE, "rule_scores_batch: S=%d outside [0, 65535]", S);
+    if (k_dtype != KVSEL_F32 && k_dtype != KVSEL_BF16) return fail(ctx, KVSEL_ERR_INVALID_ARG, "rule_scores_batch: bad dtype");
+    if (L <= 0 || Hq <= 0 || Hkv <= 0 || n_slots < 0) return fail(ctx, KVSEL_ERR_SHAPE, "rule_scores_batch: bad sizes");
+    if (Hq % Hkv) return fail(ctx, KVSEL_ERR_SHAPE, "rule_scores_batch: Hq=%d not a multiple of Hkv=%d", Hq, Hkv);
+    if (Hq / Hkv > 8) return fail(ctx, KVSEL_ERR_UNSUPPORTED, "rule_scores_batch: group size Hq/Hkv=%d > 8", Hq / Hkv);
+    if (!pow2_head_dim(D)) return fail(ctx, KVSEL_ERR_UNSUPPORTED, "rule_scores_batch: D=%d unsupported", D);
+    if ((int64_t)Hkv * D > 4096) return fail(ctx, KVSEL_ERR_UNSUPPORTED, "rule_scores_batch: Hkv*D > 4096");
+    if (slot_stride < (int64_t)Hkv * D || layer_stride < 0) return fail(ctx, KVSEL_ERR_SHAPE, "rule_scores_batch: slot_stride < Hkv*D");
+    if (L > 1 && layer_stride < (int64_t)n_slots * slot_stride) return fail(ctx, KVSEL_ERR_SHAPE, "rule_scores_batch: layers overlap");
+    size_t es = k_dtype == KVSEL_BF16 ? 2 : 4;
+    if (!aligned16(k_pool) || (layer_stride * es) % 16 || (slot_stride * es) % 16)
+        return fail(ctx, KVSEL_ERR_ALIGN, "rule_scores_batch: pool and strides must be 16-byte aligned");
+    for (int i = 0; i < S; ++i) {
+        const kvsel_rule_session& x = sessions[i];
+        if (x.N < 0) return fail(ctx, KVSEL_ERR_SHAPE, "rule_scores_batch: session %d: negative N", i);
+        if (x.N > 0 && (!x.M || !x.rule)) return fail(ctx, KVSEL_ERR_INVALID_ARG, "rule_scores_batch: session %d: null pointer", i);
+        if (x.pi < 0 || x.pi > x.N || x.q_s < 0 || x.q_s > x.q_e || x.q_e > x.N)
+            return fail(ctx, KVSEL_ERR_SHAPE, "rule_scores_batch: session %d: forced ranges outside [0,N]", i);
+        if (!x.slot_map && n_slots < x.N) return fail(ctx, KVSEL_ERR_SHAPE, "rule_scores_batch: session %d: identity slot map needs n_slots >= N", i);
+        if (x.N > 0 && (!aligned16(x.M) || !aligned16(x.rule)))
+            return fail(ctx, KVSEL_ERR_ALIGN, "rule_scores_batch: session %d: M and rule must be 16-byte aligned", i);
+    }
+    if (S == 0) return KVSEL_OK;
+    void* ws = kvsel_workspace(ctx, rule_scores_batch_workspace(L, Hq, sessions, S));
+    if (!ws) return fail(ctx, KVSEL_ERR_CUDA, "rule_scores_batch: workspace allocation failed");
+    return launched(ctx, launch_rule_scores_batch(ctx, k_pool, k_dtype, n_slots, L, Hq, Hkv, D, layer_stride, slot_stride,
+                                                  sessions, S, ws, (cudaStream_t)stream),
+                    "rule_scores_batch launch");
 }
 
 int kvsel_redirect_slots(kvsel_ctx* ctx, const int32_t* slot_in, const uint8_t* keep, int N, int32_t dead_slot,

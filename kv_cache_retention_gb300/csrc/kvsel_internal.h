@@ -73,9 +73,16 @@ const kvsel_ctx::RopeTab* kvsel_rope_tables(kvsel_ctx* ctx, int D, double base, 
 
 // ---- launchers (return cudaGetLastError() of their launches) ---------------
 
+size_t memory_update_batch_workspace(int S);
+cudaError_t launch_memory_update_batch(int dtype, int L, int Hq, int D, int norm_mode, const kvsel_memory_session* sess,
+                                       int S, void* ws, cudaStream_t s);
 cudaError_t launch_memory_update(const void* q, int dtype, int L, int Hq, int R, int D, float lambda,
                                  int first_turn, int norm_mode, float* M, float* A, cudaStream_t s);
 
+size_t rule_scores_batch_workspace(int L, int Hq, const kvsel_rule_session* sess, int S);
+cudaError_t launch_rule_scores_batch(kvsel_ctx* ctx, const void* k_pool, int dtype, int n_slots, int L, int Hq,
+                                     int Hkv, int D, int64_t layer_stride, int64_t slot_stride,
+                                     const kvsel_rule_session* sess, int S, void* ws, cudaStream_t s);
 cudaError_t launch_rule_scores(kvsel_ctx* ctx, const void* k_pool, int dtype, const int32_t* slot_map,
                                int n_slots, int L, int Hq, int Hkv, int N, int D, int64_t layer_stride,
                                int64_t slot_stride, const float* M, int pi, int q_s, int q_e,
@@ -83,6 +90,9 @@ cudaError_t launch_rule_scores(kvsel_ctx* ctx, const void* k_pool, int dtype, co
 size_t rule_scores_workspace(kvsel_ctx* ctx, int L, int Hq, int N);
 
 // need: how many of the non-forced positions to keep by score (0..|H|).
+size_t topk_batch_workspace(int S);
+cudaError_t launch_topk_batch(const kvsel_topk_session* sess, const int* need, const int* n_cand, int S, void* ws,
+                              cudaStream_t s);
 cudaError_t launch_topk(const float* score, int N, int pi, int q_s, int q_e, int need, int n_cand,
                         uint8_t* keep, int32_t* keep_idx, cudaStream_t s);
 

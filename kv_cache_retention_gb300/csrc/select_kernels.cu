@@ -13,6 +13,8 @@
 // Larger N: one 1024-thread block re-reading the scores for each pass.
 #include <cooperative_groups.h>
 
+#include <vector>
+
 #include "kvsel_internal.h"
 
 namespace cg = cooperative_groups;
@@ -189,9 +191,31 @@ constexpr int kCluster = 8;
 constexpr int kKeys = 16;
 constexpr int kClusterCap = kCluster * kThreads * kKeys;
 
+// One selection of a batched launch.
+struct TopkJob {
+    const float* score;
+    int N, pi, q_s, q_e, need, n_cand;
+    uint8_t* keep;
+    int32_t* keep_idx;
+};
+
+// batch: NULL, or one TopkJob per cluster (cluster c = CTAs 8c .. 8c+7 takes
+// batch[c]); the scalar arguments are then ignored.
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     topk_cluster_kernel(const float* __restrict__ score, int N, int pi, int q_s, int q_e, int need, int n_cand,
-                        uint8_t* __restrict__ keep, int32_t* __restrict__ keep_idx) {
+                        uint8_t* __restrict__ keep, int32_t* __restrict__ keep_idx, const TopkJob* __restrict__ batch) {
+    if (batch) {
+        const TopkJob& b = batch[blockIdx.x / kCluster];
+        score = b.score;
+        N = b.N;
+        pi = b.pi;
+        q_s = b.q_s;
+        q_e = b.q_e;
+        need = b.need;
+        n_cand = b.n_cand;
+        keep = b.keep;
+        keep_idx = b.keep_idx;
+    }
     __shared__ uint32_t sub[8][256];        // per-warp-group sub-histograms
     __shared__ uint32_t hist[2][256];       // this CTA's histogram, double-buffered across passes
     __shared__ uint32_t tot[256];
@@ -333,8 +357,35 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
 cudaError_t launch_topk(const float* score, int N, int pi, int q_s, int q_e, int need, int n_cand, uint8_t* keep,
                         int32_t* keep_idx, cudaStream_t s) {
     if (N <= kClusterCap)
-        topk_cluster_kernel<<<kCluster, kThreads, 0, s>>>(score, N, pi, q_s, q_e, need, n_cand, keep, keep_idx);
+        topk_cluster_kernel<<<kCluster, kThreads, 0, s>>>(score, N, pi, q_s, q_e, need, n_cand, keep, keep_idx, nullptr);
     else
         topk_kernel<<<1, kThreads, 0, s>>>(score, N, pi, q_s, q_e, need, n_cand, keep, keep_idx);
+    return cudaGetLastError();
+}
+
+size_t topk_batch_workspace(int S) { return (size_t)S * sizeof(TopkJob) + 256; }
+
+// Sessions that fit one cluster share one launch (a cluster each); larger ones take
+// the single-CTA kernel one by one.  need / n_cand per session as kvsel_topk_retain.
+cudaError_t launch_topk_batch(const kvsel_topk_session* sess, const int* need, const int* n_cand, int S, void* ws,
+                              cudaStream_t s) {
+    std::vector<TopkJob> jobs;
+    jobs.reserve((size_t)S);
+    for (int i = 0; i < S; ++i) {
+        const kvsel_topk_session& x = sess[i];
+        if (x.N == 0) continue;
+        if (x.N > kClusterCap) {
+            topk_kernel<<<1, kThreads, 0, s>>>(x.rule, x.N, x.pi, x.q_s, x.q_e, need[i], n_cand[i], x.keep, x.keep_idx);
+            continue;
+        }
+        jobs.push_back(TopkJob{x.rule, x.N, x.pi, x.q_s, x.q_e, need[i], n_cand[i], x.keep, x.keep_idx});
+    }
+    if (!jobs.empty()) {
+        TopkJob* dev = static_cast<TopkJob*>(ws);
+        cudaError_t e = cudaMemcpyAsync(dev, jobs.data(), jobs.size() * sizeof(TopkJob), cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return e;
+        topk_cluster_kernel<<<(unsigned)(kCluster * jobs.size()), kThreads, 0, s>>>(nullptr, 0, 0, 0, 0, 0, 0, nullptr,
+                                                                                   nullptr, dev);
+    }
     return cudaGetLastError();
 }
