@@ -429,6 +429,89 @@ def reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+EXTRA_CASES = ("restore_blocks", "rerope_shift", "workset_diff", "span_keep", "rule_scores_batch")
+
+
+def extra_profile_case(args):
+    """The widened rows at representative sizes, for ncu captures and per-call timing:
+    restore_blocks / rerope_shift: 2048 blocks of the 1M-workspace dims (L64 Hkv8 D128, 32-token
+    pages); workset_diff: two 2180-block working sets sharing two thirds; span_keep: N=92160 with
+    100 of 400 cursors deleted; rule_scores_batch: 36 sessions of 1024-8192 tokens at the 8B shape."""
+    import numpy as np
+    import torch
+
+    import kv_cache_retention_gb300 as kv
+
+    torch.cuda.set_device(0)
+    ctx = kv.Context(0)
+    rng = np.random.default_rng(1)
+    name = args.profile_kernel
+    L, Hkv, D, page = args.profile_layers, 8, 128, 32
+    if name in ("restore_blocks", "rerope_shift"):
+        n, P = 2048, 2180
+        k = torch.empty((L, Hkv, n * page, D), device="cuda", dtype=torch.bfloat16).normal_()
+        v = torch.empty_like(k).normal_()
+        kp = torch.zeros((L, P, page, Hkv, D), device="cuda", dtype=torch.bfloat16)
+        vp = torch.zeros_like(kp)
+        pages = torch.as_tensor(rng.permutation(P)[:n].astype(np.int32), device="cuda")
+        if name == "restore_blocks":
+            src = torch.arange(n, device="cuda", dtype=torch.int32)
+            fn = lambda: ctx.restore_blocks(k, v, src, pages, src * page, kp, vp, 1e6)  # noqa: E731
+            moved = 2 * 4 * L * Hkv * n * page * D  # K and V, read and written, 2 bytes each
+        else:
+            shifts = torch.as_tensor(rng.integers(-4096, 4096, n).astype(np.int32) * page, device="cuda")
+            fn = lambda: ctx.rerope_shift(kp, pages, shifts, 1e6)  # noqa: E731
+            moved = 2 * 2 * L * Hkv * n * page * D  # K read and written in place, 2 bytes each
+    elif name == "workset_diff":
+        prev = np.sort(rng.choice(40000, 2180, replace=False)).astype(np.int32)
+        keep = prev[rng.random(prev.size) < 0.67]
+        new = np.sort(np.concatenate([keep, rng.choice(np.setdiff1d(np.arange(40000), prev), 2180 - keep.size,
+                                                       replace=False)])).astype(np.int32)
+        ti = [torch.as_tensor(a, device="cuda") for a in (prev, rng.permutation(2180).astype(np.int32), new)]
+        fn = lambda: ctx.workset_diff(ti[0], ti[1], ti[2], 2180, page)  # noqa: E731
+        moved = 0
+    elif name == "span_keep":
+        N = 92160
+        start = torch.as_tensor(rng.integers(0, N, 400).astype(np.int32), device="cuda")
+        end = start + torch.as_tensor(rng.integers(16, 2048, 400).astype(np.int32), device="cuda")
+        dels = torch.as_tensor(rng.choice(400, 100, replace=False).astype(np.int32), device="cuda")
+        keep = torch.ones(N, dtype=torch.uint8, device="cuda")
+        fn = lambda: ctx.span_keep(start, end, dels, N, keep, keep_in=keep)  # noqa: E731
+        moved = 2 * N
+    else:
+        S, Hq = 36, 32
+        Ns = [int(x) for x in rng.integers(1024, 8193, S)]
+        n_slots = sum((x + 15) // 16 for x in Ns) * 16
+        pool = torch.empty((L, n_slots, Hkv, D), device="cuda", dtype=torch.bfloat16).normal_()
+        perm, at, smaps = rng.permutation(n_slots // 16), 0, []
+        for x in Ns:
+            m = (x + 15) // 16
+            j = np.arange(x)
+            smaps.append(torch.as_tensor((perm[at:at + m][j // 16] * 16 + j % 16).astype(np.int32), device="cuda"))
+            at += m
+        Ms = [torch.nn.functional.normalize(torch.randn((L, Hq, D), device="cuda"), dim=-1) for _ in Ns]
+        rules = [torch.empty(x, device="cuda") for x in Ns]
+        forced = [(64, x - 256, x) for x in Ns]
+        fn = lambda: ctx.rule_scores_batch(pool, Ms, L, Hq, Hkv, Ns, D, forced, rules, slot_maps=smaps,  # noqa: E731
+                                           n_slots=n_slots)
+        moved = sum(L * Hkv * (x - 320) * D * 2 for x in Ns)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record()
+    for _ in range(args.steps):
+        fn()
+    b0.record()
+    torch.cuda.synchronize()
+    ctx.check_device()
+    ms = a0.elapsed_time(b0) / args.steps
+    line = {"profile_case": name, "layers": L, "ms_per_call": ms}
+    if moved:
+        line["GBs"] = moved / (ms / 1e3) / 1e9
+    print(json.dumps(line), flush=True)
+
+
 def profile_case(args):
     """Small case for ncu captures: only `--profile-kernel` runs, on the bench's
     workloads cut to `--profile-layers` layers (inputs still larger than L2)."""
@@ -439,6 +522,9 @@ def profile_case(args):
     import kv_cache_retention_gb300 as kv
     from kv_cache_retention_gb300 import synth
 
+    if args.profile_kernel in EXTRA_CASES:
+        extra_profile_case(args)
+        return
     torch.cuda.set_device(0)
     tw = dataclasses.replace(synth.TOKEN[TOKEN_WL], L=args.profile_layers)
     bw = dataclasses.replace(synth.BLOCK[BLOCK_WL], L=args.profile_layers)

@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(256) memory_update_kernel(const T* __restrict_
     for (int k = 0; k < VEC; ++k) acc[k] = 0.f;
     if (r0 < rpi) {
         const T* base = q + (int64_t)head * R * D + (int64_t)c * VEC;
+#pragma unroll 4
         for (int r = r0; r < R; r += rpi) {
             uint4 raw = __ldg(reinterpret_cast<const uint4*>(base + (int64_t)r * D));
             if constexpr (sizeof(T) == 2) {
