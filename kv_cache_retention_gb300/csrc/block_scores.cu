@@ -251,6 +251,15 @@ __device__ __forceinline__ void row_terms(const float (&v)[32], float2 sc, float
     }
 }
 
+// Column pass: adds 2^(v*scale - lse2) of one 16-column chunk into its 8 packed column sums.
+__device__ __forceinline__ void col_terms(const float (&v)[16], float2 sc, float2 nl, float2* cs) {
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+        const float2 x = __ffma2_rn(make_float2(v[j], v[j + 1]), sc, nl);
+        cs[j / 2] = __fadd2_rn(cs[j / 2], make_float2(ex2(x.x), ex2(x.y)));
+    }
+}
+
 // Largest value of a 64-column slice, as a tree of three-input maxima.
 __device__ __forceinline__ float slice_max(const float (&v)[kSliceCols / 32][32]) {
     float m[8];
@@ -425,14 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int i = 0; i < a.n_it; ++i) {
                 const int k = acc_it % kNAcc;
-                // a timed-out wait makes this thread skip its work; the epilogue warps
-                // agree on giving up at the end of the unit
+                // After a timed-out wait a thread waits no more: its warp still runs the
+                // remaining tiles' TMEM loads (always in range, and warp-collective) and
+                // math on whatever the accumulator holds, and the epilogue warps agree on
+                // giving up at the end of the unit.  No per-tile vote or branch: in the
+                // column pass that alone cost a tenth of the tensor pipe's time.
                 if (ok) ok = wait_phase(&t.acc_full[k], (acc_it / kNAcc) & 1, abort_flag, a.err);
-                ok = __all_sync(0xffffffffu, ok);  // warp-uniform: TMEM loads are warp-collective
-                if (!ok) {
-                    ++acc_it;
-                    continue;
-                }
                 tc_fence_after();
                 const uint32_t taddr =
                     tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(k * kAccCols + slice * kSliceCols);
@@ -494,11 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             __syncwarp();
                             if (lane == 0) mbar_arrive(&t.acc_empty[k]);
                         }
-#pragma unroll
-                        for (int j = 0; j < 16; j += 2) {
-                            const float2 x = __ffma2_rn(make_float2(v[j], v[j + 1]), sc, nl);
-                            cs[c * 8 + j / 2] = __fadd2_rn(cs[c * 8 + j / 2], make_float2(ex2(x.x), ex2(x.y)));
-                        }
+                        col_terms(v, sc, nl, &cs[c * 8]);
                     }
                 }
                 ++acc_it;
