@@ -44,25 +44,36 @@
 
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kScale = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e)/sqrt(128), logits to base 2
 constexpr int kD = 128;
 constexpr int BM = 128;                         // TMEM lanes = query rows per MMA
 constexpr int kRowBytes = kD * 2;               // one bf16 row of 128 dims
-constexpr int kStageBytes = 192 * 1024;         // operand buffers of either pass
+
+constexpr int kNAcc = 2;                        // accumulator buffers
 
 // Operand tiling of a pass.  The fixed operand is loaded once per unit (kNF
 // buffers), the streamed one once per tile (a ring of kNS stages).
-//   row pass:    fixed A = 128 query rows, streamed B = 256 candidate blocks
-//   column pass: fixed B = 256 candidate blocks, streamed A = 128 query rows
+//   row pass:    fixed A = 128 query rows (one buffer), streamed B = 256
+//                candidate blocks in a ring of 3 x 64 KB: each B tile takes
+//                longer to arrive from L2 than one tile's MMAs, so a ring of 2
+//                left the tensor pipe idle
+//   column pass: fixed B = 256 candidate blocks, streamed A = 128 query rows in
+//                a ring of 4 x 32 KB
 template <int MODE>
 struct Tiling {
     static constexpr int kFRows = MODE == 0 ? 128 : 256, kSRows = MODE == 0 ? 256 : 128;
-    static constexpr int kNF = MODE == 0 ? 2 : 1, kNS = MODE == 0 ? 2 : 4;
+    static constexpr int kNF = 1, kNS = MODE == 0 ? 3 : 4;
     static constexpr int kFBytes = kFRows * kRowBytes, kSBytes = kSRows * kRowBytes;
-    static_assert(kNF * kFBytes + kNS * kSBytes == kStageBytes, "operand buffers");
+    static constexpr int kStageBytes = kNF * kFBytes + kNS * kSBytes;
+    static_assert(kStageBytes == (MODE == 0 ? 224 : 192) * 1024, "operand buffers");
+    static_assert(kNS >= kNAcc, "a stage ring at least as deep as the accumulator ring");
 };
 constexpr int kMaxStages = 4;
-constexpr int kNAcc = 2;                        // accumulator buffers
+// A tile's MMAs wait on one barrier of their operand stage, completed by the
+// stage's copies and by the epilogue's release of the accumulator they
+// overwrite (tile j's accumulator was last used by tile j - kNAcc).  That
+// needs kNS >= kNAcc, so that a release never lands on a stage barrier whose
+// previous phase is still open.
 constexpr int kAccCols = 256;                   // TMEM columns per accumulator buffer
 constexpr int kTmemCols = kNAcc * kAccCols;
 constexpr int kEpiWarps = 16;                   // 4 TMEM lane quarters x kSlices column slices
@@ -90,21 +101,24 @@ struct TcArgs {
     int c0, c1;        // candidate blocks [c0, c1)
     int Bcap;
     int n_blocks;
-    float scale;       // log2(e)/sqrt(D)
     float* lse2;       // [L*Hkv][rows_pad]; pad entries hold +inf
+    float2* part;      // row pass: [L*Hkv][rows_pad][kSlices] (ref, sum) of each column slice
     float* mass;       // [L*Hkv][n_blocks]
     unsigned* err;
 };
 
+template <int MODE>
 struct __align__(8) SmemTail {
-    float red[kSlices][BM][2];    // row pass: (ref, sum) per slice; column pass: [kSlices][4][64] column sums
-    uint64_t full_f[2], empty_f[2], full_s[kMaxStages], empty_s[kMaxStages], acc_full[kNAcc], acc_empty[kNAcc];
+    uint64_t full_f[2], empty_f[2], go[kMaxStages], empty_s[kMaxStages], acc_full[kNAcc];
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
+    float red[MODE == 1 ? kSlices * 4 * kSliceCols : 1];  // column pass: [slice][lane quarter][column] sums
 };
-static_assert(kSlices * BM * 2 == kSlices * 4 * kSliceCols, "column pass reuses the row pass merge buffer");
-constexpr size_t kSmemBytes = (size_t)kStageBytes + sizeof(SmemTail) + 1024;
+// operand buffers + barriers + room to align the buffers to 1024 bytes
+template <int MODE>
+constexpr size_t smem_bytes() { return (size_t)Tiling<MODE>::kStageBytes + sizeof(SmemTail<MODE>) + 1024; }
+static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448, "shared memory per CTA");
 
 // ---- PTX wrappers ----------------------------------------------------------
 
@@ -210,15 +224,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+// 16 TMEM lanes x 8 repetitions of 256 bits.  Thread t receives, for repetition j,
+// v[4j], v[4j+1] from lane t/4 and v[4j+2], v[4j+3] from lane t/4 + 8, both at
+// columns 8j + 2(t%4) and 8j + 2(t%4) + 1.
+__device__ __forceinline__ void tmem_ld16x256_8(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%"
+        "19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
@@ -251,12 +271,14 @@ __device__ __forceinline__ void row_terms(const float (&v)[32], float2 sc, float
     }
 }
 
-// Column pass: adds 2^(v*scale - lse2) of one 16-column chunk into its 8 packed column sums.
-__device__ __forceinline__ void col_terms(const float (&v)[16], float2 sc, float2 nl, float2* cs) {
+// Column pass: adds 2^(v*scale - lse2) of one TMEM lane of a 16x256b load
+// (e = 0: lane t/4, e = 1: lane t/4 + 8) into the thread's 8 packed column sums.
+__device__ __forceinline__ void col_terms(const float (&v)[32], int e, float2 sc, float lse, float2 (&cs)[8]) {
+    const float2 nl = make_float2(-lse, -lse);
 #pragma unroll
-    for (int j = 0; j < 16; j += 2) {
-        const float2 x = __ffma2_rn(make_float2(v[j], v[j + 1]), sc, nl);
-        cs[j / 2] = __fadd2_rn(cs[j / 2], make_float2(ex2(x.x), ex2(x.y)));
+    for (int j = 0; j < 8; ++j) {
+        const float2 x = __ffma2_rn(make_float2(v[4 * j + 2 * e], v[4 * j + 2 * e + 1]), sc, nl);
+        cs[j] = __fadd2_rn(cs[j], make_float2(ex2(x.x), ex2(x.y)));
     }
 }
 
@@ -272,13 +294,15 @@ __device__ __forceinline__ float slice_max(const float (&v)[kSliceCols / 32][32]
     return max3(max3(m[0], m[1], m[2]), max3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
 }
 
-// Column sums of a warp: on entry lane l holds f[c] = its row's value for column
-// c (0..63); on exit f[0], f[1] hold the sums over the warp's 32 rows of columns
-// 2l and 2l+1.  Five butterfly levels; at each the lane keeps the half of its
-// columns selected by one lane bit and sends the other half to its partner.
-__device__ __forceinline__ void column_reduce(float (&f)[64], int lane) {
+// Column sums of a warp after the column pass: on entry lane t holds, for
+// j = 0..7, the sums of columns 8j + 2(t%4) and 8j + 2(t%4) + 1 over its rows;
+// the eight lanes with the same t%4 hold the same columns.  Three butterfly
+// levels over lane bits 4, 3, 2, each keeping half of the values and sending
+// the other half to the partner; on exit f[0], f[1] hold the sums over the
+// warp's 32 rows of columns 2t and 2t + 1.
+__device__ __forceinline__ void column_reduce(float (&f)[16], int lane) {
 #pragma unroll
-    for (int s = 16, n = 32; s >= 1; s >>= 1, n >>= 1) {
+    for (int s = 16, n = 8; s >= 4; s >>= 1, n >>= 1) {
         const bool up = (lane & s) != 0;
 #pragma unroll
         for (int i = 0; i < n; ++i) {
@@ -302,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* sF = smem;                                   // [kNF][kFBytes]
     uint8_t* sS = smem + T::kNF * T::kFBytes;             // [kNS][kSBytes]
-    SmemTail& t = *reinterpret_cast<SmemTail*>(smem + kStageBytes);
+    SmemTail<MODE>& t = *reinterpret_cast<SmemTail<MODE>*>(smem + T::kStageBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int* abort_flag = &t.abort_flag;
 
@@ -312,13 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&t.empty_f[i], 1);
         }
         for (int i = 0; i < T::kNS; ++i) {
-            mbar_init(&t.full_s[i], 1);
+            mbar_init(&t.go[i], 1 + kEpiWarps);  // the stage's copies + the accumulator's release
             mbar_init(&t.empty_s[i], 1);
         }
-        for (int i = 0; i < kNAcc; ++i) {
-            mbar_init(&t.acc_full[i], 1);
-            mbar_init(&t.acc_empty[i], kEpiWarps);  // one arrival per epilogue warp
-        }
+        for (int i = 0; i < kNAcc; ++i) mbar_init(&t.acc_full[i], 1);
         mbar_init(&t.mma_done, 1);
         t.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -354,15 +375,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int st = s_it % T::kNS;
                     const int ys = MODE == 0 ? lg * a.Bcap + a.c0 + i * T::kSRows : lg * a.rows_g + i * T::kSRows;
                     if (!(ok = wait_phase(&t.empty_s[st], ((s_it / T::kNS) & 1) ^ 1, abort_flag, a.err))) break;
-                    mbar_expect_tx(&t.full_s[st], T::kSBytes);
-                    tma_load_2d(&mapS, &t.full_s[st], sS + st * T::kSBytes, 0, ys);
-                    tma_load_2d(&mapS, &t.full_s[st], sS + st * T::kSBytes + T::kSBytes / 2, 64, ys);
+                    mbar_expect_tx(&t.go[st], T::kSBytes);
+                    tma_load_2d(&mapS, &t.go[st], sS + st * T::kSBytes, 0, ys);
+                    tma_load_2d(&mapS, &t.go[st], sS + st * T::kSBytes + T::kSBytes / 2, 64, ys);
                     ++s_it;
                 }
             }
             // drain: wait until every copy this thread started has landed
             for (uint32_t i = (s_it > (uint32_t)T::kNS ? s_it - T::kNS : 0); i < s_it; ++i)
-                drain_phase(&t.full_s[i % T::kNS], (i / T::kNS) & 1);
+                drain_phase(&t.go[i % T::kNS], (i / T::kNS) & 1);
             for (uint32_t i = (f_it > (uint32_t)T::kNF ? f_it - T::kNF : 0); i < f_it; ++i)
                 drain_phase(&t.full_f[i % T::kNF], (i / T::kNF) & 1);
         }
@@ -379,8 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < a.n_it; ++i) {
                     const int st = s_it % T::kNS;
                     const int k = acc_it % kNAcc;
-                    if (!(ok = wait_phase(&t.full_s[st], (s_it / T::kNS) & 1, abort_flag, a.err))) break;
-                    if (!(ok = wait_phase(&t.acc_empty[k], ((acc_it / kNAcc) & 1) ^ 1, abort_flag, a.err))) break;
+                    // one wait per tile: the stage's operand has landed and the epilogue has
+                    // read the accumulator this tile overwrites
+                    if (!(ok = wait_phase(&t.go[st], (s_it / T::kNS) & 1, abort_flag, a.err))) break;
                     tc_fence_after();
                     const uint32_t s_base = saddr(sS + st * T::kSBytes);
                     // A = the 128-row operand, B = the 256-row one
@@ -412,7 +434,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int slice = ew >> 2;               // column slice
         const int r_local = q * 32 + lane;       // TMEM lane = query row of the tile
         const int etid = ew * 32 + lane;
-        const float2 sc = make_float2(a.scale, a.scale);
+        const float2 sc = make_float2(kScale, kScale);
+        // the first kNAcc tiles find their accumulators free
+        if (lane == 0)
+            for (int j = 0; j < kNAcc; ++j) mbar_arrive(&t.go[j % T::kNS]);
         uint32_t acc_it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
@@ -424,13 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             make_float2(0.f, 0.f)};
             // column pass: this lane's row's share of each of its slice's 64 columns,
             // and lse2 of its row in the next two tiles (loaded ahead)
-            float2 cs[kSliceCols / 2];
-            float lse_n0 = INFINITY, lse_n1 = INFINITY;
+            float2 cs[8];
+            float lse_n = INFINITY;
             if (MODE == 1) {
 #pragma unroll
-                for (int j = 0; j < kSliceCols / 2; ++j) cs[j] = make_float2(0.f, 0.f);
-                if (r_local < a.rows_pad) lse_n0 = __ldg(lse_lg + r_local);
-                if (BM + r_local < a.rows_pad && a.n_it > 1) lse_n1 = __ldg(lse_lg + BM + r_local);
+                for (int j = 0; j < 8; ++j) cs[j] = make_float2(0.f, 0.f);
+                if (r_local < a.rows_pad) lse_n = __ldg(lse_lg + r_local);
             }
             for (int i = 0; i < a.n_it; ++i) {
                 const int k = acc_it % kNAcc;
@@ -450,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_wait();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&t.acc_empty[k]);  // this warp's part of the accumulator is read
+                    if (lane == 0) mbar_arrive(&t.go[(acc_it + kNAcc) % T::kNS]);  // accumulator k is read
                     // columns past the candidate range (last tile only) are masked
                     const int nvalid = a.c1 - (a.c0 + i * kAccCols + slice * kSliceCols);
                     if (nvalid < kSliceCols) {
@@ -460,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int j = 0; j < 32; ++j)
                                 if (c * 32 + j >= nvalid) v[c][j] = -INFINITY;
                     }
-                    if (ref == -INFINITY) ref = slice_max(v) * a.scale;  // first tile with a finite logit
+                    if (ref == -INFINITY) ref = slice_max(v) * kScale;  // first tile with a finite logit
                     if (ref != -INFINITY) {
                         float2 t2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                         make_float2(0.f, 0.f)};
@@ -470,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!(fmaxf(big, fmaxf(t2[3].x, t2[3].y)) <= 0x1p64f)) {
                             // a logit far above the reference: move it to this tile's
                             // maximum, rescale the sum and take the tile again
-                            const float r_new = fmaxf(ref, slice_max(v) * a.scale);
+                            const float r_new = fmaxf(ref, slice_max(v) * kScale);
                             const float f = ex2(ref - r_new);
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
@@ -486,59 +510,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 } else {
                     // column pass: rows past rows_pad read +inf and add nothing
-                    const float lse = lse_n0;
-                    lse_n0 = lse_n1;
-                    const int r2 = (i + 2) * BM + r_local;
-                    lse_n1 = (i + 2 < a.n_it && r2 < a.rows_pad) ? __ldg(lse_lg + r2) : INFINITY;
-                    const float2 nl = make_float2(-lse, -lse);
-#pragma unroll
-                    for (int c = 0; c < kSliceCols / 16; ++c) {
-                        float v[16];
-                        tmem_ld16(taddr + 16 * c, v);
-                        tmem_ld_wait();
-                        if (c == kSliceCols / 16 - 1) {
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&t.acc_empty[k]);
-                        }
-                        col_terms(v, sc, nl, &cs[c * 8]);
-                    }
+                    const float lse = lse_n;
+                    const int r1 = (i + 1) * BM + r_local;
+                    lse_n = (i + 1 < a.n_it && r1 < a.rows_pad) ? __ldg(lse_lg + r1) : INFINITY;
+                    // the warp's 32 lanes in two halves of 16; each thread gets 4 rows x 16
+                    // columns, so the whole slice is read before the accumulator is released
+                    float v0[32], v1[32];
+                    tmem_ld16x256_8(taddr, v0);
+                    tmem_ld16x256_8(taddr + (16u << 16), v1);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&t.go[(acc_it + kNAcc) % T::kNS]);
+                    // lse2 of the thread's rows, from the lanes that loaded them
+                    const int rl = lane >> 2;
+                    col_terms(v0, 0, sc, __shfl_sync(0xffffffffu, lse, rl), cs);
+                    col_terms(v0, 1, sc, __shfl_sync(0xffffffffu, lse, rl + 8), cs);
+                    col_terms(v1, 0, sc, __shfl_sync(0xffffffffu, lse, rl + 16), cs);
+                    col_terms(v1, 1, sc, __shfl_sync(0xffffffffu, lse, rl + 24), cs);
                 }
                 ++acc_it;
             }
             if (!(ok = epi_bar_and(ok))) break;
             if (MODE == 0) {
-                // merge the column slices of each row, in slice order
+                // this slice's (reference, sum) of the row; bs_lse_merge combines the slices
                 const float s_part =
                     (s2[0].x + s2[0].y) + (s2[1].x + s2[1].y) + (s2[2].x + s2[2].y) + (s2[3].x + s2[3].y);
-                t.red[slice][r_local][0] = ref;
-                t.red[slice][r_local][1] = s_part;
-                epi_bar();
-                if (slice == 0) {
-                    const int row = o * BM + r_local;
-                    if (row >= a.rows_g && row < a.rows_pad) a.lse2[(int64_t)lg * a.rows_pad + row] = INFINITY;
-                    if (row < a.rows_g) {
-                        float m = -INFINITY;
-#pragma unroll
-                        for (int j = 0; j < kSlices; ++j) m = fmaxf(m, t.red[j][r_local][0]);
-                        float sum = 0.f;
-                        if (m != -INFINITY) {
-#pragma unroll
-                            for (int j = 0; j < kSlices; ++j) sum += t.red[j][r_local][1] * ex2(t.red[j][r_local][0] - m);
-                        }
-                        a.lse2[(int64_t)lg * a.rows_pad + row] = sum > 0.f ? m + __log2f(sum) : -INFINITY;
-                    }
-                }
+                const int row = o * BM + r_local;
+                if (row < a.rows_g) a.part[((int64_t)lg * a.rows_pad + row) * kSlices + slice] = make_float2(ref, s_part);
             } else {
                 // sum each column over the warp's rows, then over the four lane quarters
-                float f[kSliceCols];
+                float f[16];
 #pragma unroll
-                for (int j = 0; j < kSliceCols / 2; ++j) {
+                for (int j = 0; j < 8; ++j) {
                     f[2 * j] = cs[j].x;
                     f[2 * j + 1] = cs[j].y;
                 }
                 column_reduce(f, lane);
-                float* red = &t.red[0][0][0];  // [kSlices][4][kSliceCols]
+                float* red = t.red;  // [kSlices][4][kSliceCols]
                 red[(slice * 4 + q) * kSliceCols + 2 * lane] = f[0];
                 red[(slice * 4 + q) * kSliceCols + 2 * lane + 1] = f[1];
                 epi_bar();
@@ -562,6 +571,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
                      : "memory");
     }
+}
+
+// lse2 of each query row from the row pass's per-slice (reference, sum)
+// pairs, merged in slice order; rows past rows_g get +inf (they add nothing
+// in the column pass).
+__global__ void bs_lse_merge(const float2* __restrict__ part, float* lse2, int LH, int rows_g, int rows_pad) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)LH * rows_pad) return;
+    const int row = (int)(i % rows_pad);
+    if (row >= rows_g) {
+        lse2[i] = INFINITY;
+        return;
+    }
+    float2 p[kSlices];
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kSlices; ++j) {
+        p[j] = part[i * kSlices + j];
+        m = fmaxf(m, p[j].x);
+    }
+    float sum = 0.f;
+    if (m != -INFINITY) {
+#pragma unroll
+        for (int j = 0; j < kSlices; ++j) sum += p[j].y * ex2(p[j].x - m);
+    }
+    lse2[i] = sum > 0.f ? m + __log2f(sum) : -INFINITY;
 }
 
 // R[b] = sum_lg mass[lg][b] / (L*Hq) on C; zero outside C (also in mass).
@@ -611,7 +646,8 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_ro
 
 size_t block_scores_workspace(int L, int Hq, int Hkv, int M, int n_blocks) {
     const size_t rows_pad = (((size_t)(Hq / Hkv) * M + 3) & ~(size_t)3);
-    return align256((size_t)L * Hkv * rows_pad * sizeof(float)) + align256((size_t)L * Hkv * n_blocks * sizeof(float));
+    return align256((size_t)L * Hkv * rows_pad * sizeof(float)) + align256((size_t)L * Hkv * n_blocks * sizeof(float)) +
+           align256((size_t)L * Hkv * rows_pad * kSlices * sizeof(float2));
 }
 
 cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index, int L, int Hq, int Hkv, int M, int D,
@@ -628,16 +664,20 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
     float* lse2 = reinterpret_cast<float*>(w);
     const int rows_pad = (rows_g + 3) & ~3;
     w += align256((size_t)LH * rows_pad * sizeof(float));
-    float* mass = R_partial ? R_partial : reinterpret_cast<float*>(w);
+    float* mass_ws = reinterpret_cast<float*>(w);
+    float* mass = R_partial ? R_partial : mass_ws;
+    w += align256((size_t)LH * n_blocks * sizeof(float));
+    float2* part = reinterpret_cast<float2*>(w);
 
     if (ncand > 0) {
         CUtensorMap q128, i256;
         const uint64_t q_rows = (uint64_t)L * Hq * M, i_rows = (uint64_t)LH * Bcap;
         if (!make_map(&q128, q, q_rows, BM) || !make_map(&i256, index, i_rows, kAccCols)) return cudaErrorInvalidValue;
         cudaError_t e = cudaFuncSetAttribute(block_scores_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
+                                             (int)smem_bytes<0>());
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(block_scores_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+            e = cudaFuncSetAttribute(block_scores_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem_bytes<1>());
         if (e != cudaSuccess) return e;
         TcArgs a;
         a.rows_g = rows_g;
@@ -646,8 +686,8 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
         a.c1 = c1;
         a.Bcap = Bcap;
         a.n_blocks = n_blocks;
-        a.scale = kLog2e / sqrtf((float)kD);
         a.lse2 = lse2;
+        a.part = part;
         a.mass = mass;
         a.err = ctx->dev_err;
         // row pass: a unit per 128 query rows, the candidate blocks streamed 256 at a time
@@ -655,13 +695,15 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
         a.n_units = LH * a.units_per_lg;
         a.n_it = (ncand + kAccCols - 1) / kAccCols;
         int grid = a.n_units < ctx->num_sms ? a.n_units : ctx->num_sms;
-        block_scores_tc<0><<<grid, kThreads, kSmemBytes, s>>>(q128, i256, a);
+        block_scores_tc<0><<<grid, kThreads, smem_bytes<0>(), s>>>(q128, i256, a);
+        const int64_t n_rows = (int64_t)LH * rows_pad;
+        bs_lse_merge<<<(unsigned)((n_rows + 255) / 256), 256, 0, s>>>(part, lse2, LH, rows_g, rows_pad);
         // column pass: a unit per 256 candidate blocks, the query rows streamed 128 at a time
         a.units_per_lg = (ncand + kAccCols - 1) / kAccCols;
         a.n_units = LH * a.units_per_lg;
         a.n_it = (rows_g + BM - 1) / BM;
         grid = a.n_units < ctx->num_sms ? a.n_units : ctx->num_sms;
-        block_scores_tc<1><<<grid, kThreads, kSmemBytes, s>>>(i256, q128, a);
+        block_scores_tc<1><<<grid, kThreads, smem_bytes<1>(), s>>>(i256, q128, a);
     }
     bs_finalize<<<(n_blocks + 255) / 256, 256, 0, s>>>(mass, mass, R, LH, n_blocks, c0, c1,
                                                        1.0f / ((float)L * (float)Hq));
