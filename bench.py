@@ -153,7 +153,7 @@ def setup_session(kv, synth, ctx, tw, bw, torch):
 
 # kernel launches per C-ABI call (counted from the launchers in csrc/)
 LAUNCHES = {"memory_update": 1, "rule_scores": 3, "topk_retain": 1, "redirect_slots": 1, "meank_build": 1,
-            "block_scores": 3, "select_blocks": 1, "rerope_scatter": 1}
+            "block_scores": 4, "select_blocks": 1, "rerope_scatter": 1}
 
 
 def run_step(ctx, s, ev=None):
@@ -343,9 +343,9 @@ def ours(args, rank, world, local_rank):
 # DRAM bytes (read + write) per call from an ncu capture of the current kernel code, scaled to the
 # bench workload; an entry is removed whenever its kernel changes.  Source: profiles/*.md.
 PROFILED_TRAFFIC = {
-    # block_scores_tc, 4-layer capture of both passes (357.2 + 361.5 MB), x16 for 64 layers;
-    # profiles/block_scores_tc_ws1m_L4.md
-    "block_scores": 16 * (357.154816 + 361.484032) * 1e6,
+    # block_scores_tc, 4-layer capture of both passes (row 352.5 + 11.7 MB, column 353.8 + 6.5 MB),
+    # x16 for 64 layers; profiles/block_scores_tc_ws1m_L4.md
+    "block_scores": 16 * (352.475904 + 11.735552 + 353.757952 + 6.514944) * 1e6,
 }
 
 

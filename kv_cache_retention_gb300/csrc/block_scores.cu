@@ -53,19 +53,18 @@ constexpr int kNAcc = 2;                        // accumulator buffers
 
 // Operand tiling of a pass.  The fixed operand is loaded once per unit (kNF
 // buffers), the streamed one once per tile (a ring of kNS stages).
-//   row pass:    fixed A = 128 query rows (one buffer), streamed B = 256
-//                candidate blocks in a ring of 3 x 64 KB: each B tile takes
-//                longer to arrive from L2 than one tile's MMAs, so a ring of 2
-//                left the tensor pipe idle
+//   row pass:    fixed A = 128 query rows (two buffers, so that the next unit's
+//                rows load during this one), streamed B = 256 candidate blocks
+//                in a ring of 2 x 64 KB
 //   column pass: fixed B = 256 candidate blocks, streamed A = 128 query rows in
 //                a ring of 4 x 32 KB
 template <int MODE>
 struct Tiling {
     static constexpr int kFRows = MODE == 0 ? 128 : 256, kSRows = MODE == 0 ? 256 : 128;
-    static constexpr int kNF = 1, kNS = MODE == 0 ? 3 : 4;
+    static constexpr int kNF = MODE == 0 ? 2 : 1, kNS = MODE == 0 ? 2 : 4;
     static constexpr int kFBytes = kFRows * kRowBytes, kSBytes = kSRows * kRowBytes;
     static constexpr int kStageBytes = kNF * kFBytes + kNS * kSBytes;
-    static_assert(kStageBytes == (MODE == 0 ? 224 : 192) * 1024, "operand buffers");
+    static_assert(kStageBytes == 192 * 1024, "operand buffers");
     static_assert(kNS >= kNAcc, "a stage ring at least as deep as the accumulator ring");
 };
 constexpr int kMaxStages = 4;
