@@ -78,6 +78,14 @@ def _load():
             lib.orc_rerope_shift.argtypes = [P, I, P, P, I, I, I, I, I, D, I]
             lib.orc_span_keep.argtypes = [P, P, I, P, I, P, I, P]
             lib.orc_span_keep.restype = I
+            lib.orc_e4m3_decode.argtypes = [ctypes.c_uint]
+            lib.orc_e4m3_decode.restype = D
+            lib.orc_e4m3_encode.argtypes = [D]
+            lib.orc_e4m3_encode.restype = ctypes.c_uint
+            lib.orc_fp8_row_exp.argtypes = [P, I]
+            lib.orc_fp8_row_exp.restype = I
+            lib.orc_index_to_fp8.argtypes = [P, I64, I, P, P]
+            lib.orc_index_from_fp8.argtypes = [P, P, I64, I, P]
             _lib = lib
     return _lib
 
@@ -340,3 +348,43 @@ def span_keep(span_start, span_end, del_ids, N, keep_in=None):
     out = np.zeros(max(N, 1), np.uint8)
     bad = lib.orc_span_keep(_ptr(ss), _ptr(se), ss.size, _ptr(di), di.size, _ptr(ki), int(N), _ptr(out))
     return out[:N].copy(), int(bad)
+
+
+def e4m3_decode(code: int) -> float:
+    """Value of one E4M3 code (OCP 8-bit float: bias 7, 3 mantissa bits, max 448)."""
+    return float(_load().orc_e4m3_decode(int(code) & 0xFF))
+
+
+def e4m3_encode(y: float) -> int:
+    """Nearest E4M3 code to y (|y| <= 448), ties to the even code; the sign of zero is kept."""
+    return int(_load().orc_e4m3_encode(float(y)))
+
+
+def fp8_row_exp(x) -> int:
+    """Scale exponent of an index row: the smallest e >= -100 with max|x| <= 448 * 2^e."""
+    v = _c(x, np.float64)
+    return int(_load().orc_fp8_row_exp(_ptr(v), v.size))
+
+
+def index_to_fp8(index_bits):
+    """Mean-K index rows [..., D] (bf16 bits) -> (E4M3 codes uint8 [..., D], scale exponents int8 [...]).
+    Each row is stored as its codes and 2^e: value = code * 2^e."""
+    b = _c(index_bits, np.uint16)
+    D = b.shape[-1]
+    rows = b.size // D
+    codes = np.empty(b.shape, dtype=np.uint8)
+    exps = np.empty(b.shape[:-1], dtype=np.int8)
+    _load().orc_index_to_fp8(_ptr(b), rows, D, _ptr(codes), _ptr(exps))
+    return codes, exps
+
+
+def index_from_fp8(codes, exps):
+    """E4M3 codes [..., D] and scale exponents [...] -> bf16 bits [..., D] (every value is exact in bf16)."""
+    c = _c(codes, np.uint8)
+    e = _c(exps, np.int8)
+    D = c.shape[-1]
+    rows = c.size // D
+    assert e.size == rows
+    out = np.empty(c.shape, dtype=np.uint16)
+    _load().orc_index_from_fp8(_ptr(c), _ptr(e), rows, D, _ptr(out))
+    return out

@@ -601,3 +601,78 @@ int orc_span_keep(const int32_t* span_start, const int32_t* span_end, int n_curs
     }
     return bad;
 }
+
+/* ------------------------------------------------------------------------ */
+/* FP8 storage of the Mean-K index                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * KVMEM page, section "design and trade-offs" (the per-block index and its
+ * size: 9.5 GiB of index for a 10M-token workspace) and the server
+ * experiments, which keep the KV cache in FP8.  Reading: an index row (one
+ * Mean-K vector of D values for one (layer, kv head, block)) is stored as D
+ * E4M3 codes and one power-of-two scale 2^e, the value being code * 2^e.
+ *
+ * E4M3, the OCP 8-bit floating-point format: a sign bit, 4 exponent bits with
+ * bias 7 and 3 mantissa bits.  Exponent field 0 holds the subnormals m * 2^-9;
+ * fields 1..15 hold (1 + m/8) * 2^(E-7), except E = 15, m = 7, which is NaN.
+ * There is no infinity; the largest finite value is 1.75 * 2^8 = 448.
+ */
+double orc_e4m3_decode(unsigned code) {
+    const unsigned E = (code >> 3) & 15u, m = code & 7u;
+    if (E == 15u && m == 7u) return NAN;
+    const double mag = E == 0 ? ldexp((double)m, -9) : ldexp((double)(8u + m), (int)E - 10);
+    return (code & 0x80u) ? -mag : mag;
+}
+
+/* Nearest E4M3 value to y, ties to the even code (an even last mantissa bit);
+ * |y| must not exceed 448.  The sign is kept, also for results of zero. */
+unsigned orc_e4m3_encode(double y) {
+    const unsigned sign = signbit(y) ? 0x80u : 0u;
+    const double a = fabs(y);
+    unsigned code;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal spacing 2^-9; k = 8 is the smallest normal, code 0x08 */
+        code = (unsigned)nearbyint(a / ldexp(1.0, -9));
+    } else {
+        int ex;
+        frexp(a, &ex); /* a = f * 2^ex, f in [0.5, 1): 2^(ex-1) <= a < 2^ex */
+        int E = ex - 1;
+        unsigned k = (unsigned)nearbyint(a / ldexp(1.0, E - 3)); /* 8 .. 16 */
+        if (k == 16u) {
+            k = 8u;
+            ++E;
+        }
+        code = ((unsigned)(E + 7) << 3) | (k - 8u);
+    }
+    return sign | code;
+}
+
+/* Scale exponent of a row: the smallest e >= -100 with max|x| <= 448 * 2^e
+ * (an all-zero row gets -100).  448 = 0.875 * 2^9. */
+int orc_fp8_row_exp(const double* x, int D) {
+    double mx = 0.0;
+    for (int i = 0; i < D; ++i) mx = fmax(mx, fabs(x[i]));
+    if (mx == 0.0) return -100;
+    int ex;
+    const double f = frexp(mx, &ex);
+    const int e = f <= 0.875 ? ex - 9 : ex - 8;
+    return e < -100 ? -100 : e;
+}
+
+void orc_index_to_fp8(const uint16_t* idx, int64_t rows, int D, uint8_t* codes, int8_t* exps) {
+    double* x = (double*)malloc(sizeof(double) * (size_t)D);
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int i = 0; i < D; ++i) x[i] = orc_bf16_bits_to_double(idx[r * D + i]);
+        const int e = orc_fp8_row_exp(x, D);
+        exps[r] = (int8_t)e;
+        for (int i = 0; i < D; ++i) codes[r * D + i] = (uint8_t)orc_e4m3_encode(ldexp(x[i], -e));
+    }
+    free(x);
+}
+
+void orc_index_from_fp8(const uint8_t* codes, const int8_t* exps, int64_t rows, int D, uint16_t* idx) {
+    for (int64_t r = 0; r < rows; ++r)
+        for (int i = 0; i < D; ++i)
+            idx[r * D + i] = orc_double_to_bf16(ldexp(orc_e4m3_decode(codes[r * D + i]), exps[r]));
+}
