@@ -429,14 +429,16 @@ def reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-EXTRA_CASES = ("restore_blocks", "rerope_shift", "workset_diff", "span_keep", "rule_scores_batch")
+EXTRA_CASES = ("restore_blocks", "rerope_shift", "workset_diff", "span_keep", "rule_scores_batch", "index_to_fp8",
+               "index_from_fp8")
 
 
 def extra_profile_case(args):
     """The widened rows at representative sizes, for ncu captures and per-call timing:
     restore_blocks / rerope_shift: 2048 blocks of the 1M-workspace dims (L64 Hkv8 D128, 32-token
     pages); workset_diff: two 2180-block working sets sharing two thirds; span_keep: N=92160 with
-    100 of 400 cursors deleted; rule_scores_batch: 36 sessions of 1024-8192 tokens at the 8B shape."""
+    100 of 400 cursors deleted; rule_scores_batch: 36 sessions of 1024-8192 tokens at the 8B shape;
+    index_to_fp8 / index_from_fp8: the 1M-workspace index (32768 blocks, Hkv8 D128) per layer."""
     import numpy as np
     import torch
 
@@ -470,6 +472,18 @@ def extra_profile_case(args):
         ti = [torch.as_tensor(a, device="cuda") for a in (prev, rng.permutation(2180).astype(np.int32), new)]
         fn = lambda: ctx.workset_diff(ti[0], ti[1], ti[2], 2180, page)  # noqa: E731
         moved = 0
+    elif name in ("index_to_fp8", "index_from_fp8"):
+        nb = 32768
+        ix = torch.empty((L, Hkv, nb, D), device="cuda", dtype=torch.bfloat16).normal_()
+        codes = torch.empty(ix.shape, dtype=torch.uint8, device="cuda")
+        exps = torch.empty(ix.shape[:-1], dtype=torch.int8, device="cuda")
+        out = torch.empty_like(ix)
+        ctx.index_to_fp8(ix, codes, exps)
+        if name == "index_to_fp8":
+            fn = lambda: ctx.index_to_fp8(ix, codes, exps)  # noqa: E731
+        else:
+            fn = lambda: ctx.index_from_fp8(codes, exps, out)  # noqa: E731
+        moved = L * Hkv * nb * (3 * D + 1)
     elif name == "span_keep":
         N = 92160
         start = torch.as_tensor(rng.integers(0, N, 400).astype(np.int32), device="cuda")
@@ -770,6 +784,69 @@ def block_sweep(args):
         torch.cuda.empty_cache()
 
 
+def fp8_index(args):
+    """FP8 (E4M3) index storage at the 1M-token workspace (L64 Hq40 Hkv8 D128, 32768 blocks of 32, 2048
+    queries): the Mean-K index stored as codes + a scale exponent per row, expanded to bf16 before R_b.
+    Reports index bytes, the quantise and expand calls' times (CUDA events, mean over --steps) with their
+    HBM fraction, and how the FP8 index changes the selected working set (overlap of the top-k blocks)."""
+    import torch
+
+    import kv_cache_retention_gb300 as kv
+    from kv_cache_retention_gb300 import synth
+
+    torch.cuda.set_device(0)
+    ctx = kv.Context(0)
+    peaks = _peaks()
+    bw = synth.BLOCK[BLOCK_WL]
+    b = synth.block_inputs(bw, "cuda", with_staging=False)
+    index = b["index"]
+    ctx.meank_build(b["raw"], bw.block, index, first_block=bw.first_new_block)  # the new blocks' Mean-K rows
+    rows = bw.L * bw.Hkv * index.shape[2]
+    D = bw.D
+    codes = torch.empty(index.shape, dtype=torch.uint8, device="cuda")
+    exps = torch.empty(index.shape[:-1], dtype=torch.int8, device="cuda")
+    back = torch.empty_like(index)
+    calls = [("index_to_fp8", lambda: ctx.index_to_fp8(index, codes, exps)),
+             ("index_from_fp8", lambda: ctx.index_from_fp8(codes, exps, back))]
+    for _ in range(args.warmup):
+        for _, fn in calls:
+            fn()
+    torch.cuda.synchronize()
+    ev = {}
+    for _ in range(args.steps):
+        for name, fn in calls:
+            a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record()
+            fn()
+            b0.record()
+            ev.setdefault(name, []).append((a0, b0))
+    torch.cuda.synchronize()
+    ctx.check_device()
+    ms = {k: sum(x.elapsed_time(y) for x, y in v) / len(v) for k, v in ev.items()}
+    moved = rows * (2 * D + D + 1)  # bf16 row read + codes and exponent written (or the reverse)
+    out = {"workload": f"1M workspace index [L{bw.L} Hkv{bw.Hkv} {index.shape[2]} blocks D{D}]",
+           "index_bf16_MB": rows * 2 * D / 1e6, "index_fp8_MB": rows * (D + 1) / 1e6}
+    for k, v in ms.items():
+        gbs = moved / (v / 1e3) / 1e9
+        out[k] = {"ms": v, "GB_s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": moved}
+    # the working set selected from the FP8 index against the one from the bf16 index
+    R16, R8 = torch.empty(bw.n_blocks, device="cuda"), torch.empty(bw.n_blocks, device="cuda")
+    ids16 = torch.empty(bw.n_sel, device="cuda", dtype=torch.int32)
+    ids8 = torch.empty(bw.n_sel, device="cuda", dtype=torch.int32)
+    ctx.block_scores(b["q"], index, bw.n_blocks, bw.n_sink, bw.n_recent, R16)
+    ctx.block_scores(b["q"], back, bw.n_blocks, bw.n_sink, bw.n_recent, R8)
+    ctx.select_blocks(R16, bw.n_sink, bw.n_recent, bw.k, ids16)
+    ctx.select_blocks(R8, bw.n_sink, bw.n_recent, bw.k, ids8)
+    torch.cuda.synchronize()
+    ctx.check_device()
+    C = slice(bw.n_sink, bw.n_blocks - bw.n_recent)
+    same = len(set(ids16.cpu().tolist()) & set(ids8.cpu().tolist()))
+    out["R_b_max_rel_change"] = float(((R8[C] - R16[C]).abs() / R16[C]).max())
+    out["working_set_overlap"] = same / bw.n_sel
+    out["data"] = "synthetic: the bench's 1M-workspace index (drawn old blocks + Mean-K of the new raw K)"
+    print(json.dumps(out), flush=True)
+
+
 def batch_sessions(args):
     """A serving batch of 36 sessions (8B shape: L36 Hq32 Hkv8 D128, bf16 K in one shared pool of 16-slot
     pages, N drawn from 1024-8192 per session, 64 query rows per turn, C = N/4): the IntentKV step
@@ -876,9 +953,13 @@ def main():
     ap.add_argument("--restore-pipeline", action="store_true", help="throughput of the staged host -> device restore")
     ap.add_argument("--block-sweep", action="store_true", help="Mean-K block size sweep (16 / 32 / 64 tokens)")
     ap.add_argument("--batch-sessions", action="store_true", help="36-session batched IntentKV step vs one by one")
+    ap.add_argument("--fp8-index", action="store_true", help="FP8 (E4M3) index storage: quantise / expand cost, R_b change")
     args = ap.parse_args()
     if args.batch_sessions:
         batch_sessions(args)
+        return
+    if args.fp8_index:
+        fp8_index(args)
         return
     if args.block_sweep:
         block_sweep(args)

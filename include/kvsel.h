@@ -324,6 +324,24 @@ int kvsel_span_keep(kvsel_ctx* ctx, const int32_t* span_start, const int32_t* sp
                     void* stream);
 
 /*
+ * FP8 storage of a Mean-K index (KVMEM page, section "design and trade-offs":
+ * one Mean-K vector per block, layer and kv head, 9.5 GiB of index for a
+ * 10M-token workspace; its server runs keep the KV cache in FP8).  A row of D
+ * values (one (layer, kv head, block)) is stored as D E4M3 codes (OCP 8-bit
+ * float: 4 exponent bits with bias 7, 3 mantissa bits, largest value 448) and
+ * one scale exponent e, the smallest integer >= -100 with max|x| <= 448 * 2^e;
+ * a stored value is code * 2^e.  Codes round to nearest, ties to the even
+ * code.  Every stored value is exact in bf16, so kvsel_index_from_fp8's rows
+ * feed kvsel_block_scores directly.  Half the index bytes, plus one byte a row.
+ *   index  bf16 [rows][D] (16-byte aligned); codes u8 [rows][D] (4-byte
+ *   aligned); exps i8 [rows].  D in {64, 128, 256}.  Inputs must be finite.
+ */
+int kvsel_index_to_fp8(kvsel_ctx* ctx, const void* index, int64_t rows, int D, uint8_t* codes, int8_t* exps,
+                       void* stream);
+int kvsel_index_from_fp8(kvsel_ctx* ctx, const uint8_t* codes, const int8_t* exps, int64_t rows, int D, void* index,
+                         void* stream);
+
+/*
  * Differential working-set update (KVMEM, section "engineering: tiered
  * movement, page-table aliasing and position-consistent rebuild"): of the new
  * working set W_t only the blocks that are not resident in the page pool are

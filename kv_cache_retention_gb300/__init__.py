@@ -76,6 +76,8 @@ SIGNATURES = {
     "kvsel_rule_scores_batch": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I64, _I64, _P, _I, _P]),
     "kvsel_topk_retain_batch": (_I, [_P, _P, _I, _P, _P]),
     "kvsel_span_keep": (_I, [_P, _P, _P, _I, _P, _I, _P, _I, _P, _P]),
+    "kvsel_index_to_fp8": (_I, [_P, _P, _I64, _I, _P, _P, _P]),
+    "kvsel_index_from_fp8": (_I, [_P, _P, _P, _I64, _I, _P, _P]),
     "kvsel_workset_diff": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "kvsel_restore_blocks": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _D, _I, _P, _P,
                                   _I, _P]),
@@ -200,6 +202,14 @@ def kvsel_topk_retain_batch(ctx, sessions, S, n_keep_host, stream):
 
 def kvsel_span_keep(ctx, span_start, span_end, n_cursors, del_ids, n_del, keep_in, N, keep_out, stream):
     return _lib.kvsel_span_keep(ctx, span_start, span_end, n_cursors, del_ids, n_del, keep_in, N, keep_out, stream)
+
+
+def kvsel_index_to_fp8(ctx, index, rows, D, codes, exps, stream):
+    return _lib.kvsel_index_to_fp8(ctx, index, rows, D, codes, exps, stream)
+
+
+def kvsel_index_from_fp8(ctx, codes, exps, rows, D, index, stream):
+    return _lib.kvsel_index_from_fp8(ctx, codes, exps, rows, D, index, stream)
 
 
 def kvsel_workset_diff(ctx, prev_ids, prev_pages, n_prev, new_ids, n_new, P, page, new_pages, shift, in_rank,
@@ -438,6 +448,31 @@ class Context:
                                     _ptr(del_ids, i32, "del_ids") if n_del else None, n_del,
                                     _ptr(keep_in, torch.uint8, "keep_in"), int(N),
                                     _ptr(keep_out, torch.uint8, "keep_out"), self._stream(stream)))
+
+    def index_to_fp8(self, index, codes=None, exps=None, stream=None):
+        """bf16 index [..., D] -> (E4M3 codes uint8 [..., D], scale exponents int8 [...]) as CUDA tensors."""
+        torch = _torch()
+        D = index.shape[-1]
+        rows = index.numel() // D if D else 0
+        if codes is None:
+            codes = torch.empty(index.shape, dtype=torch.uint8, device=index.device)
+        if exps is None:
+            exps = torch.empty(index.shape[:-1], dtype=torch.int8, device=index.device)
+        self._check(kvsel_index_to_fp8(self.handle, _ptr(index, torch.bfloat16, "index"), rows, D,
+                                       _ptr(codes, torch.uint8, "codes"), _ptr(exps, torch.int8, "exps"),
+                                       self._stream(stream)))
+        return codes, exps
+
+    def index_from_fp8(self, codes, exps, index=None, stream=None):
+        """E4M3 codes [..., D] and exponents [...] -> bf16 index [..., D] (CUDA tensors)."""
+        torch = _torch()
+        D = codes.shape[-1]
+        rows = codes.numel() // D if D else 0
+        if index is None:
+            index = torch.empty(codes.shape, dtype=torch.bfloat16, device=codes.device)
+        self._check(kvsel_index_from_fp8(self.handle, _ptr(codes, torch.uint8, "codes"), _ptr(exps, torch.int8, "exps"),
+                                         rows, D, _ptr(index, torch.bfloat16, "index"), self._stream(stream)))
+        return index
 
     def workset_diff(self, prev_ids, prev_pages, new_ids, P, page, out=None, stream=None):
         """Retained / incoming / outgoing split of a new working set (int32 CUDA tensors).

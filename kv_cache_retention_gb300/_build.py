@@ -24,6 +24,7 @@ SOURCES = [
     "rule_scores_noalloc.cu",
     "workset_kernels.cu",
     "stage_pipeline.cu",
+    "fp8_index.cu",
 ]
 HEADERS = ["kvsel_internal.h", os.path.join("..", "..", "include", "kvsel.h")]
 

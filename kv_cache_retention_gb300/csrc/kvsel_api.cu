@@ -339,6 +339,34 @@ int kvsel_span_keep(kvsel_ctx* ctx, const int32_t* span_start, const int32_t* sp
                     "span_keep launch");
 }
 
+int kvsel_index_to_fp8(kvsel_ctx* ctx, const void* index, int64_t rows, int D, uint8_t* codes, int8_t* exps,
+                       void* stream) {
+    int rc = enter(ctx);
+    if (rc) return rc;
+    if (rows < 0) return fail(ctx, KVSEL_ERR_SHAPE, "index_to_fp8: negative row count");
+    if (D != 64 && D != 128 && D != 256) return fail(ctx, KVSEL_ERR_UNSUPPORTED, "index_to_fp8: D=%d unsupported", D);
+    if (rows == 0) return KVSEL_OK;
+    if (!index || !codes || !exps) return fail(ctx, KVSEL_ERR_INVALID_ARG, "index_to_fp8: null pointer");
+    if (!aligned16(index) || (reinterpret_cast<uintptr_t>(codes) & 3u))
+        return fail(ctx, KVSEL_ERR_ALIGN, "index_to_fp8: index must be 16-byte and codes 4-byte aligned");
+    return launched(ctx, launch_index_to_fp8(ctx, index, rows, D, codes, exps, (cudaStream_t)stream),
+                    "index_to_fp8 launch");
+}
+
+int kvsel_index_from_fp8(kvsel_ctx* ctx, const uint8_t* codes, const int8_t* exps, int64_t rows, int D, void* index,
+                         void* stream) {
+    int rc = enter(ctx);
+    if (rc) return rc;
+    if (rows < 0) return fail(ctx, KVSEL_ERR_SHAPE, "index_from_fp8: negative row count");
+    if (D != 64 && D != 128 && D != 256) return fail(ctx, KVSEL_ERR_UNSUPPORTED, "index_from_fp8: D=%d unsupported", D);
+    if (rows == 0) return KVSEL_OK;
+    if (!index || !codes || !exps) return fail(ctx, KVSEL_ERR_INVALID_ARG, "index_from_fp8: null pointer");
+    if (!aligned16(index) || (reinterpret_cast<uintptr_t>(codes) & 3u))
+        return fail(ctx, KVSEL_ERR_ALIGN, "index_from_fp8: index must be 16-byte and codes 4-byte aligned");
+    return launched(ctx, launch_index_from_fp8(ctx, codes, exps, rows, D, index, (cudaStream_t)stream),
+                    "index_from_fp8 launch");
+}
+
 int kvsel_meank_build(kvsel_ctx* ctx, const void* k_src, int L, int Hkv, int T, int D, int block, int first_block,
                       const int32_t* src_pos, double rope_base, int rope_style, void* index, int Bcap, void* stream) {
     int rc = enter(ctx);

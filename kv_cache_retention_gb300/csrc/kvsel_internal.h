@@ -112,6 +112,10 @@ cudaError_t launch_rerope(const void* k_src, int64_t sls, int64_t shs, int src_t
 cudaError_t launch_shift(void* pool, int P, const int32_t* pages, const int32_t* shifts, int n, const int32_t* n_dev,
                          int L, int Hkv, int D, int page, const kvsel_ctx::RopeTab* tab, int rope_style,
                          unsigned* dev_err, cudaStream_t s);
+cudaError_t launch_index_to_fp8(const kvsel_ctx* ctx, const void* index, int64_t rows, int D, uint8_t* codes,
+                                int8_t* exps, cudaStream_t s);
+cudaError_t launch_index_from_fp8(const kvsel_ctx* ctx, const uint8_t* codes, const int8_t* exps, int64_t rows, int D,
+                                  void* index, cudaStream_t s);
 cudaError_t launch_span_keep(const int32_t* span_start, const int32_t* span_end, int n_cursors, const int32_t* del_ids,
                              int n_del, const uint8_t* keep_in, int N, uint8_t* keep_out, unsigned* dev_err,
                              cudaStream_t s);
