@@ -95,9 +95,7 @@ __global__ void __launch_bounds__(256) memory_update_kernel(const T* __restrict_
     for (int k = 0; k < VEC; ++k) acc[k] = 0.f;
     if (r0 < rpi) {
         const T* base = q + (int64_t)head * R * D + (int64_t)c * VEC;
-#pragma unroll 4
-        for (int r = r0; r < R; r += rpi) {
-            uint4 raw = __ldg(reinterpret_cast<const uint4*>(base + (int64_t)r * D));
+        auto add = [&](const uint4& raw) {
             if constexpr (sizeof(T) == 2) {
                 const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
@@ -112,7 +110,19 @@ __global__ void __launch_bounds__(256) memory_update_kernel(const T* __restrict_
                 acc[2] += __uint_as_float(raw.z);
                 acc[3] += __uint_as_float(raw.w);
             }
+        };
+        // batches of kMemBatch 16-byte loads issued before any is summed: a head's rows are
+        // one short stream per thread, so memory-level parallelism has to come from here
+        constexpr int kMemBatch = 8;
+        int r = r0;
+        for (; r + (kMemBatch - 1) * rpi < R; r += kMemBatch * rpi) {
+            uint4 raw[kMemBatch];
+#pragma unroll
+            for (int j = 0; j < kMemBatch; ++j) raw[j] = __ldg(reinterpret_cast<const uint4*>(base + (int64_t)(r + j * rpi) * D));
+#pragma unroll
+            for (int j = 0; j < kMemBatch; ++j) add(raw[j]);
         }
+        for (; r < R; r += rpi) add(__ldg(reinterpret_cast<const uint4*>(base + (int64_t)r * D)));
 #pragma unroll
         for (int k = 0; k < VEC; ++k) sm[r0 * D + c * VEC + k] = acc[k];
     }
