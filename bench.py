@@ -577,8 +577,8 @@ def profile_case(args):
 
 def all_configs(args):
     """One JSON line per workload: per-call device times of its select step
-    (CUDA events, mean over --steps after --warmup), rows/s and the roofline
-    fraction of its bandwidth- or tensor-bound calls.  Token workloads run the
+    (CUDA events, mean over --steps after --warmup), the step replayed from one
+    CUDA graph, rows/s and the roofline fraction of its bandwidth- or tensor-bound calls.  Token workloads run the
     IntentKV step, block workloads the KVMEM step (full Mean-K build when the
     workload is not incremental; the scatter then reads the raw K of the
     selected blocks)."""
@@ -607,6 +607,31 @@ def all_configs(args):
         torch.cuda.synchronize()
         ctx.check_device()
         return {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in ev.items()}
+
+    def graph_us(calls):
+        """The step's calls captured once in a CUDA graph; mean wall time of a replay (CUDA events)."""
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _, fn in calls:
+                fn()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _, fn in calls:
+                fn()
+        for _ in range(args.warmup):
+            g.replay()
+        a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a0.record()
+        for _ in range(max(1, args.steps)):
+            g.replay()
+        b0.record()
+        torch.cuda.synchronize()
+        ctx.check_device()
+        return 1e3 * a0.elapsed_time(b0) / max(1, args.steps)
 
     def frac(bound, amount, ms):
         if bound == "hbm":
@@ -637,6 +662,7 @@ def all_configs(args):
         es = 2 if tw.dtype == "bf16" else 4
         rows = tw.L * tw.Hkv * tw.n_cand
         line = {"workload": tw.name, "kind": "IntentKV token step", "us_per_select_step": 1e3 * sum(ms.values()),
+                "us_per_select_step_graph": graph_us(calls),
                 "rows_scored_per_s": rows / (sum(ms.values()) / 1e3), "ms": ms,
                 "rule_scores": frac("hbm", tw.L * tw.n_cand * tw.Hkv * tw.D * es + tw.N * 4, ms["rule_scores"])}
         print(json.dumps(line), flush=True)
@@ -669,6 +695,7 @@ def all_configs(args):
         rows = bw.L * bw.Hkv * bw.n_cand
         build_bytes = bw.L * bw.Hkv * (built_tokens + built_tokens // bw.block) * bw.D * 2
         line = {"workload": bw.name, "kind": "KVMEM block step", "us_per_select_step": 1e3 * sum(ms.values()),
+                "us_per_select_step_graph": graph_us(calls),
                 "rows_scored_per_s": rows / (sum(ms.values()) / 1e3), "ms": ms,
                 "meank_build": frac("hbm", build_bytes, ms["meank_build"]),
                 "block_scores": frac("tensor", 2 * bw.L * bw.Hq * bw.M * bw.n_cand * bw.D, ms["block_scores"]),
