@@ -775,9 +775,16 @@ cudaError_t launch_rule_scores_batch(kvsel_ctx* ctx, const void* k_pool, int dty
         total_items += a.n_items;
         max_N = a.N > max_N ? a.N : max_N;
     }
-    // every CTA gets the same number of items, sized to fill the GPU once over all sessions
+    // every CTA gets the same number of items, sized to fill the GPU once over all sessions: the
+    // per-session ceilings must not add up to more CTAs than one wave holds, or a few SMs run a
+    // second round while the rest idle
     const int64_t grid_max = (int64_t)KVSEL_RULE_MINB * ctx->num_sms;
-    const int ipb = (int)((total_items + grid_max - 1) / grid_max > 0 ? (total_items + grid_max - 1) / grid_max : 1);
+    int ipb = (int)((total_items + grid_max - 1) / grid_max > 0 ? (total_items + grid_max - 1) / grid_max : 1);
+    for (;; ++ipb) {
+        int64_t ctas = 0;
+        for (const auto& a : args) ctas += (a.n_items + ipb - 1) / ipb;
+        if (ctas <= grid_max) break;
+    }
     int gx = 1;
     for (auto& a : args) {
         a.items_per_block = ipb;
