@@ -354,9 +354,9 @@ def ours(args, rank, world, local_rank):
 # DRAM bytes (read + write) per call from an ncu capture of the current kernel code, scaled to the
 # bench workload; an entry is removed whenever its kernel changes.  Source: profiles/*.md.
 PROFILED_TRAFFIC = {
-    # block_scores_tc, 4-layer capture of both passes (row 352.5 + 11.7 MB, column 353.8 + 6.5 MB),
+    # block_scores_tc, 4-layer capture of both passes (row 352.5 + 11.4 MB, column 354.0 + 6.6 MB),
     # x16 for 64 layers; profiles/block_scores_tc_ws1m_L4.md
-    "block_scores": 16 * (352.475904 + 11.735552 + 353.757952 + 6.514944) * 1e6,
+    "block_scores": 16 * (352.454912 + 11.352832 + 354.045952 + 6.576640) * 1e6,
 }
 
 

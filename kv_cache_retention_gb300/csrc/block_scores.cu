@@ -22,14 +22,15 @@
 //                -> mass[lg][b], complete per CTA
 //   finalize:    R[b] = sum_lg mass[lg][b] / (L*Hq), in fixed (l,g) order.
 //
-// Kernel structure (one persistent CTA per SM, 576 threads):
+// Kernel structure (one persistent CTA per SM, 608 threads):
 //   warp 0      TMA producer: the unit's fixed tile, then the streamed tiles
 //               (A ring of 2 x 32 KB, B ring of 2 x 64 KB; 128-byte swizzled,
 //               K-major, no multicast)
-//   warp 1      allocates 512 TMEM columns; lane 0 issues tcgen05.mma
-//               (kind::f16, bf16 x bf16 -> fp32, M=128 N=256 K=16, 8 per tile)
-//               into one of two 256-column accumulators and commits to
-//               mbarriers that free the smem stage and hand the accumulator on
+//   warps 1, 18 allocate 512 TMEM columns (warp 1); lane 0 of each issues
+//               tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M=128 N=256 K=16,
+//               8 per tile) for alternate tiles, each into its own 256-column
+//               accumulator, and commits to mbarriers that free the smem stage
+//               and hand the accumulator on
 //   warps 2-17  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
 //               32*(w%4)..+31; four column slices of 64), exp2 on the MUFU,
 //               packed fp32 arithmetic
@@ -79,7 +80,9 @@ constexpr int kEpiWarps = 16;                   // 4 TMEM lane quarters x kSlice
 constexpr int kSlices = kEpiWarps / 4;
 constexpr int kSliceCols = kAccCols / kSlices;  // accumulator columns per epilogue thread and tile
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kIssuer2 = 2 + kEpiWarps;         // the second MMA-issuing warp
+static_assert(kNAcc == 2, "the two MMA issuers own one accumulator each");
+constexpr int kThreads = 64 + kEpiThreads + 32;
 constexpr uint64_t kWaitNs = 1000000000ull;     // 1 s per wait
 #ifndef KVSEL_SUSPEND_NS
 #define KVSEL_SUSPEND_NS 20000
@@ -138,6 +141,16 @@ __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
         : "r"(saddr(b)), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+// Non-blocking: has the phase of parity `parity` completed?
+__device__ __forceinline__ bool mbar_done(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(saddr(b)), "r"(parity)
         : "memory");
     return ok != 0;
 }
@@ -332,14 +345,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < T::kNF; ++i) {
             mbar_init(&t.full_f[i], 1);
-            mbar_init(&t.empty_f[i], 1);
+            mbar_init(&t.empty_f[i], 2);  // both MMA issuers are done with the unit
         }
         for (int i = 0; i < T::kNS; ++i) {
             mbar_init(&t.go[i], 1 + kEpiWarps);  // the stage's copies + the accumulator's release
             mbar_init(&t.empty_s[i], 1);
         }
         for (int i = 0; i < kNAcc; ++i) mbar_init(&t.acc_full[i], 1);
-        mbar_init(&t.mma_done, 1);
+        mbar_init(&t.mma_done, 2);
         t.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapF)) : "memory");
@@ -386,9 +399,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (uint32_t i = (f_it > (uint32_t)T::kNF ? f_it - T::kNF : 0); i < f_it; ++i)
                 drain_phase(&t.full_f[i % T::kNF], (i / T::kNF) & 1);
         }
-    } else if (warp == 1) {
-        // ------------------------------ MMA issuer ------------------------------
+    } else if (warp == 1 || warp == kIssuer2) {
+        // ------------------------------ MMA issuers ------------------------------
+        // Two threads on two SM sub-partitions issue alternate tiles (tile j uses
+        // accumulator j % 2, so each issuer owns one).  One thread alone spent about
+        // as long per tile as the MMAs take: its barrier and tcgen05 instructions
+        // queue behind the epilogue's exp2 instructions on its sub-partition.
         if (lane == 0) {
+            const uint32_t me = warp == 1 ? 0u : 1u;
             uint32_t f_it = 0, s_it = 0, acc_it = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
@@ -399,6 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < a.n_it; ++i) {
                     const int st = s_it % T::kNS;
                     const int k = acc_it % kNAcc;
+                    if ((acc_it & 1u) != me) {  // the other issuer's tile
+                        ++s_it;
+                        ++acc_it;
+                        continue;
+                    }
                     // one wait per tile: the stage's operand has landed and the epilogue has
                     // read the accumulator this tile overwrites
                     if (!(ok = wait_phase(&t.go[st], (s_it / T::kNS) & 1, abort_flag, a.err))) break;
@@ -426,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(&t.mma_done);
             drain_phase(&t.mma_done, 0);
         }
-    } else {
+    } else if (warp < kIssuer2) {
         // ------------------------------ epilogue ------------------------------
         const int ew = warp - 2;                 // 0 .. kEpiWarps-1
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
@@ -455,6 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < 8; ++j) cs[j] = make_float2(0.f, 0.f);
                 if (r_local < a.rows_pad) lse_n = __ldg(lse_lg + r_local);
             }
+            bool ready = false;  // this tile's accumulator was seen complete by the probe below
             for (int i = 0; i < a.n_it; ++i) {
                 const int k = acc_it % kNAcc;
                 // After a timed-out wait a thread waits no more: its warp still runs the
@@ -462,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // math on whatever the accumulator holds, and the epilogue warps agree on
                 // giving up at the end of the unit.  No per-tile vote or branch: in the
                 // column pass that alone cost a tenth of the tensor pipe's time.
-                if (ok) ok = wait_phase(&t.acc_full[k], (acc_it / kNAcc) & 1, abort_flag, a.err);
+                if (ok && !ready) ok = wait_phase(&t.acc_full[k], (acc_it / kNAcc) & 1, abort_flag, a.err);
                 tc_fence_after();
                 const uint32_t taddr =
                     tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(k * kAccCols + slice * kSliceCols);
@@ -474,6 +498,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&t.go[(acc_it + kNAcc) % T::kNS]);  // accumulator k is read
+                    // probe the next tile's accumulator now: the answer arrives while this
+                    // tile's math runs, instead of costing a blocking wait after it
+                    ready = i + 1 < a.n_it && mbar_done(&t.acc_full[(acc_it + 1) % kNAcc], ((acc_it + 1) / kNAcc) & 1);
                     // columns past the candidate range (last tile only) are masked
                     const int nvalid = a.c1 - (a.c0 + i * kAccCols + slice * kSliceCols);
                     if (nvalid < kSliceCols) {
@@ -521,6 +548,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&t.go[(acc_it + kNAcc) % T::kNS]);
+                    // probe the next tile's accumulator now: the answer arrives while this
+                    // tile's math runs, instead of costing a blocking wait after it
+                    ready = i + 1 < a.n_it && mbar_done(&t.acc_full[(acc_it + 1) % kNAcc], ((acc_it + 1) / kNAcc) & 1);
                     // lse2 of the thread's rows, from the lanes that loaded them
                     const int rl = lane >> 2;
                     col_terms(v0, 0, sc, __shfl_sync(0xffffffffu, lse, rl), cs);
