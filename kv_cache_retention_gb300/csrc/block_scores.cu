@@ -67,6 +67,10 @@ struct Tiling {
     static constexpr int kStageBytes = kNF * kFBytes + kNS * kSBytes;
     static_assert(kStageBytes == 192 * 1024, "operand buffers");
     static_assert(kNS >= kNAcc, "a stage ring at least as deep as the accumulator ring");
+    // tile j is issued by MMA thread j % 2 and uses stage j % kNS: with kNS even every stage
+    // belongs to one issuer, which then sees each of its barrier's phases in order (an issuer
+    // skipping the other's phases could mistake an older phase for its own)
+    static_assert(kNS % 2 == 0, "an even stage ring for the two MMA issuers");
 };
 constexpr int kMaxStages = 4;
 // A tile's MMAs wait on one barrier of their operand stage, completed by the
