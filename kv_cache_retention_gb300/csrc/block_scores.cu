@@ -11,29 +11,34 @@
 // on the tensor cores.  In both, A = 128 query rows (one per TMEM lane and
 // epilogue thread) and B = 256 candidate blocks (accumulator columns):
 //   row pass:    a unit is (l,g, 128 query rows); B tiles stream.  Each lane
-//                sums 2^(x - ref) over its row, ref being a reference that only
-//                moves when a tile's sum passes 2^64
+//                sums 2^(x - ref) over its row's 64-column slice, ref being a
+//                reference that only moves when a tile's sum passes 2^64; each
+//                slice's (ref, sum) goes to the workspace and bs_lse_merge
+//                combines the four slices of a row
 //                -> lse2[r] = log2 sum_{b in C} 2^(S[r,b] log2e/sqrt(d))
-//   column pass: a unit is (l,g, 256 candidate blocks); A tiles stream.  Each
-//                lane holds lse2 of its row in a register and adds
-//                2^(x - lse2[r]) into one accumulator per column; at the end of
-//                the unit the columns are summed across lanes (a butterfly
-//                reduce-scatter) and across the four lane quarters
-//                -> mass[lg][b], complete per CTA
+//   column pass: a unit is (l,g, 256 candidate blocks); A tiles stream.  A
+//                warp reads its 32 rows x 64 columns as two 16x256b loads, so a
+//                thread holds 4 rows x 16 columns; it adds 2^(x - lse2[r]) into
+//                16 column sums (lse2 loaded one tile ahead, one lane per row,
+//                handed on by shuffles).  At the end of the unit the columns are
+//                summed across lanes (a butterfly reduce-scatter) and across the
+//                four lane quarters -> mass[lg][b], complete per CTA
 //   finalize:    R[b] = sum_lg mass[lg][b] / (L*Hq), in fixed (l,g) order.
 //
 // Kernel structure (one persistent CTA per SM, 608 threads):
 //   warp 0      TMA producer: the unit's fixed tile, then the streamed tiles
-//               (A ring of 2 x 32 KB, B ring of 2 x 64 KB; 128-byte swizzled,
-//               K-major, no multicast)
+//               (row pass: 2 x 32 KB of query rows, a ring of 2 x 64 KB of
+//               blocks; column pass: 64 KB of blocks, a ring of 4 x 32 KB of
+//               query rows; 128-byte swizzled, K-major, no multicast)
 //   warps 1, 18 allocate 512 TMEM columns (warp 1); lane 0 of each issues
 //               tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M=128 N=256 K=16,
 //               8 per tile) for alternate tiles, each into its own 256-column
 //               accumulator, and commits to mbarriers that free the smem stage
 //               and hand the accumulator on
 //   warps 2-17  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
-//               32*(w%4)..+31; four column slices of 64), exp2 on the MUFU,
-//               packed fp32 arithmetic
+//               32*(w%4)..+31; four column slices of 64), release, a
+//               non-blocking probe of the next tile's accumulator, exp2 on the
+//               MUFU, packed fp32 arithmetic
 // Every mbarrier wait is bounded (1 s of globaltimer); on a timeout the CTA
 // flags KVSEL_ERR_TIMEOUT in the device error word, drains its own copies and
 // MMAs, frees TMEM and returns.
