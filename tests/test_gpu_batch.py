@@ -65,6 +65,42 @@ def test_rule_scores_batch_matches_single_calls(ctx, dtype, L, Hq, Hkv, D):
         assert_scores_close(f64(rules[i][:x["N"]]), ref, what=f"session {i} vs oracle")
 
 
+def test_rule_scores_batch_full_size(ctx):
+    """The batched bench case at full size: 36 sessions of 1024-8192 tokens at the 8B shape
+    (L36 Hq32 Hkv8 D128) in one shared paged pool; every session against its single-session
+    call, two against the oracle."""
+    rng = np.random.default_rng(36)
+    torch.manual_seed(36)
+    L, Hq, Hkv, D = 36, 32, 8, 128
+    Ns = [int(x) for x in rng.integers(1024, 8193, 36)]
+    n_slots = sum((x + 15) // 16 for x in Ns) * 16
+    pool = torch.randn((L, n_slots, Hkv, D), device="cuda").to(torch.bfloat16)
+    perm, at, sess = rng.permutation(n_slots // 16), 0, []
+    for N in Ns:
+        m = (N + 15) // 16
+        j = np.arange(N)
+        smap = torch.as_tensor((perm[at:at + m][j // 16] * 16 + j % 16).astype(np.int32), device="cuda")
+        at += m
+        M = torch.nn.functional.normalize(torch.randn((L, Hq, D), device="cuda"), dim=-1)
+        sess.append({"N": N, "slot_map": smap, "M": M, "forced": (64, N - 256, N)})
+    rules = [torch.empty(N, device="cuda") for N in Ns]
+    ctx.rule_scores_batch(pool, [x["M"] for x in sess], L, Hq, Hkv, Ns, D, [x["forced"] for x in sess], rules,
+                          slot_maps=[x["slot_map"] for x in sess], n_slots=n_slots)
+    ctx.check_device()
+    for i, x in enumerate(sess):
+        single = torch.empty(x["N"], device="cuda")
+        ctx.rule_scores(pool, x["M"], L, Hq, Hkv, x["N"], D, *x["forced"], single, slot_map=x["slot_map"],
+                        n_slots=n_slots)
+        assert_scores_close(f64(rules[i]), f64(single), what=f"session {i} vs single call")
+    ctx.check_device()
+    host_pool = bits(pool).ravel()
+    for i in (0, 35):
+        x = sess[i]
+        ref = oracle.rule_scores(host_pool, x["M"].cpu().double().numpy(), L, Hq, Hkv, x["N"], D, *x["forced"],
+                                 slot_map=x["slot_map"].cpu().numpy(), layer_stride=n_slots * Hkv * D)
+        assert_scores_close(f64(rules[i]), ref, what=f"session {i} vs oracle")
+
+
 def test_topk_retain_batch_equals_single_calls(ctx):
     rng = np.random.default_rng(4)
     Ns = [5000, 1, 150000, 32768, 777, 131072]

@@ -154,6 +154,47 @@ def test_restore_blocks_parity(ctx, style):
         _bf16_within(got[:, dpg[i]], ref_k[:, dpg[i]], 2, f"restore entry {i}", floor=_pair_floor(raw))
 
 
+def test_restore_and_shift_full_size_sampled(ctx):
+    """The 1M-workspace restore at full size: 2048 blocks (L64 Hkv8 D128, 32-token pages) restored
+    into a shuffled pool of 2180 pages; V compared whole on the device, K on sampled (layer, entry)
+    pairs against the oracle; then those pages shifted in place and sampled again."""
+    L, Hkv, D, page, nblk, P = 64, 8, 128, 32, 2048, 2180
+    gen = torch.Generator(device="cuda").manual_seed(2048)
+    k = torch.randn((L, Hkv, nblk * page, D), generator=gen, device="cuda").to(torch.bfloat16)
+    v = torch.randn((L, Hkv, nblk * page, D), generator=gen, device="cuda").to(torch.bfloat16)
+    kp = torch.zeros((L, P, page, Hkv, D), device="cuda", dtype=torch.bfloat16)
+    vp = torch.zeros_like(kp)
+    rng = np.random.default_rng(9)
+    src = rng.permutation(nblk).astype(np.int32)
+    dpg = rng.choice(P, nblk, replace=False).astype(np.int32)
+    pos0 = (np.arange(nblk, dtype=np.int32) + 4) * page
+    ctx.restore_blocks(k, v, _i32(src), _i32(dpg), _i32(pos0), kp, vp, 1e6)
+    ctx.check_device()
+    # V: every restored page is the source block's rows, bit for bit
+    v_rows = v.view(L, Hkv, nblk, page, D)[:, :, torch.as_tensor(src, device="cuda")].permute(0, 2, 3, 1, 4)
+    assert torch.equal(vp[:, torch.as_tensor(dpg, device="cuda")], v_rows)
+    del v_rows
+    # K: sampled (layer, entry) pairs against the oracle (2 bf16 ulp of the rotation pair norm)
+    for l, i in [(0, 0), (17, 1000), (L - 1, nblk - 1)]:
+        k_l = bits(k[l:l + 1])
+        one = np.zeros((1, 1, page, Hkv, D), np.uint16)
+        ref_k, _ = oracle.restore_blocks(k_l, k_l, src[i:i + 1], np.zeros(1, np.int32), pos0[i:i + 1], one, one.copy(),
+                                         page, 1e6)
+        raw = k_l[:, :, src[i] * page:(src[i] + 1) * page].transpose(0, 2, 1, 3)
+        _bf16_within(bits(kp[l:l + 1, int(dpg[i])]), ref_k[:, 0], 2, f"restored K l={l} entry {i}",
+                     floor=_pair_floor(raw))
+    # in-place shift of every restored page by its own offset
+    shifts = rng.integers(-2 ** 16, 2 ** 16, nblk).astype(np.int32)
+    samples = [(3, 5), (40, 2047)]
+    before = {(l, i): bits(kp[l:l + 1, int(dpg[i])]) for l, i in samples}
+    ctx.rerope_shift(kp, _i32(dpg), _i32(shifts), 1e6)
+    ctx.check_device()
+    for (l, i), b0 in before.items():
+        ref = oracle.rerope_shift(b0[:, None], np.zeros(1, np.int32), shifts[i:i + 1], page, 1e6)
+        _bf16_within(bits(kp[l:l + 1, int(dpg[i])]), ref[:, 0], 2, f"shifted K l={l} entry {i}",
+                     floor=_pair_floor(b0))
+
+
 def test_restore_blocks_device_count(ctx):
     """Entries at or past the device-side count leave their pages untouched."""
     L, Hkv, D, page, P = 2, 2, 64, 16, 6
