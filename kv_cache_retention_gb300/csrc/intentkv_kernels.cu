@@ -2,20 +2,17 @@
 // (Sec. 3.2, Eq. 3-4) and the dead-slot redirect of the layout layer.
 //
 // Rule scores run in three launches so that K is read from HBM exactly once:
-//   1. rule_logits: one sweep over the K rows of every (layer, candidate
-//      token).  A producer warp looks each token up in the slot map (kept in
-//      shared memory one 256-token chunk ahead) and copies
-//      its whole K row (all kv heads, contiguous in the pool) into a 4-stage
-//      shared-memory ring with one bulk asynchronous copy (cp.async.bulk,
-//      L2 evict-first) completing on an mbarrier; 12 consumer warps read 32-byte
-//      pieces of the rows and multiply each against the G = Hq/Hkv query heads
-//      that share its kv head (GQA reuse, packed fp32x2 FMA, M in registers).
-//      The per-head partial dot products are summed across the D/16 lanes of
-//      the head with a halving shuffle exchange, and the logits (pre-scaled into
-//      the exp2 domain) go through a shared-memory tile to coalesced stores.
-//      At every tile flush one warp per head reduces the tile's (max, sum
-//      2^(z-max)) and merges it into the chunk's; one pair per (l, h, 256-token
-//      chunk) goes to global memory.
+//   1. rule_logits: one sweep over the K rows of every (layer, kv head,
+//      candidate token).  A warp task is 64 tokens of one (layer, kv head);
+//      lane t owns tokens t and t + 32 and loads their rows straight from the
+//      pool (through the slot map) in 32-byte pieces, two pieces per token in
+//      flight in a register ring that runs on into the next task.  Each piece
+//      is multiplied against the G = Hq/Hkv query heads that share the kv head
+//      (GQA reuse, packed fp32x2 FMA, M broadcast from the warp's slice of
+//      shared memory).  Logits, pre-scaled into the exp2 domain, are stored
+//      coalesced along tokens, and each lane keeps an online (max, sum
+//      2^(z-max)) per head, merged across the warp once per run of one (layer,
+//      kv head); one pair per (l, h, 64-token chunk) goes to global memory.
 //   2. rule_lse: merges the chunk partials into log2-sum-exp per (l,h).
 //   3. rule_accum: rule[j] = sum_{l,h} 2^(z - lse), a token-parallel pass over
 //      the logits (coalesced along j), reduced across warps in a fixed order.
