@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(256) memory_update_kernel(const T* __restrict_
     __shared__ float red[32];
     const int head = blockIdx.x;
     const int chunks = D / VEC;
-    const int rpi = 256 / chunks;
+    const int rpi = blockDim.x / chunks;
     const int c = threadIdx.x % chunks, r0 = threadIdx.x / chunks;
     float acc[VEC];
 #pragma unroll
@@ -616,22 +616,28 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 
+// Threads per QueryMemory block: 128 (a head per block, all heads resident at once on
+// GB300, each thread with eight 16-byte loads in flight) unless a row has more
+// 16-byte chunks than that.
+int mu_threads(int chunks) { return chunks > 128 ? 256 : 128; }
+
 cudaError_t launch_memory_update(const void* q, int dtype, int L, int Hq, int R, int D, float lambda, int first_turn,
                                  int norm_mode, float* M, float* A, cudaStream_t s) {
     const float decay = expf(-lambda);
     const int vec = dtype == KVSEL_BF16 ? 8 : 4;
-    const int rpi = 256 / (D / vec);
+    const int nt = mu_threads(D / vec);
+    const int rpi = nt / (D / vec);
     const size_t smem = sizeof(float) * ((size_t)rpi * D + D);
     const int heads = L * Hq;
     if (dtype == KVSEL_BF16) {
         if (smem > 48 * 1024)
             cudaFuncSetAttribute(memory_update_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        memory_update_kernel<__nv_bfloat16><<<heads, 256, smem, s>>>(static_cast<const __nv_bfloat16*>(q), R, D, decay,
+        memory_update_kernel<__nv_bfloat16><<<heads, nt, smem, s>>>(static_cast<const __nv_bfloat16*>(q), R, D, decay,
                                                                       first_turn, norm_mode, M, A, nullptr);
     } else {
         if (smem > 48 * 1024)
             cudaFuncSetAttribute(memory_update_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        memory_update_kernel<float><<<heads, 256, smem, s>>>(static_cast<const float*>(q), R, D, decay, first_turn,
+        memory_update_kernel<float><<<heads, nt, smem, s>>>(static_cast<const float*>(q), R, D, decay, first_turn,
                                                              norm_mode, M, A, nullptr);
     }
     return cudaGetLastError();
@@ -648,17 +654,18 @@ cudaError_t launch_memory_update_batch(int dtype, int L, int Hq, int D, int norm
     cudaError_t e = cudaMemcpyAsync(dev, jobs.data(), (size_t)S * sizeof(MemJob), cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return e;
     const int vec = dtype == KVSEL_BF16 ? 8 : 4;
-    const int rpi = 256 / (D / vec);
+    const int nt = mu_threads(D / vec);
+    const int rpi = nt / (D / vec);
     const size_t smem = sizeof(float) * ((size_t)rpi * D + D);
     const dim3 grid((unsigned)(L * Hq), (unsigned)S);
     if (dtype == KVSEL_BF16) {
         if (smem > 48 * 1024)
             cudaFuncSetAttribute(memory_update_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        memory_update_kernel<__nv_bfloat16><<<grid, 256, smem, s>>>(nullptr, 0, D, 0.f, 0, norm_mode, nullptr, nullptr, dev);
+        memory_update_kernel<__nv_bfloat16><<<grid, nt, smem, s>>>(nullptr, 0, D, 0.f, 0, norm_mode, nullptr, nullptr, dev);
     } else {
         if (smem > 48 * 1024)
             cudaFuncSetAttribute(memory_update_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        memory_update_kernel<float><<<grid, 256, smem, s>>>(nullptr, 0, D, 0.f, 0, norm_mode, nullptr, nullptr, dev);
+        memory_update_kernel<float><<<grid, nt, smem, s>>>(nullptr, 0, D, 0.f, 0, norm_mode, nullptr, nullptr, dev);
     }
     return cudaGetLastError();
 }
