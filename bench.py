@@ -606,7 +606,18 @@ def all_configs(args):
                 ev.setdefault(name, []).append((a, b))
         torch.cuda.synchronize()
         ctx.check_device()
-        return {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in ev.items()}
+        per_call = {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in ev.items()}
+        # whole steps with no per-call events (what a caller sees per step; for the µs-scale
+        # workloads the per-call events themselves cost host time)
+        a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        for _ in range(args.steps):
+            for _, fn in calls:
+                fn()
+        b0.record()
+        torch.cuda.synchronize()
+        ctx.check_device()
+        return per_call, 1e3 * a0.elapsed_time(b0) / max(1, args.steps)
 
     def graph_us(calls):
         """The step's calls captured once in a CUDA graph; mean wall time of a replay (CUDA events)."""
@@ -658,12 +669,12 @@ def all_configs(args):
             ("topk_retain", lambda: ctx.topk_retain(rule, tw.pi, tw.q_s, tw.q_e, tw.C, keep=keep, keep_idx=keep_idx)),
             ("redirect_slots", lambda: ctx.redirect_slots(smap, keep, tw.dead_slot, slot_out)),
         ]
-        ms = timed(calls)
+        ms, step_us = timed(calls)
         es = 2 if tw.dtype == "bf16" else 4
         rows = tw.L * tw.Hkv * tw.n_cand
-        line = {"workload": tw.name, "kind": "IntentKV token step", "us_per_select_step": 1e3 * sum(ms.values()),
+        line = {"workload": tw.name, "kind": "IntentKV token step", "us_per_select_step": step_us,
                 "us_per_select_step_graph": graph_us(calls),
-                "rows_scored_per_s": rows / (sum(ms.values()) / 1e3), "ms": ms,
+                "rows_scored_per_s": rows / (step_us / 1e6), "ms": ms,
                 "rule_scores": frac("hbm", tw.L * tw.n_cand * tw.Hkv * tw.D * es + tw.N * 4, ms["rule_scores"])}
         print(json.dumps(line), flush=True)
         del t, M
@@ -691,12 +702,12 @@ def all_configs(args):
             ("select_blocks", lambda: ctx.select_blocks(R, bw.n_sink, bw.n_recent, bw.k, ids)),
             ("rerope_scatter", scatter),
         ]
-        ms = timed(calls)
+        ms, step_us = timed(calls)
         rows = bw.L * bw.Hkv * bw.n_cand
         build_bytes = bw.L * bw.Hkv * (built_tokens + built_tokens // bw.block) * bw.D * 2
-        line = {"workload": bw.name, "kind": "KVMEM block step", "us_per_select_step": 1e3 * sum(ms.values()),
+        line = {"workload": bw.name, "kind": "KVMEM block step", "us_per_select_step": step_us,
                 "us_per_select_step_graph": graph_us(calls),
-                "rows_scored_per_s": rows / (sum(ms.values()) / 1e3), "ms": ms,
+                "rows_scored_per_s": rows / (step_us / 1e6), "ms": ms,
                 "meank_build": frac("hbm", build_bytes, ms["meank_build"]),
                 "block_scores": frac("tensor", 2 * bw.L * bw.Hq * bw.M * bw.n_cand * bw.D, ms["block_scores"]),
                 "rerope_scatter": frac("hbm", 2 * bw.L * bw.Hkv * moved_blocks * bw.block * bw.D * 2,

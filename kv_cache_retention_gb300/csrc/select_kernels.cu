@@ -9,8 +9,9 @@
 // The keep set is therefore a pure function of the scores: ties resolve to the
 // lower index, NaN ranks lowest, -0 == +0.
 //
-// N <= 131072 (every workload here): one cluster of 8 CTAs, keys in registers.
-// Larger N: one 1024-thread block re-reading the scores for each pass.
+// N <= 16384: one CTA, keys in registers.  N <= 131072: the same code on one
+// cluster of 8 CTAs, histograms merged through distributed shared memory.  Larger
+// N: one 1024-thread block re-reading the scores for each pass.
 #include <cooperative_groups.h>
 
 #include <vector>
@@ -199,13 +200,33 @@ struct TopkJob {
     int32_t* keep_idx;
 };
 
-// batch: NULL, or one TopkJob per cluster (cluster c = CTAs 8c .. 8c+7 takes
-// batch[c]); the scalar arguments are then ignored.
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
-    topk_cluster_kernel(const float* __restrict__ score, int N, int pi, int q_s, int q_e, int need, int n_cand,
-                        uint8_t* __restrict__ keep, int32_t* __restrict__ keep_idx, const TopkJob* __restrict__ batch) {
+// The selection over a cluster of CL CTAs.  batch: NULL, or one TopkJob per
+// cluster (cluster c = CTAs CL*c .. CL*c + CL - 1 takes batch[c]); the scalar
+// arguments are then ignored.  CL = 1 is a plain (non-cluster) launch of one CTA
+// per selection.
+// Cluster barrier and distributed shared memory view; a lone CTA (CL = 1) uses a
+// block barrier and its own shared memory.
+template <int CL>
+__device__ __forceinline__ void csync() {
+    if constexpr (CL == 1)
+        __syncthreads();
+    else
+        cg::this_cluster().sync();
+}
+template <int CL, typename T>
+__device__ __forceinline__ T* cmap(T* p, int r) {
+    if constexpr (CL == 1)
+        return p;
+    else
+        return cg::this_cluster().map_shared_rank(p, r);
+}
+
+template <int CL>
+__device__ __forceinline__ void topk_select(const float* __restrict__ score, int N, int pi, int q_s, int q_e, int need,
+                                            int n_cand, uint8_t* __restrict__ keep, int32_t* __restrict__ keep_idx,
+                                            const TopkJob* __restrict__ batch) {
     if (batch) {
-        const TopkJob& b = batch[blockIdx.x / kCluster];
+        const TopkJob& b = batch[blockIdx.x / CL];
         score = b.score;
         N = b.N;
         pi = b.pi;
@@ -222,12 +243,12 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     __shared__ int warp_sums[33];
     __shared__ int cta_tot[2];              // this CTA's (ties, kept) totals
     __shared__ uint32_t s_prefix, s_remaining;
-    cg::cluster_group cluster = cg::this_cluster();
-    const int rank = (int)cluster.block_rank();
+    int rank = 0;
+    if constexpr (CL > 1) rank = (int)cg::this_cluster().block_rank();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     // contiguous ranges: CTA rank -> [cb, ce), thread -> [j0, j1)
-    const int per_cta = (N + kCluster - 1) / kCluster;
+    const int per_cta = (N + CL - 1) / CL;
     const int cb = min(N, rank * per_cta), ce = min(N, cb + per_cta);
     const int per_thr = (ce - cb + kThreads - 1) / kThreads;
     const int j0 = min(ce, cb + tid * per_thr), j1 = min(ce, j0 + per_thr);
@@ -261,10 +282,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
                 for (int w = 0; w < 8; ++w) c += sub[w][tid];
                 hist[buf][tid] = c;
             }
-            cluster.sync();  // every CTA's histogram is complete
+            csync<CL>();  // every CTA's histogram is complete
             if (tid < 256) {
                 uint32_t c = 0;
-                for (int r = 0; r < kCluster; ++r) c += cluster.map_shared_rank(&hist[buf][0], r)[tid];
+                for (int r = 0; r < CL; ++r) c += cmap<CL>(&hist[buf][0], r)[tid];
                 tot[tid] = c;
             }
             __syncthreads();
@@ -314,8 +335,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     int total;
     int tie_base = block_exclusive_scan(ties, warp_sums, total);
     if (tid == 0) cta_tot[0] = total;
-    cluster.sync();
-    for (int r = 0; r < rank; ++r) tie_base += cluster.map_shared_rank(&cta_tot[0], r)[0];
+    csync<CL>();
+    for (int r = 0; r < rank; ++r) tie_base += cmap<CL>(&cta_tot[0], r)[0];
 
     int kept = 0;
     uint32_t keep_bits = 0;
@@ -338,8 +359,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     }
     int out_base = block_exclusive_scan(kept, warp_sums, total);
     if (tid == 0) cta_tot[1] = total;
-    cluster.sync();
-    for (int r = 0; r < rank; ++r) out_base += cluster.map_shared_rank(&cta_tot[1], r)[0];
+    csync<CL>();
+    for (int r = 0; r < rank; ++r) out_base += cmap<CL>(&cta_tot[1], r)[0];
     int pos = out_base;
 #pragma unroll
     for (int k = 0; k < kKeys; ++k) {
@@ -349,14 +370,30 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
         if (kk && keep_idx) keep_idx[pos] = j0 + k;
         pos += kk;
     }
-    cluster.sync();  // no CTA leaves while another may still read its shared memory
+    csync<CL>();  // no CTA leaves while another may still read its shared memory
+}
+
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
+    topk_cluster_kernel(const float* __restrict__ score, int N, int pi, int q_s, int q_e, int need, int n_cand,
+                        uint8_t* __restrict__ keep, int32_t* __restrict__ keep_idx, const TopkJob* __restrict__ batch) {
+    topk_select<kCluster>(score, N, pi, q_s, q_e, need, n_cand, keep, keep_idx, batch);
+}
+
+// N <= kCtaCap: one CTA, no cluster launch and no cross-CTA barrier.
+constexpr int kCtaCap = kThreads * kKeys;
+__global__ void __launch_bounds__(kThreads)
+    topk_cta_kernel(const float* __restrict__ score, int N, int pi, int q_s, int q_e, int need, int n_cand,
+                    uint8_t* __restrict__ keep, int32_t* __restrict__ keep_idx, const TopkJob* __restrict__ batch) {
+    topk_select<1>(score, N, pi, q_s, q_e, need, n_cand, keep, keep_idx, batch);
 }
 
 }  // namespace
 
 cudaError_t launch_topk(const float* score, int N, int pi, int q_s, int q_e, int need, int n_cand, uint8_t* keep,
                         int32_t* keep_idx, cudaStream_t s) {
-    if (N <= kClusterCap)
+    if (N <= kCtaCap)
+        topk_cta_kernel<<<1, kThreads, 0, s>>>(score, N, pi, q_s, q_e, need, n_cand, keep, keep_idx, nullptr);
+    else if (N <= kClusterCap)
         topk_cluster_kernel<<<kCluster, kThreads, 0, s>>>(score, N, pi, q_s, q_e, need, n_cand, keep, keep_idx, nullptr);
     else
         topk_kernel<<<1, kThreads, 0, s>>>(score, N, pi, q_s, q_e, need, n_cand, keep, keep_idx);
@@ -365,8 +402,9 @@ cudaError_t launch_topk(const float* score, int N, int pi, int q_s, int q_e, int
 
 size_t topk_batch_workspace(int S) { return (size_t)S * sizeof(TopkJob) + 256; }
 
-// Sessions that fit one cluster share one launch (a cluster each); larger ones take
-// the single-CTA kernel one by one.  need / n_cand per session as kvsel_topk_retain.
+// Sessions that fit one cluster share one launch (a cluster each, or a CTA each when
+// every such session fits one CTA); larger ones take the single-CTA re-reading
+// kernel one by one.  need / n_cand per session as kvsel_topk_retain.
 cudaError_t launch_topk_batch(const kvsel_topk_session* sess, const int* need, const int* n_cand, int S, void* ws,
                               cudaStream_t s) {
     std::vector<TopkJob> jobs;
@@ -384,8 +422,13 @@ cudaError_t launch_topk_batch(const kvsel_topk_session* sess, const int* need, c
         TopkJob* dev = static_cast<TopkJob*>(ws);
         cudaError_t e = cudaMemcpyAsync(dev, jobs.data(), jobs.size() * sizeof(TopkJob), cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess) return e;
-        topk_cluster_kernel<<<(unsigned)(kCluster * jobs.size()), kThreads, 0, s>>>(nullptr, 0, 0, 0, 0, 0, 0, nullptr,
-                                                                                   nullptr, dev);
+        bool small = true;
+        for (const TopkJob& j : jobs) small = small && j.N <= kCtaCap;
+        if (small)
+            topk_cta_kernel<<<(unsigned)jobs.size(), kThreads, 0, s>>>(nullptr, 0, 0, 0, 0, 0, 0, nullptr, nullptr, dev);
+        else
+            topk_cluster_kernel<<<(unsigned)(kCluster * jobs.size()), kThreads, 0, s>>>(nullptr, 0, 0, 0, 0, 0, 0,
+                                                                                       nullptr, nullptr, dev);
     }
     return cudaGetLastError();
 }
