@@ -177,3 +177,25 @@ def test_batched_token_step(ctx):
         assert_scores_close(f64(rules[i]), f64(r1), what=f"session {i} rule")
         ref_keep, _ = oracle.topk_retain(f64(rules[i]), *x["forced"], Cs[i])  # on the batched scores
         assert np.array_equal(keeps[i].cpu().numpy(), ref_keep)
+
+
+def test_topk_retain_batch_all_small_sessions(ctx):
+    """Every session fits one CTA (N <= 16384): the batch runs one CTA per session."""
+    rng = np.random.default_rng(5)
+    Ns = [16384, 1, 2048, 16383, 300, 9000, 16384]
+    Cs = [1000, 1, 2048, 20000, 0, 4500, 16383]
+    rules, forced = [], []
+    for N in Ns:
+        r = np.round(rng.standard_normal(N) * 8) / 8  # many ties
+        rules.append(torch.as_tensor(r.astype(np.float32), device="cuda"))
+        pi = min(N, 32)
+        forced.append((pi, max(pi, N - 64), N))
+    keeps = [torch.empty(N, dtype=torch.uint8, device="cuda") for N in Ns]
+    idxs = [torch.empty(N, dtype=torch.int32, device="cuda") for N in Ns]
+    n_keep = ctx.topk_retain_batch(rules, forced, Cs, keeps, idxs)
+    ctx.check_device()
+    for i, N in enumerate(Ns):
+        ref_keep, ref_idx = oracle.topk_retain(f64(rules[i]), *forced[i], Cs[i])
+        assert n_keep[i] == ref_idx.size, f"session {i} (N {N})"
+        assert np.array_equal(keeps[i].cpu().numpy(), ref_keep), f"session {i} (N {N})"
+        assert np.array_equal(idxs[i][:n_keep[i]].cpu().numpy(), ref_idx), f"session {i} (N {N})"

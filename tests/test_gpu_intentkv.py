@@ -197,7 +197,8 @@ def test_rule_scores_bad_slot_sets_device_error(ctx):
 
 @pytest.mark.parametrize("N,pi,qs,qe,C", [(5000, 64, 4872, 5000, 512), (92160, 256, 91136, 92160, 8192),
                                           (100, 10, 90, 100, 100), (100, 10, 90, 100, 5), (100, 100, 100, 100, 7),
-                                          (1, 0, 1, 1, 0), (3000, 0, 3000, 3000, 2999), (777, 5, 700, 777, 200)])
+                                          (1, 0, 1, 1, 0), (3000, 0, 3000, 3000, 2999), (777, 5, 700, 777, 200),
+                                          (16384, 64, 16000, 16384, 4096), (16385, 64, 16000, 16385, 4096)])
 def test_topk_exact_on_same_scores(ctx, N, pi, qs, qe, C):
     gen = torch.Generator(device="cuda").manual_seed(N + C)
     s = torch.rand(N, generator=gen, device="cuda")

@@ -161,7 +161,8 @@ def test_block_scores_full_size_sampled(ctx, name):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("nb,S,Rc,k", [(8192, 4, 64, 1024), (32768, 4, 128, 2048), (100, 4, 10, 200), (50, 30, 30, 5),
-                                       (1, 0, 0, 1), (1000, 0, 0, 0), (777, 3, 5, 769)])
+                                       (1, 0, 0, 1), (1000, 0, 0, 0), (777, 3, 5, 769),
+                                       (16384, 4, 64, 1024), (16385, 4, 64, 1024)])
 def test_select_exact_on_same_scores(ctx, nb, S, Rc, k):
     gen = torch.Generator(device="cuda").manual_seed(nb + k)
     R = torch.round(torch.rand(nb, generator=gen, device="cuda") * 100) / 100
