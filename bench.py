@@ -324,6 +324,8 @@ def ours(args, rank, world, local_rank):
     for name in ("topk_retain", "redirect_slots", "select_blocks"):
         if name in per_call:
             kernels[name] = {"bound": "latency", "ms": per_call[name]}
+    if "block_scores" in kernels:  # (query token x candidate block) pairs scored, over all layer-heads
+        kernels["block_scores"]["pairs_per_s"] = bw.L * bw.Hq * bw.M * bw.n_cand / (kernels["block_scores"]["ms"] / 1e3)
     dom = max((k for k in kernels if "achieved" in kernels[k]), key=lambda k: kernels[k]["ms"])
     d = kernels[dom]
     traffic = _profiled_traffic(dom)
@@ -408,10 +410,32 @@ def oracle_sample(tw, bw, budget_layers=2, block_queries=256):
     return est, desc
 
 
+def host_cpu():
+    """The host's CPU model (x86: the model name; Arm: implementer and part from MIDR) and core count."""
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for line in info.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+        if not model:
+            imp = [ln.split(":", 1)[1].strip() for ln in info.splitlines() if ln.startswith("CPU implementer")]
+            part = [ln.split(":", 1)[1].strip() for ln in info.splitlines() if ln.startswith("CPU part")]
+            if imp and part:
+                model = f"arm implementer {imp[0]} part {part[0]}"
+    except OSError:
+        pass
+    import platform
+    return {"model": model or platform.machine(), "nproc": os.cpu_count()}
+
+
 def cpu_baseline(args, tw, bw):
     est, desc = oracle_sample(tw, bw)
     token_rows, block_rows = workload_rows(tw, bw)
-    return {"value": (token_rows + block_rows) / est, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": desc}
+    return {"value": (token_rows + block_rows) / est, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": desc,
+            "host": host_cpu()}
 
 
 def reference(args, rank, world):
@@ -434,7 +458,8 @@ def reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded; shapes of the pages' workloads)", "config": config_dict(tw, bw, world),
-            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": desc,
+                             "host": host_cpu()},
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": wall}
     print(json.dumps(line), flush=True)
@@ -606,18 +631,18 @@ def all_configs(args):
                 ev.setdefault(name, []).append((a, b))
         torch.cuda.synchronize()
         ctx.check_device()
-        per_call = {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in ev.items()}
+        per_call = {k: statistics.median(a.elapsed_time(b) for a, b in v) for k, v in ev.items()}
         # whole steps with no per-call events (what a caller sees per step; for the µs-scale
-        # workloads the per-call events themselves cost host time)
-        a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a0.record()
-        for _ in range(args.steps):
+        # workloads the per-call events themselves cost host time); median over steps
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        marks[0].record()
+        for i in range(args.steps):
             for _, fn in calls:
                 fn()
-        b0.record()
+            marks[i + 1].record()
         torch.cuda.synchronize()
         ctx.check_device()
-        return per_call, 1e3 * a0.elapsed_time(b0) / max(1, args.steps)
+        return per_call, 1e3 * statistics.median(marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps))
 
     def graph_us(calls):
         """The step's calls captured once in a CUDA graph; mean wall time of a replay (CUDA events)."""
@@ -712,6 +737,7 @@ def all_configs(args):
                 "block_scores": frac("tensor", 2 * bw.L * bw.Hq * bw.M * bw.n_cand * bw.D, ms["block_scores"]),
                 "rerope_scatter": frac("hbm", 2 * bw.L * bw.Hkv * moved_blocks * bw.block * bw.D * 2,
                                        ms["rerope_scatter"])}
+        line["block_scores"]["pairs_per_s"] = bw.L * bw.Hq * bw.M * bw.n_cand / (ms["block_scores"] / 1e3)
         print(json.dumps(line), flush=True)
         del b
         torch.cuda.empty_cache()
