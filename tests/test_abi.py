@@ -62,3 +62,28 @@ def test_no_oracle_in_product_sources():
             if f.endswith((".py", ".cu", ".h", ".cuh")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text and "orc_" not in text, f
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """A C99 program includes the header with every warning an error, links against the library
+    and calls it (version, and a call rejected on a null context)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_kvsel.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "kvsel.h"\n'
+        "int main(void) {\n"
+        "    if (kvsel_version() != 100) return 1;\n"
+        "    if (kvsel_redirect_slots(NULL, NULL, NULL, 0, 0, NULL, NULL) != KVSEL_ERR_INVALID_ARG) return 2;\n"
+        '    printf("%s\\n", kvsel_last_error_string(NULL));\n'
+        "    return 0;\n}\n")
+    exe = tmp_path / "use_kvsel"
+    libdir = os.path.dirname(lib._name)
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe), "-L", libdir, "-lkvsel", "-Wl,-rpath," + libdir],
+                   check=True, capture_output=True, text=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True)
+    assert out.stdout.strip() == "null context"
