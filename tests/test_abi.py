@@ -64,6 +64,16 @@ def test_no_oracle_in_product_sources():
                 assert "import oracle" not in text and "from oracle" not in text and "orc_" not in text, f
 
 
+def test_oracle_shares_nothing_with_the_product():
+    """The oracle neither imports the product package nor includes its headers or kernels."""
+    odir = os.path.join(ROOT, "oracle")
+    for f in os.listdir(odir):
+        if f.endswith((".py", ".c", ".h")):
+            text = open(os.path.join(odir, f)).read()
+            assert "kv_cache_retention_gb300" not in text, f
+            assert "kvsel.h" not in text and "kvsel_internal" not in text and "csrc" not in text, f
+
+
 def test_header_is_plain_c_and_links(lib, tmp_path):
     """A C99 program includes the header with every warning an error, links against the library
     and calls it (version, and a call rejected on a null context)."""
