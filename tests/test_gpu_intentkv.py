@@ -102,6 +102,21 @@ def test_memory_update_ragged_dims(ctx):
     assert_scores_close(f64(M), ref, what="M_t D=72")
 
 
+@pytest.mark.parametrize("dtype,D,R", [(torch.bfloat16, 1024, 300), (torch.float32, 1024, 77), (torch.float32, 520, 5),
+                                       (torch.bfloat16, 16, 1000)])
+def test_memory_update_wide_and_narrow_rows(ctx, dtype, D, R):
+    """Rows of up to 1024 dims (one thread per 16-byte chunk, one row per pass) and of 16 dims
+    (64 rows per pass)."""
+    g = torch.Generator(device="cuda").manual_seed(D + R)
+    q = torch.randn((2, 3, R, D), generator=g, device="cuda").to(dtype)
+    M = torch.randn((2, 3, D), generator=g, device="cuda")
+    M0 = M.detach().cpu().double().numpy()
+    ctx.memory_update(q, 0.3, M)
+    qh = bits(q) if dtype == torch.bfloat16 else q.cpu().numpy()
+    ref, _ = oracle.memory_update(qh, 0.3, M=M0)
+    assert_scores_close(f64(M), ref, what=f"M_t D={D} R={R}")
+
+
 # ---------------------------------------------------------------------------
 # rule scores
 # ---------------------------------------------------------------------------
