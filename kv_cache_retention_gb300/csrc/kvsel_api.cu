@@ -13,14 +13,17 @@
 
 namespace {
 
-int fail(kvsel_ctx* ctx, int code, const char* fmt, ...) {
-    if (ctx) {
-        va_list ap;
-        va_start(ap, fmt);
-        vsnprintf(ctx->err, sizeof ctx->err, fmt, ap);
-        va_end(ap);
-    }
+int vfail(kvsel_ctx* ctx, int code, const char* fmt, va_list ap) {
+    if (ctx) vsnprintf(ctx->err, sizeof ctx->err, fmt, ap);
     return code;
+}
+
+int fail(kvsel_ctx* ctx, int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    const int rc = vfail(ctx, code, fmt, ap);
+    va_end(ap);
+    return rc;
 }
 
 int cuda_fail(kvsel_ctx* ctx, cudaError_t e, const char* what) {
@@ -57,13 +60,11 @@ int launched(kvsel_ctx* ctx, cudaError_t e, const char* what) {
 int kvsel_enter(kvsel_ctx* ctx) { return enter(ctx); }
 
 int kvsel_fail(kvsel_ctx* ctx, int code, const char* fmt, ...) {
-    if (ctx) {
-        va_list ap;
-        va_start(ap, fmt);
-        vsnprintf(ctx->err, sizeof ctx->err, fmt, ap);
-        va_end(ap);
-    }
-    return code;
+    va_list ap;
+    va_start(ap, fmt);
+    const int rc = vfail(ctx, code, fmt, ap);
+    va_end(ap);
+    return rc;
 }
 
 int kvsel_cuda_fail(kvsel_ctx* ctx, cudaError_t e, const char* what) { return cuda_fail(ctx, e, what); }
