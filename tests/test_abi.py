@@ -97,3 +97,18 @@ def test_header_is_plain_c_and_links(lib, tmp_path):
                    check=True, capture_output=True, text=True)
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True)
     assert out.stdout.strip() == "null context"
+
+
+def test_binding_fails_loudly_without_a_gpu_path():
+    """CPU tensors, unsupported dtypes and a missing device are errors, never a fallback."""
+    import torch
+
+    import kv_cache_retention_gb300 as kv
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        kv._ptr(torch.zeros(3))
+    with pytest.raises(TypeError):
+        kv._code(torch.zeros(3, dtype=torch.float16))
+    assert kv._ptr(None) is None
+    if not torch.cuda.is_available():
+        with pytest.raises(kv.KvselError):
+            kv.Context(0)
