@@ -301,8 +301,10 @@ typedef struct {
 } kvsel_topk_session;
 
 /*
- * kvsel_topk_retain for S sessions.  Sessions of N <= 131072 share one launch,
- * one thread-block cluster each; larger ones take the single-CTA kernel.
+ * kvsel_topk_retain for S sessions.  Sessions of N <= 131072 share one launch:
+ * one CTA each when every one of them has N <= 16384, else one thread-block
+ * cluster each; larger sessions are selected one launch each.  Results are
+ * those of kvsel_topk_retain on each session.
  * n_keep_host: NULL or a host int array [S] receiving each session's |keep|.
  */
 int kvsel_topk_retain_batch(kvsel_ctx* ctx, const kvsel_topk_session* sessions, int S, int* n_keep_host,
