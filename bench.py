@@ -208,7 +208,7 @@ def ours(args, rank, world, local_rank):
     import torch
 
     import kv_cache_retention_gb300 as kv
-    from kv_cache_retention_gb300 import synth
+    import synth
 
     torch.cuda.set_device(local_rank)
     dist = None
@@ -354,10 +354,11 @@ def ours(args, rank, world, local_rank):
 
 
 # DRAM bytes (read + write) per call from an ncu capture of the current kernel code, scaled to the
-# bench workload; an entry is removed whenever its kernel changes.  Source: profiles/*.md.
+# bench workload; an entry is removed whenever its kernel changes.
 PROFILED_TRAFFIC = {
     # block_scores_tc, 4-layer capture of both passes (row 352.5 + 11.4 MB, column 354.0 + 6.6 MB),
-    # x16 for 64 layers; profiles/block_scores_tc_ws1m_L4.md
+    # x16 for 64 layers: ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on
+    # python bench.py --profile-kernel block_scores --profile-layers 4
     "block_scores": 16 * (352.454912 + 11.352832 + 354.045952 + 6.576640) * 1e6,
 }
 
@@ -367,47 +368,156 @@ def _profiled_traffic(kernel):
 
 
 # ---------------------------------------------------------------------------
-# CPU baseline / reference arm: the fp64 oracle on a bounded sample
+# CPU baseline / reference arm: the fp64 oracle, timed on the host cores
 # ---------------------------------------------------------------------------
 
-def oracle_sample(tw, bw, budget_layers=2, block_queries=256):
-    """Time the oracle on a bounded sample of the step; return (sec_per_full_step_estimate, description).
+BLOCK_SLICE_QUERIES = 64  # query tokens per (layer, kv head) in the timed slice of the block step
 
-    Token part: the whole IntentKV step restricted to `budget_layers` layers.
-    Block part: the R_b mass of one (layer, kv head) with `block_queries`
-    query tokens per head, plus Mean-K of one (layer, kv head) of the new tokens.
-    Each part's time is scaled by its share of the full step's work."""
+
+def _oracle_worker(conn, root):
+    """A host process running the unchanged oracle on a fixed slice of the step.
+
+    ("load", tw, bw, token_slices, block_jobs): keep this worker's (layer, kv head)
+    slices of the token step's K pool ([N][D] rows of one kv head) and its block-step
+    jobs (q [1][G][m][D], index [1][1][B][D] bf16 bits).
+    ("rules", M_slices): the sum of the rule-score contributions of its slices, in
+    slice order (fp64 [N]).  ("block",): run its block-step jobs.  ("stop",): exit."""
+    sys.path.insert(0, root)
     import numpy as np
-    import torch
 
     import oracle
-    from kv_cache_retention_gb300 import synth
-
     oracle.build()
-    tws = synth.scaled(tw, L=budget_layers)
-    ti = synth.token_inputs(tws, "cpu")
-    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
-    t0 = time.perf_counter()
-    M, _ = oracle.memory_update(bits(ti["turns"][-1]), tws.lam, first_turn=True)
-    rule = oracle.rule_scores(bits(ti["pool"]).ravel(), M, tws.L, tws.Hq, tws.Hkv, tws.N, tws.D, tws.pi, tws.q_s,
-                              tws.q_e, slot_map=ti["slot_map"].numpy())
-    keep, _ = oracle.topk_retain(rule, tws.pi, tws.q_s, tws.q_e, tws.C)
-    oracle.redirect_slots(ti["slot_map"].numpy(), keep, tws.dead_slot)
-    t_tok = time.perf_counter() - t0
-    bws = synth.scaled(bw, L=1, Hkv=1, Hq=bw.Hq // bw.Hkv, M=block_queries, new_tokens=bw.new_tokens)
-    gen = torch.Generator().manual_seed(bw.seed)
-    q = torch.randn((1, bws.Hq, block_queries, bw.D), generator=gen).to(torch.bfloat16)
-    ix = (torch.randn((1, 1, bw.n_blocks, bw.D), generator=gen) * 0.5).to(torch.bfloat16)
-    raw = torch.randn((1, 1, bw.new_tokens, bw.D), generator=gen).to(torch.bfloat16)
-    t0 = time.perf_counter()
-    oracle.meank_build(bits(raw), bw.block, Bcap=bw.new_tokens // bw.block)
-    oracle.block_mass(bits(q), bits(ix), bw.n_blocks, bw.n_sink, bw.n_recent, 0, 0)
-    t_blk = time.perf_counter() - t0
-    est = t_tok * (tw.L / budget_layers) + t_blk * (bw.L * bw.Hkv) * (bw.M / block_queries)
-    desc = (f"oracle, 1 thread: token step on {budget_layers} of {tw.L} layers ({t_tok:.2f} s) and R_b of 1 of "
-            f"{bw.L * bw.Hkv} (layer, kv head) pairs with {block_queries} of {bw.M} query tokens ({t_blk:.2f} s), "
-            f"scaled by work share to one full step ({est:.1f} s)")
-    return est, desc
+    tw = bw = None
+    slices, jobs, slot_map = [], [], None
+    while True:
+        msg = conn.recv()
+        if msg[0] == "stop":
+            break
+        if msg[0] == "load":
+            _, tw, bw, slot_map, slices, jobs = msg
+            conn.send("ok")
+        elif msg[0] == "rules":
+            G = tw.Hq // tw.Hkv
+            acc = np.zeros(tw.N)
+            for k, Mlg in zip(slices, msg[1]):
+                acc += oracle.rule_scores(k.ravel(), Mlg.reshape(1, G, tw.D), 1, G, 1, tw.N, tw.D, tw.pi, tw.q_s,
+                                          tw.q_e, slot_map=slot_map, layer_stride=tw.N * tw.D, slot_stride=tw.D)
+            conn.send(acc)
+        elif msg[0] == "block":
+            for q, ix in jobs:
+                oracle.block_mass(q, ix, bw.n_blocks, bw.n_sink, bw.n_recent, 0, 0)
+            conn.send("ok")
+    conn.close()
+
+
+class OracleStep:
+    """The oracle's select step on the host cores, run as `procs` processes.
+
+    Token part (IntentKV, the whole step, measured): QueryMemory update of the timed
+    turn, rule scores of every (layer, kv head) (the unchanged oracle on disjoint
+    (layer, kv head) slices, one fixed share per process, partial rule vectors added
+    in a fixed order), top-C*, redirect.
+    Block part (KVMEM R_b, a declared slice): one (layer, kv head) mass row per
+    process with BLOCK_SLICE_QUERIES query tokens and every candidate block; its wall
+    time over its work fraction estimates the whole block part at the same process
+    count (the (layer, kv head) rows are independent).
+    Inputs are drawn on the host with the workloads' shapes (the oracle shares no
+    state with the GPU path); drawing and loading them is outside the timing."""
+
+    def __init__(self, tw, bw, procs=None):
+        import multiprocessing as mp
+
+        import numpy as np
+        import torch
+
+        import oracle
+        import synth
+        oracle.build()
+        self.tw, self.bw = tw, bw
+        self.procs = procs or max(1, min(16, os.cpu_count() or 1))
+        P, G = self.procs, tw.Hq // tw.Hkv
+        ti = synth.token_inputs(tw, "cpu")
+        bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+        pool = bits(ti["pool"])                                   # [L][N][Hkv][D]
+        self.slot_map = ti["slot_map"].numpy()
+        self.q_last = bits(ti["turns"][tw.turns - 1])
+        M = None
+        for t in range(tw.turns - 1):  # the session's earlier turns (state before the timed turn)
+            M, _ = oracle.memory_update(bits(ti["turns"][t]), tw.lam, M=M, first_turn=(t == 0))
+        self.M_prev = M
+        self.pairs = [[(l, g) for i, (l, g) in enumerate((l, g) for l in range(tw.L) for g in range(tw.Hkv))
+                       if i % P == r] for r in range(P)]
+        bstd = (bw.offset_sigma ** 2 + 1.0 / bw.block) ** 0.5
+        mp_ctx = mp.get_context("spawn")
+        self.workers = []
+        for r in range(P):
+            a, b = mp_ctx.Pipe()
+            proc = mp_ctx.Process(target=_oracle_worker, args=(b, ROOT), daemon=True)
+            proc.start()
+            l, g = (r * 37) % bw.L, r % bw.Hkv
+            q = synth.bf16_bits(synth.portable_normal((1, bw.Hq // bw.Hkv, BLOCK_SLICE_QUERIES, bw.D),
+                                                      (bw.seed, synth.PORTABLE_Q, l, g)))
+            ix = synth.bf16_bits(synth.portable_normal((1, 1, bw.n_blocks, bw.D), (bw.seed, synth.PORTABLE_INDEX, l, g),
+                                                       bstd))
+            a.send(("load", tw, bw, self.slot_map, [np.ascontiguousarray(pool[l_, :, g_, :]) for l_, g_ in self.pairs[r]],
+                    [(q, ix)]))
+            self.workers.append((proc, a))
+        del ti, pool
+        for _, a in self.workers:
+            assert a.recv() == "ok"
+        self.G = G
+        self.frac_block = P * BLOCK_SLICE_QUERIES / (bw.L * bw.Hkv * bw.M)
+
+    def close(self):
+        for proc, a in self.workers:
+            try:
+                a.send(("stop",))
+            except Exception:
+                pass
+        for proc, _ in self.workers:
+            proc.join(timeout=30)
+
+    def step(self):
+        """One sample step; returns (token step s, block slice wall s)."""
+        import numpy as np
+
+        import oracle
+        tw, G = self.tw, self.G
+        t0 = time.perf_counter()
+        M, _ = oracle.memory_update(self.q_last, tw.lam, M=self.M_prev)
+        for r, (_, a) in enumerate(self.workers):
+            a.send(("rules", [M[l, g * G:(g + 1) * G] for l, g in self.pairs[r]]))
+        rule = np.zeros(tw.N)
+        for _, a in self.workers:
+            rule += a.recv()
+        keep, _ = oracle.topk_retain(rule, tw.pi, tw.q_s, tw.q_e, tw.C)
+        oracle.redirect_slots(self.slot_map, keep, tw.dead_slot)
+        t1 = time.perf_counter()
+        for _, a in self.workers:
+            a.send(("block",))
+        for _, a in self.workers:
+            assert a.recv() == "ok"
+        t2 = time.perf_counter()
+        return t1 - t0, t2 - t1
+
+    def figures(self, t_tok, t_blk):
+        """The baseline's fields from the measured parts (medians over steps)."""
+        tw, bw = self.tw, self.bw
+        token_rows, block_rows = workload_rows(tw, bw)
+        est = t_tok + t_blk / self.frac_block
+        desc = (f"oracle (fp64 C) on {self.procs} processes: whole token step ({t_tok:.2f} s measured; rule scores "
+                f"over {tw.L * tw.Hkv} (layer, kv head) slices); R_b slice of {self.procs} of {bw.L * bw.Hkv} "
+                f"(layer, kv head) rows x {BLOCK_SLICE_QUERIES} of {bw.M} query tokens ({t_blk:.2f} s measured, "
+                f"work fraction {self.frac_block:.3g}); full step estimated {est:.0f} s")
+        return {"value": (token_rows + block_rows) / est, "unit": "rows/s", "cores": self.procs, "kind": "oracle",
+                "sample": desc, "measured_s": t_tok + t_blk, "extrapolated": True, "est_full_step_s": est,
+                "token_step": {"measured_s": t_tok, "rows": token_rows, "procs": self.procs, "work_fraction": 1.0,
+                               "extrapolated": False},
+                "block_step": {"measured_s": t_blk, "rows": block_rows, "procs": self.procs,
+                               "work_fraction": self.frac_block, "extrapolated": True,
+                               "slice": f"{self.procs} (layer, kv head) rows x {BLOCK_SLICE_QUERIES} query tokens, "
+                                        f"all {bw.n_blocks} blocks"},
+                "nproc": os.cpu_count(), "host": host_cpu()}
 
 
 def host_cpu():
@@ -432,35 +542,47 @@ def host_cpu():
 
 
 def cpu_baseline(args, tw, bw):
-    est, desc = oracle_sample(tw, bw)
-    token_rows, block_rows = workload_rows(tw, bw)
-    return {"value": (token_rows + block_rows) / est, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": desc,
-            "host": host_cpu()}
+    """The oracle on the host cores: one sample step (rank 0, N=1)."""
+    o = OracleStep(tw, bw)
+    try:
+        t_tok, t_blk = o.step()
+        return o.figures(t_tok, t_blk)
+    finally:
+        o.close()
 
 
 def reference(args, rank, world):
+    """The reference arm: the fp64 oracle, each step one sample step of the workload
+    (the whole token step and a slice of the block step, OracleStep).  ms_per_step is
+    the measured time of a sample step; value is the whole step's rows over the
+    estimated whole-step time (fields say which parts are measured and which scaled)."""
     if rank != 0:
         return
-    from kv_cache_retention_gb300 import synth
+    import synth
     tw, bw = synth.TOKEN[TOKEN_WL], synth.BLOCK[BLOCK_WL]
-    for _ in range(args.warmup):
-        oracle_sample(tw, bw, budget_layers=1, block_queries=64)
-    ests, desc = [], ""
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        est, desc = oracle_sample(tw, bw, budget_layers=1, block_queries=64)
-        ests.append(est)
-    wall = time.perf_counter() - t0
-    token_rows, block_rows = workload_rows(tw, bw)
-    sec = sum(ests)
-    value = (token_rows + block_rows) * args.steps / sec
+    o = OracleStep(tw, bw)
+    try:
+        for _ in range(args.warmup):
+            o.step()
+        toks, blks = [], []
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            a, b = o.step()
+            toks.append(a)
+            blks.append(b)
+        wall = time.perf_counter() - t0
+    finally:
+        o.close()
+    cpu = o.figures(statistics.median(toks), statistics.median(blks))
+    value = cpu["value"]
     line = {"impl": "reference", "metric": "KV rows scored/s", "value": value, "unit": "rows/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded; shapes of the pages' workloads)", "config": config_dict(tw, bw, world),
-            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": desc,
-                             "host": host_cpu()},
+            "cpu_baseline": cpu,
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "timing": "ms_per_step: measured wall time of one sample step (whole token step + block slice); "
+                      "value: whole-step rows / (token step measured + block slice wall / its work fraction)",
             "wall_s": wall}
     print(json.dumps(line), flush=True)
 
@@ -570,7 +692,7 @@ def profile_case(args):
     import torch
 
     import kv_cache_retention_gb300 as kv
-    from kv_cache_retention_gb300 import synth
+    import synth
 
     if args.profile_kernel in EXTRA_CASES:
         extra_profile_case(args)
@@ -610,7 +732,7 @@ def all_configs(args):
     import torch
 
     import kv_cache_retention_gb300 as kv
-    from kv_cache_retention_gb300 import synth
+    import synth
 
     torch.cuda.set_device(0)
     ctx = kv.Context(0)
@@ -816,7 +938,7 @@ def block_sweep(args):
     import torch
 
     import kv_cache_retention_gb300 as kv
-    from kv_cache_retention_gb300 import synth
+    import synth
 
     torch.cuda.set_device(0)
     ctx = kv.Context(0)
@@ -867,7 +989,7 @@ def fp8_index(args):
     import torch
 
     import kv_cache_retention_gb300 as kv
-    from kv_cache_retention_gb300 import synth
+    import synth
 
     torch.cuda.set_device(0)
     ctx = kv.Context(0)

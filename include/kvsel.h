@@ -133,18 +133,18 @@ int kvsel_rule_scores(kvsel_ctx* ctx, const void* k_pool, int k_dtype, const int
  * kvsel_rule_scores without any device allocation.  The pages have no
  * counterpart: this is a deployment variant for callers that cannot let a
  * library allocate device memory, such as serving engines that give nearly all
- * of the GPU to their own KV page pool and allocator, code recorded into a CUDA
- * graph (no allocation inside stream capture), and latency-critical loops that
- * cannot take cudaFree's implicit device synchronisation.
- * Same arguments, rules and result as kvsel_rule_scores; the scratch it needs
- * (4*L*Hq*N bytes plus a little) comes from a fixed 64 MiB array inside the
- * library, which every GPU that loads the library holds until the process
- * exits.  A size that needs more returns KVSEL_ERR_UNSUPPORTED without
- * launching.  The first call on a device looks up the array's device address
- * (a one-time set-up with that device current); make that first call before
- * any stream capture.  All calls share the one array and it keeps the last
- * call's contents (nothing in it needs clearing between calls): calls that
- * overlap on the GPU, on any stream or context of the process, race.
+ * of the GPU to their own KV page pool and allocator, and latency-critical
+ * loops that cannot take cudaFree's implicit device synchronisation.
+ * Same arguments, rules and result as kvsel_rule_scores (the same kernels, so
+ * bit-identical scores); the scratch it needs (4*L*Hq*N bytes plus a little)
+ * comes from a fixed 64 MiB array inside the library, which every GPU that
+ * loads the library holds until the process exits.  A size that needs more
+ * returns KVSEL_ERR_UNSUPPORTED without launching.  The first call with a
+ * context looks up the array's device address on the context's device (a
+ * one-time set-up with that device current, kept in the context); make that
+ * first call before any stream capture.  All calls share the one array and it
+ * keeps the last call's contents (nothing in it needs clearing between calls):
+ * calls that overlap on the GPU, on any stream or context of the process, race.
  */
 int kvsel_rule_scores_noalloc(kvsel_ctx* ctx, const void* k_pool, int k_dtype, const int32_t* slot_map,
                               int n_slots, int L, int Hq, int Hkv, int N, int D, int64_t layer_stride,

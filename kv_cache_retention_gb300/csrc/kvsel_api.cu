@@ -69,6 +69,30 @@ int kvsel_fail(kvsel_ctx* ctx, int code, const char* fmt, ...) {
 
 int kvsel_cuda_fail(kvsel_ctx* ctx, cudaError_t e, const char* what) { return cuda_fail(ctx, e, what); }
 
+int kvsel_check_rule_scores_args(kvsel_ctx* ctx, const char* who, const void* k_pool, int k_dtype,
+                                 const int32_t* slot_map, int n_slots, int L, int Hq, int Hkv, int N, int D,
+                                 int64_t layer_stride, int64_t slot_stride, const float* M, int pi, int q_s, int q_e,
+                                 const float* rule) {
+    if (!k_pool || !M || !rule) return fail(ctx, KVSEL_ERR_INVALID_ARG, "%s: null pointer", who);
+    if (k_dtype != KVSEL_F32 && k_dtype != KVSEL_BF16) return fail(ctx, KVSEL_ERR_INVALID_ARG, "%s: bad dtype", who);
+    if (L <= 0 || Hq <= 0 || Hkv <= 0 || N < 0 || n_slots < 0) return fail(ctx, KVSEL_ERR_SHAPE, "%s: bad sizes", who);
+    if (Hq % Hkv) return fail(ctx, KVSEL_ERR_SHAPE, "%s: Hq=%d not a multiple of Hkv=%d", who, Hq, Hkv);
+    if (Hq / Hkv > 8) return fail(ctx, KVSEL_ERR_UNSUPPORTED, "%s: group size Hq/Hkv=%d > 8", who, Hq / Hkv);
+    if (!pow2_head_dim(D)) return fail(ctx, KVSEL_ERR_UNSUPPORTED, "%s: D=%d unsupported", who, D);
+    if ((int64_t)Hkv * D > 4096) return fail(ctx, KVSEL_ERR_UNSUPPORTED, "%s: Hkv*D > 4096", who);
+    if (pi < 0 || pi > N || q_s < 0 || q_s > q_e || q_e > N)
+        return fail(ctx, KVSEL_ERR_SHAPE, "%s: forced ranges outside [0,N]", who);
+    if (!slot_map && n_slots < N) return fail(ctx, KVSEL_ERR_SHAPE, "%s: identity slot map needs n_slots >= N", who);
+    if (slot_stride < (int64_t)Hkv * D || layer_stride < 0)
+        return fail(ctx, KVSEL_ERR_SHAPE, "%s: slot_stride < Hkv*D", who);
+    if (L > 1 && layer_stride < (int64_t)n_slots * slot_stride)
+        return fail(ctx, KVSEL_ERR_SHAPE, "%s: layers overlap", who);
+    const int64_t es = k_dtype == KVSEL_BF16 ? 2 : 4;
+    if (!aligned16(k_pool) || (layer_stride * es) % 16 || (slot_stride * es) % 16 || !aligned16(M) || !aligned16(rule))
+        return fail(ctx, KVSEL_ERR_ALIGN, "%s: pool, strides, M and rule must be 16-byte aligned", who);
+    return KVSEL_OK;
+}
+
 void* kvsel_workspace(kvsel_ctx* ctx, size_t bytes) {
     if (bytes == 0) bytes = 256;
     if (bytes <= ctx->ws_bytes) return ctx->ws;
@@ -217,20 +241,9 @@ int kvsel_rule_scores(kvsel_ctx* ctx, const void* k_pool, int k_dtype, const int
                       const float* M, int pi, int q_s, int q_e, float* rule, void* stream) {
     int rc = enter(ctx);
     if (rc) return rc;
-    if (!k_pool || !M || !rule) return fail(ctx, KVSEL_ERR_INVALID_ARG, "rule_scores: null pointer");
-    if (k_dtype != KVSEL_F32 && k_dtype != KVSEL_BF16) return fail(ctx, KVSEL_ERR_INVALID_ARG, "rule_scores: bad dtype");
-    if (L <= 0 || Hq <= 0 || Hkv <= 0 || N < 0 || n_slots < 0) return fail(ctx, KVSEL_ERR_SHAPE, "rule_scores: bad sizes");
-    if (Hq % Hkv) return fail(ctx, KVSEL_ERR_SHAPE, "rule_scores: Hq=%d not a multiple of Hkv=%d", Hq, Hkv);
-    if (Hq / Hkv > 8) return fail(ctx, KVSEL_ERR_UNSUPPORTED, "rule_scores: group size Hq/Hkv=%d > 8", Hq / Hkv);
-    if (!pow2_head_dim(D)) return fail(ctx, KVSEL_ERR_UNSUPPORTED, "rule_scores: D=%d unsupported", D);
-    if ((int64_t)Hkv * D > 4096) return fail(ctx, KVSEL_ERR_UNSUPPORTED, "rule_scores: Hkv*D > 4096");
-    if (pi < 0 || pi > N || q_s < 0 || q_s > q_e || q_e > N) return fail(ctx, KVSEL_ERR_SHAPE, "rule_scores: forced ranges outside [0,N]");
-    if (!slot_map && n_slots < N) return fail(ctx, KVSEL_ERR_SHAPE, "rule_scores: identity slot map needs n_slots >= N");
-    if (slot_stride < (int64_t)Hkv * D || layer_stride < 0) return fail(ctx, KVSEL_ERR_SHAPE, "rule_scores: slot_stride < Hkv*D");
-    if (L > 1 && layer_stride < (int64_t)n_slots * slot_stride) return fail(ctx, KVSEL_ERR_SHAPE, "rule_scores: layers overlap");
-    size_t es = k_dtype == KVSEL_BF16 ? 2 : 4;
-    if (!aligned16(k_pool) || (layer_stride * es) % 16 || (slot_stride * es) % 16 || !aligned16(M) || !aligned16(rule))
-        return fail(ctx, KVSEL_ERR_ALIGN, "rule_scores: pool, strides, M and rule must be 16-byte aligned");
+    rc = kvsel_check_rule_scores_args(ctx, "rule_scores", k_pool, k_dtype, slot_map, n_slots, L, Hq, Hkv, N, D,
+                                      layer_stride, slot_stride, M, pi, q_s, q_e, rule);
+    if (rc) return rc;
     if (N == 0) return KVSEL_OK;
     void* ws = kvsel_workspace(ctx, rule_scores_workspace(ctx, L, Hq, N));
     if (!ws) return fail(ctx, KVSEL_ERR_CUDA, "rule_scores: workspace allocation failed");

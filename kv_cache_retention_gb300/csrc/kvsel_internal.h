@@ -37,6 +37,9 @@ struct kvsel_ctx {
         cudaStream_t copy_stream = nullptr;
         size_t capacity = 0;
     } stager;
+    // Device address of the fixed scratch array of kvsel_rule_scores_noalloc on
+    // this context's device, looked up by that call's first use on the context.
+    void* noalloc_scratch = nullptr;
     char err[512] = {0};
 };
 
@@ -62,6 +65,12 @@ enum kvsel_devcheck : unsigned {
 int kvsel_enter(kvsel_ctx* ctx);
 int kvsel_fail(kvsel_ctx* ctx, int code, const char* fmt, ...);
 int kvsel_cuda_fail(kvsel_ctx* ctx, cudaError_t e, const char* what);
+// The argument rules of kvsel_rule_scores (shared by its no-allocation variant);
+// KVSEL_OK or the failure code, with `who` leading the error string.
+int kvsel_check_rule_scores_args(kvsel_ctx* ctx, const char* who, const void* k_pool, int k_dtype,
+                                 const int32_t* slot_map, int n_slots, int L, int Hq, int Hkv, int N, int D,
+                                 int64_t layer_stride, int64_t slot_stride, const float* M, int pi, int q_s, int q_e,
+                                 const float* rule);
 // Frees the staging buffers, events and copy stream of kvsel_stage_restore.
 void kvsel_stager_release(kvsel_ctx* ctx);
 

@@ -239,3 +239,72 @@ def scatter_plan_full(w: BlockWorkload, page_perm):
     """Destination of working-set entry r (ascending ids): page page_perm[r], position r*block."""
     r = torch.arange(w.n_sel, device=page_perm.device, dtype=torch.int32)
     return page_perm[r.long()].to(torch.int32), (r * w.block).to(torch.int32)
+
+
+# ---------------------------------------------------------------------------
+# platform-independent draws (inputs of the stored full-size oracle values)
+# ---------------------------------------------------------------------------
+# The stored fp64 block scores of the two block workloads are computed once on
+# one host and compared on another (an x86 host writes them, the Arm host of the
+# GPU reads them).  torch's CPU normal sampler is not the same on both: its
+# vectorised Box-Muller path calls different transcendental implementations per
+# instruction set.  numpy's PCG64 stream, seeded through SeedSequence, is
+# defined bit for bit, and its float32 ziggurat normal sampler uses table
+# lookups and IEEE arithmetic except in its rare tail and wedge branches, so a
+# seed gives the same float32 draws on both hosts.  Every draw is keyed by
+# (seed, tensor kind, layer) so that layers can be drawn in any order and in
+# parallel.  A SHA-256 over the bf16 bytes, layer by layer, is recorded with the
+# stored values and checked wherever they are used.
+
+PORTABLE_RAW_OFFSET, PORTABLE_RAW_NOISE, PORTABLE_Q, PORTABLE_INDEX = 1, 2, 3, 4
+
+
+def portable_normal(shape, key, std=1.0):
+    """float32 N(0, std^2) draws from numpy's PCG64 seeded with the integer tuple `key`."""
+    import numpy as np
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([int(k) for k in key])))
+    x = g.standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        x *= np.float32(std)
+    return x
+
+
+def bf16_bits(x):
+    """float32 numpy array -> bf16 bit patterns (uint16), round to nearest even (torch's cast)."""
+    import numpy as np
+    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def portable_block_layer(w: BlockWorkload, l: int):
+    """Layer l of a block workload's inputs, as bf16 bit patterns (numpy uint16).
+
+    Returns {"q": [Hq][M][D], and "raw": [Hkv][n_blocks*block][D] (full build: per
+    (kv head, block, channel) offset ~ N(0, sigma^2) shared by the block's tokens,
+    plus N(0,1) per token) or "index": [Hkv][n_blocks][D] (incremental workspace:
+    every indexed block drawn directly as N(0, sigma^2 + 1/block), the spread of
+    an offset plus the mean of `block` unit normals)}."""
+    out = {"q": bf16_bits(portable_normal((w.Hq, w.M, w.D), (w.seed, PORTABLE_Q, l)))}
+    if w.incremental:
+        std = (w.offset_sigma ** 2 + 1.0 / w.block) ** 0.5
+        out["index"] = bf16_bits(portable_normal((w.Hkv, w.n_blocks, w.D), (w.seed, PORTABLE_INDEX, l), std))
+    else:
+        off = portable_normal((w.Hkv, w.n_blocks, 1, w.D), (w.seed, PORTABLE_RAW_OFFSET, l), w.offset_sigma)
+        noise = portable_normal((w.Hkv, w.n_blocks, w.block, w.D), (w.seed, PORTABLE_RAW_NOISE, l))
+        noise += off
+        out["raw"] = bf16_bits(noise.reshape(w.Hkv, w.n_blocks * w.block, w.D))
+    return out
+
+
+def portable_layer_digest(layer):
+    """SHA-256 (hex) of one layer's bf16 bytes: q, then raw or index."""
+    import hashlib
+    h = hashlib.sha256()
+    h.update(layer["q"].tobytes())
+    h.update((layer["raw"] if "raw" in layer else layer["index"]).tobytes())
+    return h.hexdigest()
+
+
+def portable_digest(layer_digests):
+    """SHA-256 (hex) over the per-layer digests in layer order."""
+    import hashlib
+    return hashlib.sha256("".join(layer_digests).encode()).hexdigest()

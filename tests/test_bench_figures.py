@@ -2,7 +2,7 @@
 roofline numerators), launches per step and the profiled traffic, worked out by hand for the
 8B-shaped token step and the 1M-workspace block step."""
 import bench
-from kv_cache_retention_gb300 import synth
+import synth
 
 TW, BW = synth.TOKEN[bench.TOKEN_WL], synth.BLOCK[bench.BLOCK_WL]
 

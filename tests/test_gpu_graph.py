@@ -5,7 +5,7 @@ captured in one CUDA graph and replayed.  The replay must give the eager results
 import pytest
 import torch
 
-from kv_cache_retention_gb300 import synth
+import synth
 
 pytestmark = pytest.mark.gpu
 

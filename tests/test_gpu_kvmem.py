@@ -10,7 +10,7 @@ from helpers import assert_keep_sets_match, assert_scores_close, bf16_ulp, bits,
 pytestmark = pytest.mark.gpu
 
 import kv_cache_retention_gb300 as kv  # noqa: E402
-from kv_cache_retention_gb300 import synth  # noqa: E402
+import synth  # noqa: E402
 
 
 @pytest.fixture(scope="module")

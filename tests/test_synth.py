@@ -5,7 +5,7 @@ import dataclasses
 
 import torch
 
-from kv_cache_retention_gb300 import synth
+import synth
 
 
 def test_token_workload_counts():
