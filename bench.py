@@ -588,7 +588,7 @@ def reference(args, rank, world):
 
 
 EXTRA_CASES = ("restore_blocks", "rerope_shift", "workset_diff", "span_keep", "rule_scores_batch", "index_to_fp8",
-               "index_from_fp8")
+               "index_from_fp8", "topk_small")
 
 
 def extra_profile_case(args):
@@ -596,7 +596,8 @@ def extra_profile_case(args):
     restore_blocks / rerope_shift: 2048 blocks of the 1M-workspace dims (L64 Hkv8 D128, 32-token
     pages); workset_diff: two 2180-block working sets sharing two thirds; span_keep: N=92160 with
     100 of 400 cursors deleted; rule_scores_batch: 36 sessions of 1024-8192 tokens at the 8B shape;
-    index_to_fp8 / index_from_fp8: the 1M-workspace index (32768 blocks, Hkv8 D128) per layer."""
+    index_to_fp8 / index_from_fp8: the 1M-workspace index (32768 blocks, Hkv8 D128) per layer;
+    topk_small: top-C* of a 16384-token session (C=4096, the one-CTA path)."""
     import numpy as np
     import torch
 
@@ -642,6 +643,13 @@ def extra_profile_case(args):
         else:
             fn = lambda: ctx.index_from_fp8(codes, exps, out)  # noqa: E731
         moved = L * Hkv * nb * (3 * D + 1)
+    elif name == "topk_small":
+        N = 16384
+        score = torch.rand(N, device="cuda")
+        keep = torch.empty(N, dtype=torch.uint8, device="cuda")
+        keep_idx = torch.empty(N, dtype=torch.int32, device="cuda")
+        fn = lambda: ctx.topk_retain(score, 256, N - 512, N, 4096, keep=keep, keep_idx=keep_idx)  # noqa: E731
+        moved = 5 * N
     elif name == "span_keep":
         N = 92160
         start = torch.as_tensor(rng.integers(0, N, 400).astype(np.int32), device="cuda")
@@ -1144,7 +1152,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-kernel", default=None, help="run only this call on a cut-down case (for ncu)")
+    ap.add_argument("--profile-kernel", default=None,
+                    help="run only this call (or these, comma-separated) on a cut-down case (for ncu)")
     ap.add_argument("--profile-layers", type=int, default=4)
     ap.add_argument("--all-configs", action="store_true", help="time the select step of every workload, one line each")
     ap.add_argument("--restore-pipeline", action="store_true", help="throughput of the staged host -> device restore")
@@ -1168,7 +1177,8 @@ def main():
         restore_pipeline(args)
         return
     if args.profile_kernel:
-        profile_case(args)
+        for name in args.profile_kernel.split(","):  # several calls in turn, each on its own case
+            profile_case(argparse.Namespace(**{**vars(args), "profile_kernel": name}))
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus if "RANK" in os.environ else 1)))

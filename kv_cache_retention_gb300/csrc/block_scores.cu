@@ -116,12 +116,15 @@ struct TcArgs {
     float2* part;      // row pass: [L*Hkv][rows_pad][kSlices] (ref, sum) of each column slice
     float* mass;       // [L*Hkv][n_blocks]
     unsigned* err;
+    uint64_t wait_ns;  // give-up limit of a bounded wait
+    int stuck;         // test hook: the row pass's first MMA issuer waits on a barrier nothing completes
 };
 
 template <int MODE>
 struct __align__(8) SmemTail {
     uint64_t full_f[2], empty_f[2], go[kMaxStages], empty_s[kMaxStages], acc_full[kNAcc];
     uint64_t mma_done;
+    uint64_t never;    // no thread arrives on it (the give-up test hook waits here)
     uint32_t tmem_base;
     int abort_flag;
     float red[MODE == 1 ? kSlices * 4 * kSliceCols : 1];  // column pass: [slice][lane quarter][column] sums
@@ -169,16 +172,17 @@ __device__ __forceinline__ uint64_t gtimer() {
     return t;
 }
 
-// Bounded wait for the phase of parity `parity`.  Returns false if this or
-// another role gave up (the CTA is then draining).
-__device__ __noinline__ bool wait_phase(uint64_t* b, uint32_t parity, volatile int* abort_flag, unsigned* err) {
+// Bounded wait for the phase of parity `parity`, giving up after limit_ns.
+// Returns false if this or another role gave up (the CTA is then draining).
+__device__ __noinline__ bool wait_phase(uint64_t* b, uint32_t parity, volatile int* abort_flag, unsigned* err,
+                                       uint64_t limit_ns) {
     if (mbar_test(b, parity)) return true;
     const uint64_t t0 = gtimer();
     for (uint32_t i = 1;; ++i) {
         if (mbar_test(b, parity)) return true;
         if ((i & 63) == 0) {
             if (*abort_flag) return false;
-            if (gtimer() - t0 > kWaitNs) {
+            if (gtimer() - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicOr(err, (unsigned)KVSEL_DEV_TIMEOUT);
                 return false;
@@ -362,6 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kNAcc; ++i) mbar_init(&t.acc_full[i], 1);
         mbar_init(&t.mma_done, 2);
+        mbar_init(&t.never, 1);
         t.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapF)) : "memory");
@@ -387,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int lg = u / a.units_per_lg, o = u % a.units_per_lg;
                 const int fs = f_it % T::kNF;
                 const int yf = MODE == 0 ? lg * a.rows_g + o * T::kFRows : lg * a.Bcap + a.c0 + o * T::kFRows;
-                if (!(ok = wait_phase(&t.empty_f[fs], ((f_it / T::kNF) & 1) ^ 1, abort_flag, a.err))) break;
+                if (!(ok = wait_phase(&t.empty_f[fs], ((f_it / T::kNF) & 1) ^ 1, abort_flag, a.err, a.wait_ns))) break;
                 mbar_expect_tx(&t.full_f[fs], T::kFBytes);
                 tma_load_2d(&mapF, &t.full_f[fs], sF + fs * T::kFBytes, 0, yf);
                 tma_load_2d(&mapF, &t.full_f[fs], sF + fs * T::kFBytes + T::kFBytes / 2, 64, yf);
@@ -395,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < a.n_it; ++i) {
                     const int st = s_it % T::kNS;
                     const int ys = MODE == 0 ? lg * a.Bcap + a.c0 + i * T::kSRows : lg * a.rows_g + i * T::kSRows;
-                    if (!(ok = wait_phase(&t.empty_s[st], ((s_it / T::kNS) & 1) ^ 1, abort_flag, a.err))) break;
+                    if (!(ok = wait_phase(&t.empty_s[st], ((s_it / T::kNS) & 1) ^ 1, abort_flag, a.err, a.wait_ns))) break;
                     mbar_expect_tx(&t.go[st], T::kSBytes);
                     tma_load_2d(&mapS, &t.go[st], sS + st * T::kSBytes, 0, ys);
                     tma_load_2d(&mapS, &t.go[st], sS + st * T::kSBytes + T::kSBytes / 2, 64, ys);
@@ -418,9 +423,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t me = warp == 1 ? 0u : 1u;
             uint32_t f_it = 0, s_it = 0, acc_it = 0;
             bool ok = true;
+            // test hook: a wait that can only give up, taken while the producer's
+            // copies and the other issuer's MMAs are in flight
+            if (MODE == 0 && a.stuck && me == 0) ok = wait_phase(&t.never, 0, abort_flag, a.err, a.wait_ns);
             for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
                 const int fs = f_it % T::kNF;
-                if (!(ok = wait_phase(&t.full_f[fs], (f_it / T::kNF) & 1, abort_flag, a.err))) break;
+                if (!(ok = wait_phase(&t.full_f[fs], (f_it / T::kNF) & 1, abort_flag, a.err, a.wait_ns))) break;
                 tc_fence_after();
                 const uint32_t f_base = saddr(sF + fs * T::kFBytes);
                 for (int i = 0; i < a.n_it; ++i) {
@@ -433,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     // one wait per tile: the stage's operand has landed and the epilogue has
                     // read the accumulator this tile overwrites
-                    if (!(ok = wait_phase(&t.go[st], (s_it / T::kNS) & 1, abort_flag, a.err))) break;
+                    if (!(ok = wait_phase(&t.go[st], (s_it / T::kNS) & 1, abort_flag, a.err, a.wait_ns))) break;
                     tc_fence_after();
                     const uint32_t s_base = saddr(sS + st * T::kSBytes);
                     // A = the 128-row operand, B = the 256-row one
@@ -495,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // math on whatever the accumulator holds, and the epilogue warps agree on
                 // giving up at the end of the unit.  No per-tile vote or branch: in the
                 // column pass that alone cost a tenth of the tensor pipe's time.
-                if (ok && !ready) ok = wait_phase(&t.acc_full[k], (acc_it / kNAcc) & 1, abort_flag, a.err);
+                if (ok && !ready) ok = wait_phase(&t.acc_full[k], (acc_it / kNAcc) & 1, abort_flag, a.err, a.wait_ns);
                 tc_fence_after();
                 const uint32_t taddr =
                     tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(k * kAccCols + slice * kSliceCols);
@@ -690,7 +698,7 @@ size_t block_scores_workspace(int L, int Hq, int Hkv, int M, int n_blocks) {
 
 cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index, int L, int Hq, int Hkv, int M, int D,
                                 int n_blocks, int Bcap, int n_sink, int n_recent, float* R, float* R_partial, void* ws,
-                                cudaStream_t s) {
+                                cudaStream_t s, uint64_t wait_ns, int stuck) {
     (void)D;
     const int G = Hq / Hkv;
     const int rows_g = G * M;
@@ -728,6 +736,8 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
         a.part = part;
         a.mass = mass;
         a.err = ctx->dev_err;
+        a.wait_ns = wait_ns;
+        a.stuck = stuck;
         // row pass: a unit per 128 query rows, the candidate blocks streamed 256 at a time
         a.units_per_lg = (rows_g + BM - 1) / BM;
         a.n_units = LH * a.units_per_lg;
@@ -741,6 +751,8 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
         a.n_units = LH * a.units_per_lg;
         a.n_it = (rows_g + BM - 1) / BM;
         grid = a.n_units < ctx->num_sms ? a.n_units : ctx->num_sms;
+        a.stuck = 0;  // the test hook and its wait limit apply to the row pass only
+        a.wait_ns = KVSEL_BLOCK_WAIT_NS;
         block_scores_tc<1><<<grid, kThreads, smem_bytes<1>(), s>>>(i256, q128, a);
     }
     bs_finalize<<<(n_blocks + 255) / 256, 256, 0, s>>>(mass, mass, R, LH, n_blocks, c0, c1,

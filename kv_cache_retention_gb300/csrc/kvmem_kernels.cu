@@ -8,6 +8,13 @@
 // angle p * theta_i is rebuilt by the angle-addition formula from two tables
 // of cos/sin computed in fp64 and stored in fp32, so that large positions keep
 // ~1e-7 absolute accuracy (a plain fp32 product p * theta_i would not).
+//
+// Turning a pair (a, b) in fp32 this way leaves an absolute error below
+// 2^-20.5 * rho, rho = |(a, b)|.  That is under half a bf16 ulp of an output r
+// as long as |r| >= 2^-11.5 * rho.  Outputs that nearly cancel (|r| below
+// 2^-11 * max(|a|, |b|), about one pair in 1700) are turned again in fp64 from fp64
+// copies of the same tables and rounded once to bf16, so every output lands
+// within one bf16 ulp of the exactly rotated value rounded to bf16.
 #include <cuda_bf16.h>
 
 #include "kvsel_internal.h"
@@ -16,7 +23,8 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-__global__ void rope_tables_kernel(float2* __restrict__ lo, float2* __restrict__ hi, int D, double base) {
+__global__ void rope_tables_kernel(float2* __restrict__ lo, float2* __restrict__ hi, double2* __restrict__ lo64,
+                                   double2* __restrict__ hi64, int D, double base) {
     const int half = D / 2;
     const int64_t total = (int64_t)(KVSEL_ROPE_LO + KVSEL_ROPE_HI) * half;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
@@ -28,10 +36,12 @@ __global__ void rope_tables_kernel(float2* __restrict__ lo, float2* __restrict__
         if (row < KVSEL_ROPE_LO) {
             sincos((double)row * theta, &s, &c);
             lo[row * half + i] = make_float2((float)c, (float)s);
+            lo64[row * half + i] = make_double2(c, s);
         } else {
             const int64_t r = row - KVSEL_ROPE_LO;
             sincos((double)(r * KVSEL_ROPE_LO) * theta, &s, &c);
             hi[r * half + i] = make_float2((float)c, (float)s);
+            hi64[r * half + i] = make_double2(c, s);
         }
     }
 }
@@ -42,6 +52,118 @@ __device__ __forceinline__ float2 rope_cs(const float2* __restrict__ tlo, const 
     const float2 a = __ldg(thi + (int64_t)(p >> KVSEL_ROPE_LO_BITS) * half + i);
     const float2 b = __ldg(tlo + (int64_t)(p & (KVSEL_ROPE_LO - 1)) * half + i);
     return make_float2(fmaf(a.x, b.x, -a.y * b.y), fmaf(a.y, b.x, a.x * b.y));
+}
+
+// The same in fp64, from the fp64 tables.
+__device__ __forceinline__ double2 rope_cs64(const double2* __restrict__ tlo, const double2* __restrict__ thi,
+                                             int half, int p, int i) {
+    const double2 a = __ldg(thi + (int64_t)(p >> KVSEL_ROPE_LO_BITS) * half + i);
+    const double2 b = __ldg(tlo + (int64_t)(p & (KVSEL_ROPE_LO - 1)) * half + i);
+    return make_double2(fma(a.x, b.x, -a.y * b.y), fma(a.y, b.x, a.x * b.y));
+}
+
+// fp64 turn of one rotation pair, elements ia and ib of a bf16 row read again from
+// memory (the row is not overwritten before this runs), at position p and
+// frequency f (sine negated when neg); each output rounded once to bf16 and
+// returned as the exactly representable fp32 value.  Out of line: it runs for
+// about one pair in 1700, and an inlined copy would be predicated into every pass.
+__device__ __noinline__ float2 turn_pair_fp64(const __nv_bfloat16* __restrict__ row, int ia, int ib,
+                                              const double2* __restrict__ tlo64, const double2* __restrict__ thi64,
+                                              int half, int p, int f, int neg) {
+    const double a = __bfloat162float(row[ia]), b = __bfloat162float(row[ib]);
+    double2 c = rope_cs64(tlo64, thi64, half, p, f);
+    if (neg) c.y = -c.y;
+    return make_float2(__bfloat162float(__double2bfloat16(fma(a, c.x, -b * c.y))),
+                       __bfloat162float(__double2bfloat16(fma(b, c.x, a * c.y))));
+}
+
+// (cos, sin) tables in shared memory, one row of D/2 frequencies per position.
+// Frequencies f of a row are grouped by eight (the ones a NeoX chunk pair uses):
+// group g holds four float4 (c_f, c_f+1, s_f, s_f+1) for f = 8g, 8g+2, 8g+4, 8g+6
+// and one float4 of padding, so that the eight groups a warp reads at once fall
+// in different shared-memory banks, and the packed fp32x2 turn below finds its
+// cosines and sines in register pairs.
+constexpr int kQuadsPerGroup = 5;
+__device__ __forceinline__ void cs_put(float4* row, int f, float c, float s) {
+    float* q = reinterpret_cast<float*>(row + (f >> 3) * kQuadsPerGroup + ((f & 7) >> 1));
+    q[f & 1] = c;
+    q[2 + (f & 1)] = s;
+}
+__device__ __forceinline__ float2 cs_get(const float4* row, int f) {
+    const float* q = reinterpret_cast<const float*>(row + (f >> 3) * kQuadsPerGroup + ((f & 7) >> 1));
+    return make_float2(q[f & 1], q[2 + (f & 1)]);
+}
+
+// Records in `near` (bit k) whether pair k's fp32 turn (ra, rb) of (a, b) has an
+// output below 2^-11 of its larger input.
+__device__ __forceinline__ void mark_near(unsigned& near, int k, float a, float b, float ra, float rb) {
+    near |= (fminf(fabsf(ra), fabsf(rb)) < fmaxf(fabsf(a), fabsf(b)) * 0x1p-11f ? 1u : 0u) << k;
+}
+
+// Turns again in fp64 the pairs marked in `near`, reading their inputs from `row`.
+template <bool NEOX>
+__device__ __forceinline__ void fix_near(unsigned near, float (&xa)[8], float (&xb)[8], int f0, int fa, int fb,
+                                         const __nv_bfloat16* __restrict__ row, int ca, int cb,
+                                         const double2* __restrict__ tlo64, const double2* __restrict__ thi64,
+                                         int half, int p, bool neg) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        if (near & (1u << k)) {
+            float& a = NEOX ? xa[k] : (k < 4 ? xa[2 * k] : xb[2 * (k - 4)]);
+            float& b = NEOX ? xb[k] : (k < 4 ? xa[2 * k + 1] : xb[2 * (k - 4) + 1]);
+            const int ia = NEOX ? 8 * ca + k : (k < 4 ? 8 * ca + 2 * k : 8 * cb + 2 * (k - 4));
+            const int ib = NEOX ? 8 * cb + k : ia + 1;
+            const int f = NEOX ? f0 + k : (k < 4 ? fa + k : fb + k - 4);
+            const float2 r = turn_pair_fp64(row, ia, ib, tlo64, thi64, half, p, f, neg ? 1 : 0);
+            a = r.x;
+            b = r.y;
+        }
+    }
+}
+
+// Turns the 8 rotation pairs held in two unpacked 16-byte chunks (chunks ca and
+// cb of `row`) with the (cos, sin) table row `tq` of their position.  NeoX: pair
+// k is (xa[k], xb[k]) at frequency f0 + k (f0 a multiple of 8), turned two pairs
+// at a time in packed fp32x2; interleaved: pairs (xa[2k], xa[2k+1]) at fa + k and
+// (xb[2k], xb[2k+1]) at fb + k.  A pair with an output below 2^-11 of its larger
+// input is turned again in fp64.
+template <bool NEOX>
+__device__ __forceinline__ void turn_chunks(float (&xa)[8], float (&xb)[8], const float4* __restrict__ tq, int f0,
+                                            int fa, int fb, const __nv_bfloat16* __restrict__ row, int ca, int cb,
+                                            const double2* __restrict__ tlo64, const double2* __restrict__ thi64,
+                                            int half, int p, bool neg) {
+    unsigned near = 0;
+    if (NEOX) {
+        const float4* grp = tq + (f0 >> 3) * kQuadsPerGroup;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 q = grp[j];
+            const float2 c2 = make_float2(q.x, q.y), s2 = make_float2(q.z, q.w);
+            const float2 a2 = make_float2(xa[2 * j], xa[2 * j + 1]), b2 = make_float2(xb[2 * j], xb[2 * j + 1]);
+            const float2 ra2 = __ffma2_rn(a2, c2, __fmul2_rn(b2, make_float2(-s2.x, -s2.y)));
+            const float2 rb2 = __ffma2_rn(b2, c2, __fmul2_rn(a2, s2));
+            mark_near(near, 2 * j, a2.x, b2.x, ra2.x, rb2.x);
+            mark_near(near, 2 * j + 1, a2.y, b2.y, ra2.y, rb2.y);
+            xa[2 * j] = ra2.x;
+            xa[2 * j + 1] = ra2.y;
+            xb[2 * j] = rb2.x;
+            xb[2 * j + 1] = rb2.y;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            float& a = k < 4 ? xa[2 * k] : xb[2 * (k - 4)];
+            float& b = k < 4 ? xa[2 * k + 1] : xb[2 * (k - 4) + 1];
+            const float2 c = cs_get(tq, k < 4 ? fa + k : fb + k - 4);
+            const float ra = fmaf(a, c.x, -b * c.y);
+            const float rb = fmaf(b, c.x, a * c.y);
+            mark_near(near, k, a, b, ra, rb);
+            a = ra;
+            b = rb;
+        }
+    }
+    if (__any_sync(__activemask(), near != 0))
+        fix_near<NEOX>(near, xa, xb, f0, fa, fb, row, ca, cb, tlo64, thi64, half, p, neg);
 }
 
 __device__ __forceinline__ void unpack8(uint4 raw, float (&x)[8]) {
@@ -164,22 +286,26 @@ __global__ void __launch_bounds__(256) meank_kernel(const __nv_bfloat16* __restr
 // pairs -- so no data crosses lanes.  Rows r = t*Hkv + g are contiguous in the
 // destination page; each source row is contiguous too.
 constexpr int kLayerGroup = 8;
+#ifndef KVSEL_REROPE_MINB
+#define KVSEL_REROPE_MINB 4  // resident CTAs per SM the register budget allows (64 registers)
+#endif
 
 // Incoming-block restore.  WITH_V also copies the block's V rows (V carries no
 // position) to the same page of v_pool in the same pass.  n_dev, when given, is
 // a device-side entry count: CTAs past it return at once, so a launch sized
 // for the largest count needs no host round trip.
 template <bool WITH_V>
-__global__ void __launch_bounds__(256) rerope_kernel(const __nv_bfloat16* __restrict__ k_src, int64_t sls, int64_t shs,
+__global__ void __launch_bounds__(256, KVSEL_REROPE_MINB) rerope_kernel(const __nv_bfloat16* __restrict__ k_src, int64_t sls, int64_t shs,
                                                      int src_tokens, const int32_t* __restrict__ src_block,
                                                      const int32_t* __restrict__ dst_page,
                                                      const int32_t* __restrict__ dst_pos0, const int32_t* n_dev,
                                                      int L, int Hkv, int D, int page, const float2* tlo,
-                                                     const float2* thi, int style, __nv_bfloat16* __restrict__ pool,
+                                                     const float2* thi, const double2* tlo64, const double2* thi64,
+                                                     int style, __nv_bfloat16* __restrict__ pool,
                                                      const __nv_bfloat16* __restrict__ v_src,
                                                      __nv_bfloat16* __restrict__ v_pool, int P, unsigned* dev_err) {
     if (n_dev && (int)blockIdx.x >= __ldg(n_dev)) return;
-    extern __shared__ float2 cs[];  // [page][D/2]
+    extern __shared__ float4 cs[];  // [page][D/16 groups][kQuadsPerGroup]
     const int i = blockIdx.x;
     const int l0 = blockIdx.y * kLayerGroup, l1 = min(L, l0 + kLayerGroup);
     const int sb = __ldg(src_block + i), dp = __ldg(dst_page + i), p0 = __ldg(dst_pos0 + i);
@@ -193,55 +319,82 @@ __global__ void __launch_bounds__(256) rerope_kernel(const __nv_bfloat16* __rest
         return;  // whole block leaves together
     }
     const int half = D / 2;
-    for (int idx = threadIdx.x; idx < page * half; idx += blockDim.x)
-        cs[idx] = rope_cs(tlo, thi, half, p0 + idx / half, idx % half);
+    const int PR = D >> 4;              // chunk pairs per row = frequency groups of eight
+    const int qrow = PR * kQuadsPerGroup;  // float4 per table row
+    for (int idx = threadIdx.x; idx < page * half; idx += blockDim.x) {
+        const float2 c = rope_cs(tlo, thi, half, p0 + idx / half, idx % half);
+        cs_put(cs + (idx / half) * qrow, idx % half, c.x, c.y);
+    }
     __syncthreads();
-    const int PR = D >> 4;              // chunk pairs per row
-    const int total = page * Hkv * PR;
-    for (int l = l0; l < l1; ++l) {
-        const __nv_bfloat16* src_l = k_src + (int64_t)l * sls + (int64_t)sb * page * D;
-        __nv_bfloat16* dst = pool + ((int64_t)l * P + dp) * (int64_t)page * Hkv * D;
-        for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
-            const int cp = idx % PR, r = idx / PR;
-            const int t = r / Hkv, g = r % Hkv;
-            const __nv_bfloat16* srow = src_l + (int64_t)g * shs + (int64_t)t * D;
-            __nv_bfloat16* drow = dst + (int64_t)r * D;
-            const float2* cst = cs + t * half;
-            // NeoX: chunk cp holds dims 8cp.. (first half), chunk cp + PR holds dims 8cp + D/2..
-            // interleaved: chunks cp and cp + PR each hold 4 adjacent pairs
-            const int ca = cp, cb = cp + PR;
-            float xa[8], xb[8];
-            unpack8(__ldcs(reinterpret_cast<const uint4*>(srow + 8 * ca)), xa);
-            unpack8(__ldcs(reinterpret_cast<const uint4*>(srow + 8 * cb)), xb);
-            if (style == KVSEL_ROPE_NEOX) {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float2 c = cst[8 * cp + k];
-                    const float a = xa[k], b = xb[k];
-                    xa[k] = fmaf(a, c.x, -b * c.y);
-                    xb[k] = fmaf(b, c.x, a * c.y);
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < 8; k += 2) {
-                    const float2 c1 = cst[4 * ca + k / 2], c2 = cst[4 * cb + k / 2];
-                    const float a1 = xa[k], b1 = xa[k + 1], a2 = xb[k], b2 = xb[k + 1];
-                    xa[k] = fmaf(a1, c1.x, -b1 * c1.y);
-                    xa[k + 1] = fmaf(b1, c1.x, a1 * c1.y);
-                    xb[k] = fmaf(a2, c2.x, -b2 * c2.y);
-                    xb[k + 1] = fmaf(b2, c2.x, a2 * c2.y);
-                }
-            }
-            __stcs(reinterpret_cast<uint4*>(drow + 8 * ca), pack8(xa));
-            __stcs(reinterpret_cast<uint4*>(drow + 8 * cb), pack8(xb));
-            if constexpr (WITH_V) {
-                // V: the same two 16-byte chunks of the V row, copied as they are
-                const __nv_bfloat16* vrow = v_src + (srow - k_src);
-                __nv_bfloat16* vdst = v_pool + (drow - pool);
-                __stcs(reinterpret_cast<uint4*>(vdst + 8 * ca), __ldcs(reinterpret_cast<const uint4*>(vrow + 8 * ca)));
-                __stcs(reinterpret_cast<uint4*>(vdst + 8 * cb), __ldcs(reinterpret_cast<const uint4*>(vrow + 8 * cb)));
-            }
+    // A thread keeps one chunk pair cp of rows r0, r0 + dr, ... of every layer
+    // (blockDim is a multiple of PR), and loads its next row's chunks before it
+    // turns the current ones.
+    const int rows = page * Hkv;
+    const int cp = threadIdx.x & (PR - 1), r0 = threadIdx.x / PR;
+    if (r0 >= rows) return;  // no barrier follows
+    const int dr = blockDim.x / PR, dt = dr / Hkv, dg = dr % Hkv;
+    const int t0 = r0 / Hkv, g0 = r0 % Hkv;
+    // NeoX: chunk cp holds dims 8cp.. (first half), chunk cp + PR holds dims 8cp + D/2..
+    // interleaved: chunks cp and cp + PR each hold 4 adjacent pairs
+    const int ca = cp, cb = cp + PR;
+    auto src_row = [&](int l, int t, int g) {
+        return k_src + (int64_t)l * sls + (int64_t)sb * page * D + (int64_t)g * shs + (int64_t)t * D;
+    };
+    int l = l0, r = r0, t = t0, g = g0;
+    const __nv_bfloat16* srow = src_row(l, t, g);
+    uint4 wa = __ldcs(reinterpret_cast<const uint4*>(srow + 8 * ca));
+    uint4 wb = __ldcs(reinterpret_cast<const uint4*>(srow + 8 * cb));
+    for (;;) {
+        int ln = l, rn = r + dr, tn = t + dt, gn = g + dg;
+        if (gn >= Hkv) {
+            gn -= Hkv;
+            ++tn;
         }
+        if (rn >= rows) {
+            ++ln;
+            rn = r0;
+            tn = t0;
+            gn = g0;
+        }
+        const bool more = ln < l1;
+        const __nv_bfloat16* snext = more ? src_row(ln, tn, gn) : srow;
+        uint4 na = make_uint4(0, 0, 0, 0), nb = na;
+        if (more) {
+            na = __ldcs(reinterpret_cast<const uint4*>(snext + 8 * ca));
+            nb = __ldcs(reinterpret_cast<const uint4*>(snext + 8 * cb));
+        }
+        __nv_bfloat16* drow = pool + (((int64_t)l * P + dp) * page * Hkv + r) * (int64_t)D;
+        uint4 va, vb;
+        const __nv_bfloat16* vrow = nullptr;
+        if constexpr (WITH_V) {
+            // V: the same two 16-byte chunks of the V row, copied as they are
+            vrow = v_src + (srow - k_src);
+            va = __ldcs(reinterpret_cast<const uint4*>(vrow + 8 * ca));
+            vb = __ldcs(reinterpret_cast<const uint4*>(vrow + 8 * cb));
+        }
+        float xa[8], xb[8];
+        unpack8(wa, xa);
+        unpack8(wb, xb);
+        const float4* cst = cs + t * qrow;
+        if (style == KVSEL_ROPE_NEOX)
+            turn_chunks<true>(xa, xb, cst, 8 * cp, 0, 0, srow, ca, cb, tlo64, thi64, half, p0 + t, false);
+        else
+            turn_chunks<false>(xa, xb, cst, 0, 4 * ca, 4 * cb, srow, ca, cb, tlo64, thi64, half, p0 + t, false);
+        __stcs(reinterpret_cast<uint4*>(drow + 8 * ca), pack8(xa));
+        __stcs(reinterpret_cast<uint4*>(drow + 8 * cb), pack8(xb));
+        if constexpr (WITH_V) {
+            __nv_bfloat16* vdst = v_pool + (drow - pool);
+            __stcs(reinterpret_cast<uint4*>(vdst + 8 * ca), va);
+            __stcs(reinterpret_cast<uint4*>(vdst + 8 * cb), vb);
+        }
+        if (!more) break;
+        l = ln;
+        r = rn;
+        t = tn;
+        g = gn;
+        srow = snext;
+        wa = na;
+        wb = nb;
     }
 }
 
@@ -249,12 +402,13 @@ __global__ void __launch_bounds__(256) rerope_kernel(const __nv_bfloat16* __rest
 // shifts[i] positions (negative: backwards), one rounding to bf16.  Grid: one
 // CTA per (entry, group of kLayerGroup layers); the D/2 (cos, sin) pairs of the
 // shift are computed once per CTA.
-__global__ void __launch_bounds__(256) shift_kernel(__nv_bfloat16* __restrict__ pool, int P,
+__global__ void __launch_bounds__(256, KVSEL_REROPE_MINB) shift_kernel(__nv_bfloat16* __restrict__ pool, int P,
                                                     const int32_t* __restrict__ pages,
                                                     const int32_t* __restrict__ shifts, const int32_t* n_dev, int L,
                                                     int Hkv, int D, int page, const float2* tlo, const float2* thi,
-                                                    int style, unsigned* dev_err) {
-    __shared__ float2 cs[128];  // [D/2]
+                                                    const double2* tlo64, const double2* thi64, int style,
+                                                    unsigned* dev_err) {
+    __shared__ float4 cs[16 * kQuadsPerGroup];  // one table row (D <= 256)
     if (n_dev && (int)blockIdx.x >= __ldg(n_dev)) return;
     const int i = blockIdx.x;
     const int l0 = blockIdx.y * kLayerGroup, l1 = min(L, l0 + kLayerGroup);
@@ -269,52 +423,61 @@ __global__ void __launch_bounds__(256) shift_kernel(__nv_bfloat16* __restrict__ 
     const int half = D / 2;
     for (int idx = threadIdx.x; idx < half; idx += blockDim.x) {
         const float2 c = rope_cs(tlo, thi, half, mag, idx);
-        cs[idx] = make_float2(c.x, sh < 0 ? -c.y : c.y);  // a backward turn negates the sine
+        cs_put(cs, idx, c.x, sh < 0 ? -c.y : c.y);  // a backward turn negates the sine
     }
     __syncthreads();
     const int PR = D >> 4;
-    const int total = page * Hkv * PR;
-    for (int l = l0; l < l1; ++l) {
-        __nv_bfloat16* base = pool + ((int64_t)l * P + pg) * (int64_t)page * Hkv * D;
-        for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
-            const int cp = idx % PR, r = idx / PR;
-            __nv_bfloat16* row = base + (int64_t)r * D;
-            const int ca = cp, cb = cp + PR;
-            float xa[8], xb[8];
-            unpack8(*reinterpret_cast<const uint4*>(row + 8 * ca), xa);
-            unpack8(*reinterpret_cast<const uint4*>(row + 8 * cb), xb);
-            if (style == KVSEL_ROPE_NEOX) {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float2 c = cs[8 * cp + k];
-                    const float a = xa[k], b = xb[k];
-                    xa[k] = fmaf(a, c.x, -b * c.y);
-                    xb[k] = fmaf(b, c.x, a * c.y);
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < 8; k += 2) {
-                    const float2 c1 = cs[4 * ca + k / 2], c2 = cs[4 * cb + k / 2];
-                    const float a1 = xa[k], b1 = xa[k + 1], a2 = xb[k], b2 = xb[k + 1];
-                    xa[k] = fmaf(a1, c1.x, -b1 * c1.y);
-                    xa[k + 1] = fmaf(b1, c1.x, a1 * c1.y);
-                    xb[k] = fmaf(a2, c2.x, -b2 * c2.y);
-                    xb[k + 1] = fmaf(b2, c2.x, a2 * c2.y);
-                }
-            }
-            *reinterpret_cast<uint4*>(row + 8 * ca) = pack8(xa);
-            *reinterpret_cast<uint4*>(row + 8 * cb) = pack8(xb);
+    // as in rerope_kernel: a thread keeps one chunk pair of rows r0, r0 + dr, ...
+    // of every layer and loads its next row before it turns the current one
+    const int rows = page * Hkv;
+    const int cp = threadIdx.x & (PR - 1), r0 = threadIdx.x / PR;
+    if (r0 >= rows) return;  // no barrier follows
+    const int dr = blockDim.x / PR;
+    const int ca = cp, cb = cp + PR;
+    auto row_of = [&](int l, int r) { return pool + (((int64_t)l * P + pg) * page * Hkv + r) * (int64_t)D; };
+    int l = l0, r = r0;
+    __nv_bfloat16* row = row_of(l, r);
+    uint4 wa = *reinterpret_cast<const uint4*>(row + 8 * ca);
+    uint4 wb = *reinterpret_cast<const uint4*>(row + 8 * cb);
+    for (;;) {
+        int ln = l, rn = r + dr;
+        if (rn >= rows) {
+            ++ln;
+            rn = r0;
         }
+        const bool more = ln < l1;
+        __nv_bfloat16* rnext = more ? row_of(ln, rn) : row;
+        uint4 na = make_uint4(0, 0, 0, 0), nb = na;
+        if (more) {
+            na = *reinterpret_cast<const uint4*>(rnext + 8 * ca);
+            nb = *reinterpret_cast<const uint4*>(rnext + 8 * cb);
+        }
+        float xa[8], xb[8];
+        unpack8(wa, xa);
+        unpack8(wb, xb);
+        if (style == KVSEL_ROPE_NEOX)
+            turn_chunks<true>(xa, xb, cs, 8 * cp, 0, 0, row, ca, cb, tlo64, thi64, half, mag, sh < 0);
+        else
+            turn_chunks<false>(xa, xb, cs, 0, 4 * ca, 4 * cb, row, ca, cb, tlo64, thi64, half, mag, sh < 0);
+        *reinterpret_cast<uint4*>(row + 8 * ca) = pack8(xa);
+        *reinterpret_cast<uint4*>(row + 8 * cb) = pack8(xb);
+        if (!more) break;
+        l = ln;
+        r = rn;
+        row = rnext;
+        wa = na;
+        wb = nb;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_rope_tables(float2* lo, float2* hi, int D, double base, cudaStream_t s) {
+cudaError_t launch_rope_tables(float2* lo, float2* hi, double2* lo64, double2* hi64, int D, double base,
+                               cudaStream_t s) {
     const int64_t total = (int64_t)(KVSEL_ROPE_LO + KVSEL_ROPE_HI) * (D / 2);
     int grid = (int)((total + 255) / 256);
     if (grid > 8192) grid = 8192;
-    rope_tables_kernel<<<grid, 256, 0, s>>>(lo, hi, D, base);
+    rope_tables_kernel<<<grid, 256, 0, s>>>(lo, hi, lo64, hi64, D, base);
     return cudaGetLastError();
 }
 
@@ -335,14 +498,14 @@ cudaError_t launch_rerope(const void* k_src, int64_t sls, int64_t shs, int src_t
                           int Hkv, int D, int page, const kvsel_ctx::RopeTab* tab, int rope_style, void* pool,
                           const void* v_src, void* v_pool, int P, unsigned* dev_err, cudaStream_t s) {
     const dim3 grid((unsigned)n, (unsigned)((L + kLayerGroup - 1) / kLayerGroup));
-    const size_t smem = sizeof(float2) * (size_t)page * (D / 2);
+    const size_t smem = sizeof(float4) * (size_t)page * (D / 16) * kQuadsPerGroup;
     auto kern = v_src ? rerope_kernel<true> : rerope_kernel<false>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
     kern<<<grid, 256, smem, s>>>(static_cast<const __nv_bfloat16*>(k_src), sls, shs, src_tokens, src_block, dst_page,
-                                 dst_pos0, n_dev, L, Hkv, D, page, tab->lo, tab->hi, rope_style,
+                                 dst_pos0, n_dev, L, Hkv, D, page, tab->lo, tab->hi, tab->lo64, tab->hi64, rope_style,
                                  static_cast<__nv_bfloat16*>(pool), static_cast<const __nv_bfloat16*>(v_src),
                                  static_cast<__nv_bfloat16*>(v_pool), P, dev_err);
     return cudaGetLastError();
@@ -353,6 +516,6 @@ cudaError_t launch_shift(void* pool, int P, const int32_t* pages, const int32_t*
                          unsigned* dev_err, cudaStream_t s) {
     const dim3 grid((unsigned)n, (unsigned)((L + kLayerGroup - 1) / kLayerGroup));
     shift_kernel<<<grid, 256, 0, s>>>(static_cast<__nv_bfloat16*>(pool), P, pages, shifts, n_dev, L, Hkv, D, page,
-                                      tab->lo, tab->hi, rope_style, dev_err);
+                                      tab->lo, tab->hi, tab->lo64, tab->hi64, rope_style, dev_err);
     return cudaGetLastError();
 }

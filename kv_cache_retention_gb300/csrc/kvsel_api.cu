@@ -115,19 +115,28 @@ const kvsel_ctx::RopeTab* kvsel_rope_tables(kvsel_ctx* ctx, int D, double base, 
         if (ctx->rope[i].D == D && ctx->rope[i].base == base) return &ctx->rope[i];
     int slot = ctx->n_rope < 8 ? ctx->n_rope : 7;  // keep at most 8; recycle the last
     kvsel_ctx::RopeTab& t = ctx->rope[slot];
-    if (t.lo) {
+    auto release = [&t]() {
         cudaFree(t.lo);
         cudaFree(t.hi);
+        cudaFree(t.lo64);
+        cudaFree(t.hi64);
         t.lo = t.hi = nullptr;
-    }
+        t.lo64 = t.hi64 = nullptr;
+        t.D = 0;
+    };
+    if (t.lo) release();
     size_t half = (size_t)D / 2;
-    if (cudaMalloc(&t.lo, sizeof(float2) * half * KVSEL_ROPE_LO) != cudaSuccess) return nullptr;
-    if (cudaMalloc(&t.hi, sizeof(float2) * half * KVSEL_ROPE_HI) != cudaSuccess) {
-        cudaFree(t.lo);
-        t.lo = nullptr;
+    if (cudaMalloc(&t.lo, sizeof(float2) * half * KVSEL_ROPE_LO) != cudaSuccess ||
+        cudaMalloc(&t.hi, sizeof(float2) * half * KVSEL_ROPE_HI) != cudaSuccess ||
+        cudaMalloc(&t.lo64, sizeof(double2) * half * KVSEL_ROPE_LO) != cudaSuccess ||
+        cudaMalloc(&t.hi64, sizeof(double2) * half * KVSEL_ROPE_HI) != cudaSuccess) {
+        release();
         return nullptr;
     }
-    if (launch_rope_tables(t.lo, t.hi, D, base, s) != cudaSuccess) return nullptr;
+    if (launch_rope_tables(t.lo, t.hi, t.lo64, t.hi64, D, base, s) != cudaSuccess) {
+        release();
+        return nullptr;
+    }
     t.D = D;
     t.base = base;
     if (slot == ctx->n_rope) ++ctx->n_rope;
@@ -168,6 +177,8 @@ int kvsel_ctx_destroy(kvsel_ctx* ctx) {
     for (int i = 0; i < ctx->n_rope; ++i) {
         cudaFree(ctx->rope[i].lo);
         cudaFree(ctx->rope[i].hi);
+        cudaFree(ctx->rope[i].lo64);
+        cudaFree(ctx->rope[i].hi64);
     }
     delete ctx;
     return KVSEL_OK;
@@ -176,6 +187,7 @@ int kvsel_ctx_destroy(kvsel_ctx* ctx) {
 const char* kvsel_last_error_string(const kvsel_ctx* ctx) { return ctx ? ctx->err : "null context"; }
 
 int kvsel_check_device(kvsel_ctx* ctx, void* stream) {
+    const kvsel_trace trace_("kvsel_check_device");
     int rc = enter(ctx);
     if (rc) return rc;
     cudaStream_t s = (cudaStream_t)stream;
@@ -198,6 +210,7 @@ int kvsel_check_device(kvsel_ctx* ctx, void* stream) {
 
 int kvsel_memory_update(kvsel_ctx* ctx, const void* q_rows, int q_dtype, int L, int Hq, int R, int D,
                         float lambda, int first_turn, int norm_mode, float* M, float* A, void* stream) {
+    const kvsel_trace trace_("kvsel_memory_update");
     int rc = enter(ctx);
     if (rc) return rc;
     if (!q_rows || !M) return fail(ctx, KVSEL_ERR_INVALID_ARG, "memory_update: null q_rows or M");
@@ -213,6 +226,7 @@ int kvsel_memory_update(kvsel_ctx* ctx, const void* q_rows, int q_dtype, int L, 
 
 int kvsel_memory_update_batch(kvsel_ctx* ctx, int q_dtype, int L, int Hq, int D, int norm_mode,
                               const kvsel_memory_session* sessions, int S, void* stream) {
+    const kvsel_trace trace_("kvsel_memory_update_batch");
     int rc = enter(ctx);
     if (rc) return rc;
     if (S < 0 || S > 65535 || (S > 0 && !sessions)) return fail(ctx, KVSEL_ERR_INVALID_ARG, "memory_update_batch: bad session table");
@@ -239,6 +253,7 @@ int kvsel_memory_update_batch(kvsel_ctx* ctx, int q_dtype, int L, int Hq, int D,
 int kvsel_rule_scores(kvsel_ctx* ctx, const void* k_pool, int k_dtype, const int32_t* slot_map, int n_slots,
                       int L, int Hq, int Hkv, int N, int D, int64_t layer_stride, int64_t slot_stride,
                       const float* M, int pi, int q_s, int q_e, float* rule, void* stream) {
+    const kvsel_trace trace_("kvsel_rule_scores");
     int rc = enter(ctx);
     if (rc) return rc;
     rc = kvsel_check_rule_scores_args(ctx, "rule_scores", k_pool, k_dtype, slot_map, n_slots, L, Hq, Hkv, N, D,
@@ -254,6 +269,7 @@ int kvsel_rule_scores(kvsel_ctx* ctx, const void* k_pool, int k_dtype, const int
 
 int kvsel_topk_retain(kvsel_ctx* ctx, const float* score, int N, int pi, int q_s, int q_e, int C, uint8_t* keep,
                       int32_t* keep_idx, int* n_keep_host, void* stream) {
+    const kvsel_trace trace_("kvsel_topk_retain");
     int rc = enter(ctx);
     if (rc) return rc;
     if (!score || (!keep && !keep_idx)) return fail(ctx, KVSEL_ERR_INVALID_ARG, "topk_retain: null score or no output");
@@ -271,6 +287,7 @@ int kvsel_topk_retain(kvsel_ctx* ctx, const float* score, int N, int pi, int q_s
 
 int kvsel_topk_retain_batch(kvsel_ctx* ctx, const kvsel_topk_session* sessions, int S, int* n_keep_host,
                             void* stream) {
+    const kvsel_trace trace_("kvsel_topk_retain_batch");
     int rc = enter(ctx);
     if (rc) return rc;
     if (S < 0 || (S > 0 && !sessions)) return fail(ctx, KVSEL_ERR_INVALID_ARG, "topk_retain_batch: bad session table");
@@ -297,6 +314,7 @@ int kvsel_topk_retain_batch(kvsel_ctx* ctx, const kvsel_topk_session* sessions, 
 int kvsel_rule_scores_batch(kvsel_ctx* ctx, const void* k_pool, int k_dtype, int n_slots, int L, int Hq, int Hkv,
                             int D, int64_t layer_stride, int64_t slot_stride, const kvsel_rule_session* sessions,
                             int S, void* stream) {
+    const kvsel_trace trace_("kvsel_rule_scores_batch");
     int rc = enter(ctx);
     if (rc) return rc;
     if (!k_pool || (S > 0 && !sessions)) return fail(ctx, KVSEL_ERR_INVALID_ARG, "rule_scores_batch: null pointer");
@@ -332,6 +350,7 @@ int kvsel_rule_scores_batch(kvsel_ctx* ctx, const void* k_pool, int k_dtype, int
 
 int kvsel_redirect_slots(kvsel_ctx* ctx, const int32_t* slot_in, const uint8_t* keep, int N, int32_t dead_slot,
                          int32_t* slot_out, void* stream) {
+    const kvsel_trace trace_("kvsel_redirect_slots");
     int rc = enter(ctx);
     if (rc) return rc;
     if (!slot_in || !keep || !slot_out) return fail(ctx, KVSEL_ERR_INVALID_ARG, "redirect_slots: null pointer");
@@ -342,6 +361,7 @@ int kvsel_redirect_slots(kvsel_ctx* ctx, const int32_t* slot_in, const uint8_t* 
 
 int kvsel_span_keep(kvsel_ctx* ctx, const int32_t* span_start, const int32_t* span_end, int n_cursors,
                     const int32_t* del_ids, int n_del, const uint8_t* keep_in, int N, uint8_t* keep_out, void* stream) {
+    const kvsel_trace trace_("kvsel_span_keep");
     int rc = enter(ctx);
     if (rc) return rc;
     if (N < 0 || n_cursors < 0 || n_del < 0) return fail(ctx, KVSEL_ERR_SHAPE, "span_keep: negative size");
@@ -355,6 +375,7 @@ int kvsel_span_keep(kvsel_ctx* ctx, const int32_t* span_start, const int32_t* sp
 
 int kvsel_index_to_fp8(kvsel_ctx* ctx, const void* index, int64_t rows, int D, uint8_t* codes, int8_t* exps,
                        void* stream) {
+    const kvsel_trace trace_("kvsel_index_to_fp8");
     int rc = enter(ctx);
     if (rc) return rc;
     if (rows < 0) return fail(ctx, KVSEL_ERR_SHAPE, "index_to_fp8: negative row count");
@@ -369,6 +390,7 @@ int kvsel_index_to_fp8(kvsel_ctx* ctx, const void* index, int64_t rows, int D, u
 
 int kvsel_index_from_fp8(kvsel_ctx* ctx, const uint8_t* codes, const int8_t* exps, int64_t rows, int D, void* index,
                          void* stream) {
+    const kvsel_trace trace_("kvsel_index_from_fp8");
     int rc = enter(ctx);
     if (rc) return rc;
     if (rows < 0) return fail(ctx, KVSEL_ERR_SHAPE, "index_from_fp8: negative row count");
@@ -383,6 +405,7 @@ int kvsel_index_from_fp8(kvsel_ctx* ctx, const uint8_t* codes, const int8_t* exp
 
 int kvsel_meank_build(kvsel_ctx* ctx, const void* k_src, int L, int Hkv, int T, int D, int block, int first_block,
                       const int32_t* src_pos, double rope_base, int rope_style, void* index, int Bcap, void* stream) {
+    const kvsel_trace trace_("kvsel_meank_build");
     int rc = enter(ctx);
     if (rc) return rc;
     if (!k_src || !index) return fail(ctx, KVSEL_ERR_INVALID_ARG, "meank_build: null pointer");
@@ -405,8 +428,10 @@ int kvsel_meank_build(kvsel_ctx* ctx, const void* k_src, int L, int Hkv, int T, 
                     "meank_build launch");
 }
 
-int kvsel_block_scores(kvsel_ctx* ctx, const void* q, const void* index, int L, int Hq, int Hkv, int M, int D,
-                       int n_blocks, int Bcap, int n_sink, int n_recent, float* R, float* R_partial, void* stream) {
+// kvsel_block_scores with the bounded waits' limit and the give-up test hook as arguments.
+static int block_scores_call(kvsel_ctx* ctx, const void* q, const void* index, int L, int Hq, int Hkv, int M, int D,
+                      int n_blocks, int Bcap, int n_sink, int n_recent, float* R, float* R_partial, void* stream,
+                      uint64_t wait_ns, int stuck) {
     int rc = enter(ctx);
     if (rc) return rc;
     if (!q || !index || !R) return fail(ctx, KVSEL_ERR_INVALID_ARG, "block_scores: null pointer");
@@ -420,12 +445,37 @@ int kvsel_block_scores(kvsel_ctx* ctx, const void* q, const void* index, int L, 
     void* ws = kvsel_workspace(ctx, block_scores_workspace(L, Hq, Hkv, M, n_blocks));
     if (!ws) return fail(ctx, KVSEL_ERR_CUDA, "block_scores: workspace allocation failed");
     return launched(ctx, launch_block_scores(ctx, q, index, L, Hq, Hkv, M, D, n_blocks, Bcap, n_sink, n_recent, R,
-                                             R_partial, ws, (cudaStream_t)stream),
+                                             R_partial, ws, (cudaStream_t)stream, wait_ns, stuck),
                     "block_scores launch");
+}
+
+int kvsel_block_scores(kvsel_ctx* ctx, const void* q, const void* index, int L, int Hq, int Hkv, int M, int D,
+                       int n_blocks, int Bcap, int n_sink, int n_recent, float* R, float* R_partial, void* stream) {
+    const kvsel_trace trace_("kvsel_block_scores");
+    return block_scores_call(ctx, q, index, L, Hq, Hkv, M, D, n_blocks, Bcap, n_sink, n_recent, R, R_partial, stream,
+                             KVSEL_BLOCK_WAIT_NS, 0);
+}
+
+// Test entry (not part of the public header): kvsel_block_scores in which the row
+// pass's first MMA issuer of every CTA waits on a barrier that nothing completes,
+// with every bounded wait of the row pass limited to wait_ns.  That wait gives up while copies and
+// MMAs are in flight, so the call exercises the tensor-core kernel's give-up path:
+// flag KVSEL_ERR_TIMEOUT in the device error word, drain its own copies and MMAs
+// (bounded waits), free TMEM and return.  R holds no meaningful values afterwards;
+// kvsel_check_device reports KVSEL_ERR_TIMEOUT.
+int kvsel_test_block_scores_give_up(kvsel_ctx* ctx, const void* q, const void* index, int L, int Hq, int Hkv, int M,
+                                    int D, int n_blocks, int Bcap, int n_sink, int n_recent, float* R,
+                                    uint64_t wait_ns, void* stream) {
+    const kvsel_trace trace_("kvsel_test_block_scores_give_up");
+    if (wait_ns == 0 || wait_ns > KVSEL_BLOCK_WAIT_NS)
+        return fail(ctx, KVSEL_ERR_INVALID_ARG, "test_block_scores_give_up: wait_ns must be in (0, 1 s]");
+    return block_scores_call(ctx, q, index, L, Hq, Hkv, M, D, n_blocks, Bcap, n_sink, n_recent, R, nullptr, stream,
+                             wait_ns, 1);
 }
 
 int kvsel_select_blocks(kvsel_ctx* ctx, const float* R, int n_blocks, int n_sink, int n_recent, int k, int32_t* ids,
                         int* n_sel_host, void* stream) {
+    const kvsel_trace trace_("kvsel_select_blocks");
     int rc = enter(ctx);
     if (rc) return rc;
     if (!R || !ids) return fail(ctx, KVSEL_ERR_INVALID_ARG, "select_blocks: null pointer");
@@ -445,6 +495,7 @@ int kvsel_rerope_scatter(kvsel_ctx* ctx, const void* k_src, int64_t src_layer_st
                          int src_tokens, const int32_t* src_block, const int32_t* dst_page, const int32_t* dst_pos0,
                          int n, int L, int Hkv, int D, int page, double rope_base, int rope_style, void* pool, int P,
                          void* stream) {
+    const kvsel_trace trace_("kvsel_rerope_scatter");
     int rc = enter(ctx);
     if (rc) return rc;
     if (!k_src || !src_block || !dst_page || !dst_pos0 || !pool) return fail(ctx, KVSEL_ERR_INVALID_ARG, "rerope_scatter: null pointer");
@@ -470,6 +521,7 @@ int kvsel_workset_diff(kvsel_ctx* ctx, const int32_t* prev_ids, const int32_t* p
                        const int32_t* new_ids, int n_new, int P, int page, int32_t* new_pages, int32_t* shift,
                        int32_t* in_rank, int32_t* in_page, int32_t* mv_rank, int32_t* mv_shift, int32_t* out_page,
                        int32_t* counts, void* stream) {
+    const kvsel_trace trace_("kvsel_workset_diff");
     int rc = enter(ctx);
     if (rc) return rc;
     if (n_prev < 0 || n_new < 0 || P <= 0 || page <= 0) return fail(ctx, KVSEL_ERR_SHAPE, "workset_diff: bad sizes");
@@ -489,6 +541,7 @@ int kvsel_restore_blocks(kvsel_ctx* ctx, const void* k_src, const void* v_src, i
                          int64_t src_head_stride, int src_tokens, const int32_t* src_block, const int32_t* dst_page,
                          const int32_t* dst_pos0, int n, const int32_t* n_dev, int L, int Hkv, int D, int page,
                          double rope_base, int rope_style, void* k_pool, void* v_pool, int P, void* stream) {
+    const kvsel_trace trace_("kvsel_restore_blocks");
     int rc = enter(ctx);
     if (rc) return rc;
     if (!k_src || !v_src || !src_block || !dst_page || !dst_pos0 || !k_pool || !v_pool)
@@ -515,6 +568,7 @@ int kvsel_restore_blocks(kvsel_ctx* ctx, const void* k_src, const void* v_src, i
 int kvsel_rerope_shift(kvsel_ctx* ctx, void* pool, int P, const int32_t* pages, const int32_t* shifts, int n,
                        const int32_t* n_dev, int L, int Hkv, int D, int page, double rope_base, int rope_style,
                        void* stream) {
+    const kvsel_trace trace_("kvsel_rerope_shift");
     int rc = enter(ctx);
     if (rc) return rc;
     if (!pool || !pages || !shifts) return fail(ctx, KVSEL_ERR_INVALID_ARG, "rerope_shift: null pointer");

@@ -3,8 +3,10 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "../../include/kvsel.h"
 
@@ -16,12 +18,15 @@ struct kvsel_ctx {
     size_t ws_bytes = 0;
     // Device error word: kernels OR kvsel_devcheck bits into it on bad data.
     unsigned* dev_err = nullptr;
-    // RoPE angle tables, one per (D, base): split-position cos/sin pairs.
+    // RoPE angle tables, one per (D, base): split-position cos/sin pairs, in
+    // fp32 for the fast path and in fp64 for outputs that nearly cancel.
     struct RopeTab {
         int D = 0;
         double base = 0.0;
-        float2* lo = nullptr;  // [KVSEL_ROPE_LO][D/2]: angle lo * theta_i
-        float2* hi = nullptr;  // [KVSEL_ROPE_HI][D/2]: angle hi * LO * theta_i
+        float2* lo = nullptr;     // [KVSEL_ROPE_LO][D/2]: angle lo * theta_i
+        float2* hi = nullptr;     // [KVSEL_ROPE_HI][D/2]: angle hi * LO * theta_i
+        double2* lo64 = nullptr;  // the same angles in fp64
+        double2* hi64 = nullptr;
     };
     RopeTab rope[8];
     int n_rope = 0;
@@ -59,6 +64,29 @@ enum kvsel_devcheck : unsigned {
 #define KVSEL_ROPE_LO (1 << KVSEL_ROPE_LO_BITS)
 #define KVSEL_ROPE_HI (1 << 14)
 #define KVSEL_MAX_POS (KVSEL_ROPE_LO * KVSEL_ROPE_HI)  // 2^24
+
+// NVTX range around one C-ABI call, named after the call, for profilers and
+// tracers.  Off unless the environment variable KVSEL_NVTX is set to 1 when the
+// library first checks it; then every kvsel_* call that launches work pushes a
+// range on entry and pops it on return.
+inline bool kvsel_nvtx_on() {
+    static const bool on = [] {
+        const char* v = getenv("KVSEL_NVTX");
+        return v && v[0] == '1' && v[1] == 0;
+    }();
+    return on;
+}
+struct kvsel_trace {
+    const bool on;
+    explicit kvsel_trace(const char* name) : on(kvsel_nvtx_on()) {
+        if (on) nvtxRangePushA(name);
+    }
+    ~kvsel_trace() {
+        if (on) nvtxRangePop();
+    }
+    kvsel_trace(const kvsel_trace&) = delete;
+    kvsel_trace& operator=(const kvsel_trace&) = delete;
+};
 
 // Error helpers shared by the translation units that implement calls:
 // entry guard, formatted failure (sets the context's error string), CUDA failure.
@@ -108,7 +136,8 @@ cudaError_t launch_topk(const float* score, int N, int pi, int q_s, int q_e, int
 cudaError_t launch_redirect(const int32_t* slot_in, const uint8_t* keep, int N, int32_t dead,
                             int32_t* slot_out, cudaStream_t s);
 
-cudaError_t launch_rope_tables(float2* lo, float2* hi, int D, double base, cudaStream_t s);
+cudaError_t launch_rope_tables(float2* lo, float2* hi, double2* lo64, double2* hi64, int D, double base,
+                               cudaStream_t s);
 
 cudaError_t launch_meank(const void* k_src, int L, int Hkv, int T, int D, int block, int first_block,
                          const int32_t* src_pos, const kvsel_ctx::RopeTab* tab, int rope_style,
@@ -134,7 +163,12 @@ cudaError_t launch_workset_diff(const int32_t* prev_ids, const int32_t* prev_pag
                                 int32_t* mv_shift, int32_t* out_page, int32_t* counts, unsigned* dev_err,
                                 cudaStream_t s);
 
+// wait_ns: how long a bounded wait inside the tensor-core kernels waits before it
+// gives up (KVSEL_BLOCK_WAIT_NS in normal calls); stuck: test hook, see
+// kvsel_test_block_scores_give_up.
+constexpr uint64_t KVSEL_BLOCK_WAIT_NS = 1000000000ull;
 cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index, int L, int Hq, int Hkv,
                                 int M, int D, int n_blocks, int Bcap, int n_sink, int n_recent, float* R,
-                                float* R_partial, void* ws, cudaStream_t s);
+                                float* R_partial, void* ws, cudaStream_t s, uint64_t wait_ns = KVSEL_BLOCK_WAIT_NS,
+                                int stuck = 0);
 size_t block_scores_workspace(int L, int Hq, int Hkv, int M, int n_blocks);

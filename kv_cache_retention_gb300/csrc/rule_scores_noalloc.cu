@@ -30,6 +30,7 @@ extern "C" int kvsel_rule_scores_noalloc(kvsel_ctx* ctx, const void* k_pool, int
                                          int n_slots, int L, int Hq, int Hkv, int N, int D, int64_t layer_stride,
                                          int64_t slot_stride, const float* M, int pi, int q_s, int q_e, float* rule,
                                          void* stream) {
+    const kvsel_trace trace_("kvsel_rule_scores_noalloc");
     int rc = kvsel_enter(ctx);  // also makes the context's device current
     if (rc) return rc;
     rc = kvsel_check_rule_scores_args(ctx, "rule_scores_noalloc", k_pool, k_dtype, slot_map, n_slots, L, Hq, Hkv, N,

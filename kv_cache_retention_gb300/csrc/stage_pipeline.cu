@@ -95,6 +95,7 @@ int kvsel_stage_restore(kvsel_ctx* ctx, const void* host_k, const void* host_v, 
                         const int32_t* dst_pos0, int n, int L, int Hkv, int D, int page, double rope_base,
                         int rope_style, void* k_pool, void* v_pool, int P, int chunk_blocks, int gather_threads,
                         int mode, void* stream) {
+    const kvsel_trace trace_("kvsel_stage_restore");
     int rc = kvsel_enter(ctx);
     if (rc) return rc;
     if (!host_k || !host_v || !blocks || !dst_page || !dst_pos0 || !k_pool || !v_pool)

@@ -187,14 +187,13 @@ def _scatter_check(ctx, k_src, src_block, dst_page, dst_pos0, P, page, base, sty
     sb, dp, d0 = src_block.cpu().numpy(), dst_page.cpu().numpy(), dst_pos0.cpu().numpy()
     untouched = np.setdiff1d(np.arange(P), dp)
     assert np.array_equal(got[:, untouched], before[:, untouched])
-    sel = np.arange(len(sb)) if n_check is None else np.linspace(0, len(sb) - 1, n_check).astype(int)
+    # sampled entries: evenly spread, with the first and the last (the largest compact positions)
+    sel = np.arange(len(sb)) if n_check is None else np.unique(np.linspace(0, len(sb) - 1, n_check).astype(int))
     ks = bits(k_src)
     for i in sel:
         ref = oracle.rerope_scatter(ks, sb[i:i + 1], np.array([0], np.int32), d0[i:i + 1],
                                     np.zeros((L, 1, page, Hkv, D), np.uint16), page, base, style)
-        raw = oracle.bf16_to_f64(ks[:, :, sb[i] * page:(sb[i] + 1) * page])     # [L,Hkv,page,D]
-        pair_mag = np.abs(raw).max(axis=-1, keepdims=True).transpose(0, 2, 1, 3)  # [L,page,Hkv,1]
-        _bf16_within(got[:, dp[i]], ref[:, 0], 2, f"re-RoPE entry {i}", floor=2.0 ** -14 * pair_mag)
+        _bf16_within(got[:, dp[i]], ref[:, 0], 2, f"re-RoPE entry {i}")
 
 
 @pytest.mark.parametrize("style", [kv.ROPE_NEOX, kv.ROPE_INTERLEAVED])
@@ -242,7 +241,7 @@ def test_rerope_full_size_incremental_sampled(ctx):
     inp = synth.block_inputs(w, "cuda")
     sb, dp, d0 = synth.scatter_plan_incremental(w, inp["page_perm"])
     _scatter_check(ctx, inp["staging"], sb, dp, d0, inp["pool"].shape[1], w.block, w.rope_base, kv.ROPE_NEOX,
-                   n_check=3)
+                   n_check=64)
 
 
 # ---------------------------------------------------------------------------
@@ -280,4 +279,4 @@ def test_kvmem_step_chain(ctx):
     for r in range(0, n, 7):
         ref = oracle.rerope_scatter(ks, ids_np[r:r + 1], np.array([0], np.int32), np.array([r * w.block], np.int32),
                                     np.zeros((w.L, 1, w.block, w.Hkv, w.D), np.uint16), w.block, w.rope_base)
-        _bf16_within(got[:, dst_page[r].item()], ref[:, 0], 2, f"scatter rank {r}", floor=2.0 ** -12)
+        _bf16_within(got[:, dst_page[r].item()], ref[:, 0], 2, f"scatter rank {r}")

@@ -86,3 +86,43 @@ def test_full_build_scatter_plan():
     assert x["raw"].shape == (1, 1, 40 * 32, 128) and "staging" not in x
     page, pos0 = synth.scatter_plan_full(w, x["page_perm"])
     assert len(page) == w.n_sel and torch.equal(pos0, torch.arange(w.n_sel, dtype=torch.int32) * 32)
+
+
+# ---------------------------------------------------------------------------
+# platform-independent draws (inputs of the stored full-size oracle values)
+# ---------------------------------------------------------------------------
+
+def test_portable_draws_are_fixed():
+    """The first draws of one key, as recorded on the host that wrote the stored oracle values
+    (bf16 bit patterns): a change in numpy's PCG64 stream or normal sampler shows up here."""
+    x = synth.portable_normal((6,), (1005, 4, 0))
+    assert synth.bf16_bits(x).tolist() == [15906, 16161, 48408, 49002, 49057, 16242]
+
+
+def test_portable_draws_spread_and_independence():
+    import numpy as np
+    a = synth.portable_normal((1 << 20,), (7, 1, 0)).astype(np.float64)
+    b = synth.portable_normal((1 << 20,), (7, 1, 1)).astype(np.float64)
+    assert abs(a.mean()) < 5e-3 and abs(a.std() - 1) < 5e-3
+    assert abs(np.corrcoef(a, b)[0, 1]) < 5e-3       # another layer key: another stream
+    s = synth.portable_normal((1 << 16,), (7, 1, 0), std=0.25)
+    assert np.array_equal(s, a[:1 << 16].astype(np.float32) * np.float32(0.25))
+
+
+def test_portable_block_layers():
+    import numpy as np
+    w = synth.scaled(synth.BLOCK["ws1m"], L=2, Hq=10, Hkv=2, n_blocks=64, M=8)
+    x0, x0b, x1 = synth.portable_block_layer(w, 0), synth.portable_block_layer(w, 0), synth.portable_block_layer(w, 1)
+    assert x0["q"].shape == (10, 8, 128) and x0["index"].shape == (2, 64, 128) and x0["q"].dtype == np.uint16
+    assert synth.portable_layer_digest(x0) == synth.portable_layer_digest(x0b) != synth.portable_layer_digest(x1)
+    # the workspace index spreads as offset + mean of a block: sigma^2 + 1/block
+    big = synth.scaled(w, n_blocks=4096)
+    v = (synth.portable_block_layer(big, 0)["index"].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert abs(v.std() - (0.25 + 1 / 32) ** 0.5) < 0.01
+    # full build: raw K of a block shares one offset per channel
+    m = synth.scaled(synth.BLOCK["meank262k"], L=1, Hq=5, Hkv=1, n_blocks=512, M=4)
+    raw = (synth.portable_block_layer(m, 0)["raw"].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    means = raw.reshape(1, 512, 32, 128).mean(axis=2)
+    assert abs(means.std() - (0.25 + 1 / 32) ** 0.5) < 0.02 and abs(raw.std() - 1.25 ** 0.5) < 0.01
+    d = synth.portable_digest([synth.portable_layer_digest(x0), synth.portable_layer_digest(x1)])
+    assert len(d) == 64 and d != synth.portable_digest([synth.portable_layer_digest(x1), synth.portable_layer_digest(x0)])
