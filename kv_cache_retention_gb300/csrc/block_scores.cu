@@ -8,28 +8,33 @@
 // For one (layer l, kv head g) the G = Hq/Hkv query heads' rows form one
 // contiguous [G*M][128] bf16 matrix Q_lg and the index one [Bcap][128] matrix
 // K_lg.  The logits S = Q_lg K_lg^T are never stored; two passes recompute them
-// on the tensor cores.  In both, A = 128 query rows (one per TMEM lane and
-// epilogue thread) and B = 256 candidate blocks (accumulator columns):
-//   row pass:    a unit is (l,g, 128 query rows); B tiles stream.  Each lane
-//                sums 2^(x - ref) over its row's 64-column slice, ref being a
-//                reference that only moves when a tile's sum passes 2^64; each
-//                slice's (ref, sum) goes to the workspace and bs_lse_merge
-//                combines the four slices of a row
+// on the tensor cores.  A unit holds a fixed operand of 256 rows (B, the
+// accumulator columns) and streams the other operand 128 rows a tile (A, the
+// TMEM lanes):
+//   row pass:    a unit is (l,g, 256 query rows); tiles of 128 candidate blocks
+//                stream.  A warp reads its 32 blocks x 64 query rows as two
+//                16x256b loads, so a thread holds 4 blocks x 16 rows, and adds
+//                2^(x - ref) into 16 per-row sums.  ref: one per (warp, row),
+//                the row's largest logit over the warp's blocks of the unit's
+//                first tile plus 64 (log2) of headroom, moved up by 64 when a
+//                sum passes 2^100.  At the end of the unit the sums are added
+//                across the warp's lanes (butterfly) and merged across the four
+//                lane quarters with their references
 //                -> lse2[r] = log2 sum_{b in C} 2^(S[r,b] log2e/sqrt(d))
-//   column pass: a unit is (l,g, 256 candidate blocks); A tiles stream.  A
-//                warp reads its 32 rows x 64 columns as two 16x256b loads, so a
-//                thread holds 4 rows x 16 columns; it adds 2^(x - lse2[r]) into
-//                16 column sums (lse2 loaded one tile ahead, one lane per row,
-//                handed on by shuffles).  At the end of the unit the columns are
-//                summed across lanes (a butterfly reduce-scatter) and across the
-//                four lane quarters -> mass[lg][b], complete per CTA
+//   column pass: a unit is (l,g, 256 candidate blocks); tiles of 128 query rows
+//                stream.  A thread holds 4 rows x 16 blocks; it adds
+//                2^(x - lse2[r]) into 16 per-block sums (lse2 loaded one tile
+//                ahead, one lane per row, handed on by shuffles).  At the end of
+//                the unit the sums are added across lanes (butterfly) and across
+//                the four lane quarters -> mass[lg][b], complete per CTA
 //   finalize:    R[b] = sum_lg mass[lg][b] / (L*Hq), in fixed (l,g) order.
+// Either way each unit's results are complete inside one CTA: no atomics, no
+// partial results in global memory.
 //
 // Kernel structure (one persistent CTA per SM, 608 threads):
-//   warp 0      TMA producer: the unit's fixed tile, then the streamed tiles
-//               (row pass: 2 x 32 KB of query rows, a ring of 2 x 64 KB of
-//               blocks; column pass: 64 KB of blocks, a ring of 4 x 32 KB of
-//               query rows; 128-byte swizzled, K-major, no multicast)
+//   warp 0      TMA producer: the unit's fixed tile (64 KB), then the streamed
+//               tiles through a ring of 4 x 32 KB (128-byte swizzled, K-major,
+//               no multicast)
 //   warps 1, 18 allocate 512 TMEM columns (warp 1); lane 0 of each issues
 //               tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M=128 N=256 K=16,
 //               8 per tile) for alternate tiles, each into its own 256-column
@@ -46,28 +51,27 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "kvsel_internal.h"
 
 namespace {
 
 constexpr float kScale = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e)/sqrt(128), logits to base 2
 constexpr int kD = 128;
-constexpr int BM = 128;                         // TMEM lanes = query rows per MMA
+constexpr int BM = 128;                         // TMEM lanes = streamed rows per MMA
 constexpr int kRowBytes = kD * 2;               // one bf16 row of 128 dims
 
 constexpr int kNAcc = 2;                        // accumulator buffers
 
-// Operand tiling of a pass.  The fixed operand is loaded once per unit (kNF
-// buffers), the streamed one once per tile (a ring of kNS stages).
-//   row pass:    fixed A = 128 query rows (two buffers, so that the next unit's
-//                rows load during this one), streamed B = 256 candidate blocks
-//                in a ring of 2 x 64 KB
-//   column pass: fixed B = 256 candidate blocks, streamed A = 128 query rows in
-//                a ring of 4 x 32 KB
-template <int MODE>
+// Operand tiling of both passes: the fixed operand (B, 256 rows, the
+// accumulator columns) is loaded once per unit, the streamed one (A, 128 rows,
+// the TMEM lanes) once per tile through a ring of kNS stages.
+//   row pass:    fixed = 256 query rows, streamed = 128 candidate blocks
+//   column pass: fixed = 256 candidate blocks, streamed = 128 query rows
 struct Tiling {
-    static constexpr int kFRows = MODE == 0 ? 128 : 256, kSRows = MODE == 0 ? 256 : 128;
-    static constexpr int kNF = MODE == 0 ? 2 : 1, kNS = MODE == 0 ? 2 : 4;
+    static constexpr int kFRows = 256, kSRows = 128;
+    static constexpr int kNF = 1, kNS = 4;
     static constexpr int kFBytes = kFRows * kRowBytes, kSBytes = kSRows * kRowBytes;
     static constexpr int kStageBytes = kNF * kFBytes + kNS * kSBytes;
     static_assert(kStageBytes == 192 * 1024, "operand buffers");
@@ -113,7 +117,6 @@ struct TcArgs {
     int Bcap;
     int n_blocks;
     float* lse2;       // [L*Hkv][rows_pad]; pad entries hold +inf
-    float2* part;      // row pass: [L*Hkv][rows_pad][kSlices] (ref, sum) of each column slice
     float* mass;       // [L*Hkv][n_blocks]
     unsigned* err;
     uint64_t wait_ns;  // give-up limit of a bounded wait
@@ -127,11 +130,14 @@ struct __align__(8) SmemTail {
     uint64_t never;    // no thread arrives on it (the give-up test hook waits here)
     uint32_t tmem_base;
     int abort_flag;
-    float red[MODE == 1 ? kSlices * 4 * kSliceCols : 1];  // column pass: [slice][lane quarter][column] sums
+    // unit end: [slice][lane quarter][column] (reference, sum) pairs (row pass) or sums (column pass)
+    float red[(MODE == 0 ? 2 : 1) * kSlices * 4 * kSliceCols];
+    // row pass: each epilogue warp's negated references of its 64 query rows
+    float nref[MODE == 0 ? kEpiWarps * kSliceCols : 1];
 };
 // operand buffers + barriers + room to align the buffers to 1024 bytes
 template <int MODE>
-constexpr size_t smem_bytes() { return (size_t)Tiling<MODE>::kStageBytes + sizeof(SmemTail<MODE>) + 1024; }
+constexpr size_t smem_bytes() { return (size_t)Tiling::kStageBytes + sizeof(SmemTail<MODE>) + 1024; }
 static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448, "shared memory per CTA");
 
 // ---- PTX wrappers ----------------------------------------------------------
@@ -146,6 +152,13 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
+}
+// Arrive from lane 0 of the warp only, as a predicated instruction (no branch).
+__device__ __forceinline__ void mbar_arrive_lane0(uint64_t* b, int lane) {
+    asm volatile("{\n .reg .pred p;\n setp.eq.s32 p, %1, 0;\n @p mbarrier.arrive.shared::cta.b64 _, [%0];\n}\n" ::"r"(
+                     saddr(b)),
+                 "r"(lane)
+                 : "memory");
 }
 __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
     uint32_t ok;
@@ -174,9 +187,10 @@ __device__ __forceinline__ uint64_t gtimer() {
 
 // Bounded wait for the phase of parity `parity`, giving up after limit_ns.
 // Returns false if this or another role gave up (the CTA is then draining).
-__device__ __noinline__ bool wait_phase(uint64_t* b, uint32_t parity, volatile int* abort_flag, unsigned* err,
-                                       uint64_t limit_ns) {
-    if (mbar_test(b, parity)) return true;
+// The first try_wait (which may park the thread until the phase completes) is
+// inlined; the retry loop with its time limit is not.
+__device__ __noinline__ bool wait_phase_retry(uint64_t* b, uint32_t parity, volatile int* abort_flag, unsigned* err,
+                                             uint64_t limit_ns) {
     const uint64_t t0 = gtimer();
     for (uint32_t i = 1;; ++i) {
         if (mbar_test(b, parity)) return true;
@@ -189,6 +203,10 @@ __device__ __noinline__ bool wait_phase(uint64_t* b, uint32_t parity, volatile i
             }
         }
     }
+}
+__device__ __forceinline__ bool wait_phase(uint64_t* b, uint32_t parity, volatile int* abort_flag, unsigned* err,
+                                           uint64_t limit_ns) {
+    return mbar_test(b, parity) || wait_phase_retry(b, parity, abort_flag, err, limit_ns);
 }
 
 // Bounded wait that ignores the abort flag: used to drain this thread's own
@@ -236,19 +254,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%"
-        "19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
 // 16 TMEM lanes x 8 repetitions of 256 bits.  Thread t receives, for repetition j,
 // v[4j], v[4j+1] from lane t/4 and v[4j+2], v[4j+3] from lane t/4 + 8, both at
 // columns 8j + 2(t%4) and 8j + 2(t%4) + 1.
@@ -287,15 +292,6 @@ __device__ __forceinline__ bool epi_bar_and(bool v) {
 
 // ---- epilogue helpers -----------------------------------------------------
 
-// Sum of 2^(v*scale - ref) over one 32-column chunk into four packed accumulators.
-__device__ __forceinline__ void row_terms(const float (&v)[32], float2 sc, float2 nr, float2 (&t2)[4]) {
-#pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-        const float2 x = __ffma2_rn(make_float2(v[i], v[i + 1]), sc, nr);
-        t2[(i >> 1) & 3] = __fadd2_rn(t2[(i >> 1) & 3], make_float2(ex2(x.x), ex2(x.y)));
-    }
-}
-
 // Column pass: adds 2^(v*scale - lse2) of one TMEM lane of a 16x256b load
 // (e = 0: lane t/4, e = 1: lane t/4 + 8) into the thread's 8 packed column sums.
 __device__ __forceinline__ void col_terms(const float (&v)[32], int e, float2 sc, float lse, float2 (&cs)[8]) {
@@ -307,16 +303,32 @@ __device__ __forceinline__ void col_terms(const float (&v)[32], int e, float2 sc
     }
 }
 
-// Largest value of a 64-column slice, as a tree of three-input maxima.
-__device__ __forceinline__ float slice_max(const float (&v)[kSliceCols / 32][32]) {
-    float m[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) m[j] = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < kSliceCols / 32; ++c)
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) m[(i >> 1) & 7] = max3(m[(i >> 1) & 7], v[c][i], v[c][i + 1]);
-    return max3(max3(m[0], m[1], m[2]), max3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+// Row pass: adds 2^(v*scale - ref) of column pair j over the
+// thread's four TMEM lanes (two 16x256b loads, each lanes t/4 and t/4 + 8) into
+// that pair's packed sum; nr: the pair's negated references.
+__device__ __forceinline__ void col_pair_terms(const float (&v0)[32], const float (&v1)[32], int j, float2 sc,
+                                               float2 nr, float2& sum) {
+    const float2 x0 = __ffma2_rn(make_float2(v0[4 * j], v0[4 * j + 1]), sc, nr);
+    const float2 x1 = __ffma2_rn(make_float2(v0[4 * j + 2], v0[4 * j + 3]), sc, nr);
+    const float2 x2 = __ffma2_rn(make_float2(v1[4 * j], v1[4 * j + 1]), sc, nr);
+    const float2 x3 = __ffma2_rn(make_float2(v1[4 * j + 2], v1[4 * j + 3]), sc, nr);
+    sum = __fadd2_rn(sum, make_float2(ex2(x0.x), ex2(x0.y)));
+    sum = __fadd2_rn(sum, make_float2(ex2(x1.x), ex2(x1.y)));
+    sum = __fadd2_rn(sum, make_float2(ex2(x2.x), ex2(x2.y)));
+    sum = __fadd2_rn(sum, make_float2(ex2(x3.x), ex2(x3.y)));
+}
+
+// Largest of column pair j's values over the thread's four TMEM lanes (two loads).
+__device__ __forceinline__ float2 col_max(const float (&v0)[32], const float (&v1)[32], int j) {
+    return make_float2(fmaxf(max3(v0[4 * j], v0[4 * j + 2], v1[4 * j]), v1[4 * j + 2]),
+                       fmaxf(max3(v0[4 * j + 1], v0[4 * j + 3], v1[4 * j + 1]), v1[4 * j + 3]));
+}
+
+// Merge of two (reference, sum) pairs of base-2 exponentials.
+__device__ __forceinline__ float2 lse2_merge(float2 a, float2 b) {
+    const float m = fmaxf(a.x, b.x);
+    if (m == -INFINITY) return make_float2(-INFINITY, 0.f);
+    return make_float2(m, a.y * ex2(a.x - m) + b.y * ex2(b.x - m));
 }
 
 // Column sums of a warp after the column pass: on entry lane t holds, for
@@ -341,12 +353,12 @@ __device__ __forceinline__ void column_reduce(float (&f)[16], int lane) {
 // ---- the kernel -----------------------------------------------------------
 
 // MODE 0: row pass, MODE 1: column pass (operand roles in Tiling).  Either
-// way one tile is one 128 x 256 accumulator: TMEM lane = query row, column =
-// candidate block.
+// way one tile is one 128 x 256 accumulator: TMEM lanes = the streamed rows,
+// columns = the unit's fixed rows.
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     block_scores_tc(const __grid_constant__ CUtensorMap mapF, const __grid_constant__ CUtensorMap mapS, const TcArgs a) {
-    using T = Tiling<MODE>;
+    using T = Tiling;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* sF = smem;                                   // [kNF][kFBytes]
@@ -391,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
                 const int lg = u / a.units_per_lg, o = u % a.units_per_lg;
                 const int fs = f_it % T::kNF;
-                const int yf = MODE == 0 ? lg * a.rows_g + o * T::kFRows : lg * a.Bcap + a.c0 + o * T::kFRows;
+                const int yf = MODE == 1 ? lg * a.Bcap + a.c0 + o * T::kFRows : lg * a.rows_g + o * T::kFRows;
                 if (!(ok = wait_phase(&t.empty_f[fs], ((f_it / T::kNF) & 1) ^ 1, abort_flag, a.err, a.wait_ns))) break;
                 mbar_expect_tx(&t.full_f[fs], T::kFBytes);
                 tma_load_2d(&mapF, &t.full_f[fs], sF + fs * T::kFBytes, 0, yf);
@@ -399,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++f_it;
                 for (int i = 0; i < a.n_it; ++i) {
                     const int st = s_it % T::kNS;
-                    const int ys = MODE == 0 ? lg * a.Bcap + a.c0 + i * T::kSRows : lg * a.rows_g + i * T::kSRows;
+                    const int ys = MODE == 1 ? lg * a.rows_g + i * T::kSRows : lg * a.Bcap + a.c0 + i * T::kSRows;
                     if (!(ok = wait_phase(&t.empty_s[st], ((s_it / T::kNS) & 1) ^ 1, abort_flag, a.err, a.wait_ns))) break;
                     mbar_expect_tx(&t.go[st], T::kSBytes);
                     tma_load_2d(&mapS, &t.go[st], sS + st * T::kSBytes, 0, ys);
@@ -444,8 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = wait_phase(&t.go[st], (s_it / T::kNS) & 1, abort_flag, a.err, a.wait_ns))) break;
                     tc_fence_after();
                     const uint32_t s_base = saddr(sS + st * T::kSBytes);
-                    // A = the 128-row operand, B = the 256-row one
-                    const uint32_t a_base = MODE == 0 ? f_base : s_base, b_base = MODE == 0 ? s_base : f_base;
+                    // A = the streamed 128-row operand, B = the unit's fixed 256 rows
+                    const uint32_t a_base = s_base, b_base = f_base;
                     const uint32_t d_tmem = tmem_base + (uint32_t)(k * kAccCols);
 #pragma unroll
                     for (int kk = 0; kk < kD / 16; ++kk) {
@@ -471,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ew = warp - 2;                 // 0 .. kEpiWarps-1
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
         const int slice = ew >> 2;               // column slice
-        const int r_local = q * 32 + lane;       // TMEM lane = query row of the tile
+        const int r_local = q * 32 + lane;       // this lane's TMEM lane (column pass: a query row of the tile)
         const int etid = ew * 32 + lane;
         const float2 sc = make_float2(kScale, kScale);
         // the first kNAcc tiles find their accumulators free
@@ -482,80 +494,106 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
             const int lg = u / a.units_per_lg, o = u % a.units_per_lg;
             const float* lse_lg = a.lse2 + (int64_t)lg * a.rows_pad;
-            // row pass: reference and sum of this lane's row over its slice
-            float ref = -INFINITY;
-            float2 s2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                            make_float2(0.f, 0.f)};
-            // column pass: this lane's row's share of each of its slice's 64 columns,
-            // and lse2 of its row in the next two tiles (loaded ahead)
+            // the thread's 16 sums (row pass: per query row, column pass: per block)
             float2 cs[8];
-            float lse_n = INFINITY;
-            if (MODE == 1) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) cs[j] = make_float2(0.f, 0.f);
-                if (r_local < a.rows_pad) lse_n = __ldg(lse_lg + r_local);
-            }
+            for (int j = 0; j < 8; ++j) cs[j] = make_float2(0.f, 0.f);
+            // column pass: lse2 of this lane's row in the next tile (loaded ahead)
+            float lse_n = INFINITY;
+            if (MODE == 1 && r_local < a.rows_pad) lse_n = __ldg(lse_lg + r_local);
+            // row pass: the warp's negated references of its 64 query rows, in shared
+            // memory (set by the unit's first tile)
+            float* const wref = t.nref + (MODE == 0 ? ew * kSliceCols : 0);
             bool ready = false;  // this tile's accumulator was seen complete by the probe below
-            for (int i = 0; i < a.n_it; ++i) {
-                const int k = acc_it % kNAcc;
+            const uint32_t taddr_q = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(slice * kSliceCols);
+            // One tile, accumulator K = the tile's position in the accumulator ring; MASK:
+            // the row pass's last tile, whose TMEM lanes past the candidate range are masked.
+            auto tile = [&](auto kc, auto maskc, int i) {
+                constexpr int K = decltype(kc)::value;
+                constexpr bool MASK = decltype(maskc)::value;
                 // After a timed-out wait a thread waits no more: its warp still runs the
                 // remaining tiles' TMEM loads (always in range, and warp-collective) and
                 // math on whatever the accumulator holds, and the epilogue warps agree on
                 // giving up at the end of the unit.  No per-tile vote or branch: in the
                 // column pass that alone cost a tenth of the tensor pipe's time.
-                if (ok && !ready) ok = wait_phase(&t.acc_full[k], (acc_it / kNAcc) & 1, abort_flag, a.err, a.wait_ns);
+                if (ok && !ready) ok = wait_phase(&t.acc_full[K], (acc_it >> 1) & 1u, abort_flag, a.err, a.wait_ns);
                 tc_fence_after();
-                const uint32_t taddr =
-                    tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(k * kAccCols + slice * kSliceCols);
+                const uint32_t taddr = taddr_q + (uint32_t)(K * kAccCols);
+                // releases accumulator K on the stage barrier of the tile kNAcc ahead
+                uint64_t* release = &t.go[(acc_it + kNAcc) % T::kNS];
+                const bool more = i + 1 < a.n_it;
+                const uint32_t next_par = ((acc_it + 1) >> 1) & 1u;
                 if (MODE == 0) {
-                    float v[kSliceCols / 32][32];
-#pragma unroll
-                    for (int c = 0; c < kSliceCols / 32; ++c) tmem_ld32(taddr + 32 * c, v[c]);
+                    // row pass: TMEM lanes are candidate blocks, columns query rows; a
+                    // thread holds 4 blocks x 16 rows and sums each row
+                    float v0[32], v1[32];
+                    tmem_ld16x256_8(taddr, v0);
+                    tmem_ld16x256_8(taddr + (16u << 16), v1);
                     tmem_ld_wait();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&t.go[(acc_it + kNAcc) % T::kNS]);  // accumulator k is read
-                    // probe the next tile's accumulator now: the answer arrives while this
-                    // tile's math runs, instead of costing a blocking wait after it
-                    ready = i + 1 < a.n_it && mbar_done(&t.acc_full[(acc_it + 1) % kNAcc], ((acc_it + 1) / kNAcc) & 1);
-                    // columns past the candidate range (last tile only) are masked
-                    const int nvalid = a.c1 - (a.c0 + i * kAccCols + slice * kSliceCols);
-                    if (nvalid < kSliceCols) {
+                    mbar_arrive_lane0(release, lane);
+                    ready = more && mbar_done(&t.acc_full[1 - K], next_par);
+                    if (MASK) {
+                        // blocks past the candidate range (TMEM lanes q*32 + 16h + t/4 + 8e)
+                        const int b0 = a.c0 + i * BM + q * 32 + (lane >> 2);
+                        const bool ok00 = b0 < a.c1, ok01 = b0 + 8 < a.c1, ok10 = b0 + 16 < a.c1, ok11 = b0 + 24 < a.c1;
 #pragma unroll
-                        for (int c = 0; c < kSliceCols / 32; ++c)
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (c * 32 + j >= nvalid) v[c][j] = -INFINITY;
-                    }
-                    if (ref == -INFINITY) ref = slice_max(v) * kScale;  // first tile with a finite logit
-                    if (ref != -INFINITY) {
-                        float2 t2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                                        make_float2(0.f, 0.f)};
-#pragma unroll
-                        for (int c = 0; c < kSliceCols / 32; ++c) row_terms(v[c], sc, make_float2(-ref, -ref), t2);
-                        const float big = fmaxf(max3(t2[0].x, t2[0].y, t2[1].x), max3(t2[1].y, t2[2].x, t2[2].y));
-                        if (!(fmaxf(big, fmaxf(t2[3].x, t2[3].y)) <= 0x1p64f)) {
-                            // a logit far above the reference: move it to this tile's
-                            // maximum, rescale the sum and take the tile again
-                            const float r_new = fmaxf(ref, slice_max(v) * kScale);
-                            const float f = ex2(ref - r_new);
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                s2[j] = make_float2(s2[j].x * f, s2[j].y * f);
-                                t2[j] = make_float2(0.f, 0.f);
-                            }
-                            ref = r_new;
-#pragma unroll
-                            for (int c = 0; c < kSliceCols / 32; ++c) row_terms(v[c], sc, make_float2(-ref, -ref), t2);
+                        for (int j = 0; j < 8; ++j) {
+                            if (!ok00) v0[4 * j] = v0[4 * j + 1] = -INFINITY;
+                            if (!ok01) v0[4 * j + 2] = v0[4 * j + 3] = -INFINITY;
+                            if (!ok10) v1[4 * j] = v1[4 * j + 1] = -INFINITY;
+                            if (!ok11) v1[4 * j + 2] = v1[4 * j + 3] = -INFINITY;
                         }
+                    }
+                    const int cq = 2 * (lane & 3);  // the thread's first column within each 8
+                    if (i == 0) {
+                        // references: each column's largest logit over the warp's 32 blocks of
+                        // the unit's first tile, plus 64 (log2) of headroom; 0 where the warp
+                        // holds no candidate
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) s2[j] = __fadd2_rn(s2[j], t2[j]);
+                        for (int j = 0; j < 8; ++j) {
+                            float2 m = col_max(v0, v1, j);
+#pragma unroll
+                            for (int o2 = 4; o2 <= 16; o2 <<= 1)
+                                m = make_float2(fmaxf(m.x, __shfl_xor_sync(0xffffffffu, m.x, o2)),
+                                                fmaxf(m.y, __shfl_xor_sync(0xffffffffu, m.y, o2)));
+                            if (lane < 4)
+                                *reinterpret_cast<float2*>(wref + 8 * j + cq) =
+                                    make_float2(m.x == -INFINITY ? 0.f : -(m.x * kScale + 64.f),
+                                                m.y == -INFINITY ? 0.f : -(m.y * kScale + 64.f));
+                        }
+                        __syncwarp();
+                    }
+                    // column pair by column pair, so that one pair's references are live at a time
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float2 nr = *reinterpret_cast<const float2*>(wref + 8 * j + cq);
+                        col_pair_terms(v0, v1, j, sc, nr, cs[j]);
+                    }
+                    float big = fmaxf(max3(cs[0].x, cs[0].y, cs[1].x), max3(cs[1].y, cs[2].x, cs[2].y));
+                    big = fmaxf(big, max3(cs[3].x, cs[3].y, cs[4].x));
+                    big = fmaxf(big, max3(cs[4].y, cs[5].x, cs[5].y));
+                    big = fmaxf(big, max3(cs[6].x, cs[6].y, fmaxf(cs[7].x, cs[7].y)));
+                    if (__any_sync(0xffffffffu, !(big <= 0x1p100f))) {
+                        // sums far above their references: move every reference of the warp
+                        // up by 64 and scale the sums down to match
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) cs[j] = make_float2(cs[j].x * 0x1p-64f, cs[j].y * 0x1p-64f);
+                        if (lane < 4) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                float2* r = reinterpret_cast<float2*>(wref + 8 * j + cq);
+                                *r = make_float2(r->x - 64.f, r->y - 64.f);
+                            }
+                        }
+                        __syncwarp();
                     }
                 } else {
                     // column pass: rows past rows_pad read +inf and add nothing
                     const float lse = lse_n;
                     const int r1 = (i + 1) * BM + r_local;
-                    lse_n = (i + 1 < a.n_it && r1 < a.rows_pad) ? __ldg(lse_lg + r1) : INFINITY;
+                    lse_n = (more && r1 < a.rows_pad) ? __ldg(lse_lg + r1) : INFINITY;
                     // the warp's 32 lanes in two halves of 16; each thread gets 4 rows x 16
                     // columns, so the whole slice is read before the accumulator is released
                     float v0[32], v1[32];
@@ -564,10 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_wait();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&t.go[(acc_it + kNAcc) % T::kNS]);
-                    // probe the next tile's accumulator now: the answer arrives while this
-                    // tile's math runs, instead of costing a blocking wait after it
-                    ready = i + 1 < a.n_it && mbar_done(&t.acc_full[(acc_it + 1) % kNAcc], ((acc_it + 1) / kNAcc) & 1);
+                    mbar_arrive_lane0(release, lane);
+                    ready = more && mbar_done(&t.acc_full[1 - K], next_par);
                     // lse2 of the thread's rows, from the lanes that loaded them
                     const int rl = lane >> 2;
                     col_terms(v0, 0, sc, __shfl_sync(0xffffffffu, lse, rl), cs);
@@ -575,15 +611,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                     col_terms(v1, 0, sc, __shfl_sync(0xffffffffu, lse, rl + 16), cs);
                     col_terms(v1, 1, sc, __shfl_sync(0xffffffffu, lse, rl + 24), cs);
                 }
+            };
+            using K0 = std::integral_constant<int, 0>;
+            using K1 = std::integral_constant<int, 1>;
+            using M0 = std::integral_constant<bool, false>;
+            using M1 = std::integral_constant<bool, true>;
+            for (int i = 0; i < a.n_it; ++i) {
+                // only the row pass's last tile can run past the candidate range
+                const bool mask = MODE == 0 && i + 1 == a.n_it;
+                if (acc_it & 1u) {
+                    if (mask) tile(K1{}, M1{}, i); else tile(K1{}, M0{}, i);
+                } else {
+                    if (mask) tile(K0{}, M1{}, i); else tile(K0{}, M0{}, i);
+                }
                 ++acc_it;
             }
             if (!(ok = epi_bar_and(ok))) break;
             if (MODE == 0) {
-                // this slice's (reference, sum) of the row; bs_lse_merge combines the slices
-                const float s_part =
-                    (s2[0].x + s2[0].y) + (s2[1].x + s2[1].y) + (s2[2].x + s2[2].y) + (s2[3].x + s2[3].y);
-                const int row = o * BM + r_local;
-                if (row < a.rows_g) a.part[((int64_t)lg * a.rows_pad + row) * kSlices + slice] = make_float2(ref, s_part);
+                // each query row's sum over the warp's blocks (one reference per warp and
+                // column), then a (reference, sum) merge over the four lane quarters in
+                // fixed order -> lse2 of the unit's 256 query rows
+                float f[16];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    f[2 * j] = cs[j].x;
+                    f[2 * j + 1] = cs[j].y;
+                }
+                column_reduce(f, lane);
+                float2* red = reinterpret_cast<float2*>(t.red);  // [kSlices][4][kSliceCols]
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int col = 2 * lane + c;
+                    red[(slice * 4 + q) * kSliceCols + col] = make_float2(f[c] > 0.f ? -wref[col] : -INFINITY, f[c]);
+                }
+                epi_bar();
+                if (etid < kAccCols) {
+                    const int sl = etid / kSliceCols, cc = etid % kSliceCols;
+                    const float2* rc = red + sl * 4 * kSliceCols + cc;
+                    const float2 m = lse2_merge(lse2_merge(lse2_merge(rc[0], rc[kSliceCols]), rc[2 * kSliceCols]),
+                                                rc[3 * kSliceCols]);
+                    const int row = o * T::kFRows + etid;
+                    if (row < a.rows_g)
+                        a.lse2[(int64_t)lg * a.rows_pad + row] = m.y > 0.f ? m.x + __log2f(m.y) : -INFINITY;
+                    else if (row < a.rows_pad)
+                        a.lse2[(int64_t)lg * a.rows_pad + row] = INFINITY;
+                }
             } else {
                 // sum each column over the warp's rows, then over the four lane quarters
                 float f[16];
@@ -619,32 +691,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// lse2 of each query row from the row pass's per-slice (reference, sum)
-// pairs, merged in slice order; rows past rows_g get +inf (they add nothing
-// in the column pass).
-__global__ void bs_lse_merge(const float2* __restrict__ part, float* lse2, int LH, int rows_g, int rows_pad) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= (int64_t)LH * rows_pad) return;
-    const int row = (int)(i % rows_pad);
-    if (row >= rows_g) {
-        lse2[i] = INFINITY;
-        return;
-    }
-    float2 p[kSlices];
-    float m = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kSlices; ++j) {
-        p[j] = part[i * kSlices + j];
-        m = fmaxf(m, p[j].x);
-    }
-    float sum = 0.f;
-    if (m != -INFINITY) {
-#pragma unroll
-        for (int j = 0; j < kSlices; ++j) sum += p[j].y * ex2(p[j].x - m);
-    }
-    lse2[i] = sum > 0.f ? m + __log2f(sum) : -INFINITY;
-}
-
 // R[b] = sum_lg mass[lg][b] / (L*Hq) on C; zero outside C (also in mass).
 __global__ void bs_finalize(const float* __restrict__ mass_in, float* mass, float* R, int LH, int n_blocks, int c0,
                             int c1, float inv) {
@@ -662,18 +708,7 @@ __global__ void bs_finalize(const float* __restrict__ mass_in, float* mass, floa
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-PFN_cuTensorMapEncodeTiled_v12000 encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
+PFN_cuTensorMapEncodeTiled_v12000 encoder() { return kvsel_tmap_encoder(); }
 
 // 2-D bf16 [rows][128] view, box {64 columns, box_rows}, 128-byte swizzle, zero fill.
 bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
@@ -690,10 +725,22 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_ro
 
 }  // namespace
 
+PFN_cuTensorMapEncodeTiled_v12000 kvsel_tmap_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
 size_t block_scores_workspace(int L, int Hq, int Hkv, int M, int n_blocks) {
     const size_t rows_pad = (((size_t)(Hq / Hkv) * M + 3) & ~(size_t)3);
-    return align256((size_t)L * Hkv * rows_pad * sizeof(float)) + align256((size_t)L * Hkv * n_blocks * sizeof(float)) +
-           align256((size_t)L * Hkv * rows_pad * kSlices * sizeof(float2));
+    return align256((size_t)L * Hkv * rows_pad * sizeof(float)) + align256((size_t)L * Hkv * n_blocks * sizeof(float));
 }
 
 cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index, int L, int Hq, int Hkv, int M, int D,
@@ -712,13 +759,15 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
     w += align256((size_t)LH * rows_pad * sizeof(float));
     float* mass_ws = reinterpret_cast<float*>(w);
     float* mass = R_partial ? R_partial : mass_ws;
-    w += align256((size_t)LH * n_blocks * sizeof(float));
-    float2* part = reinterpret_cast<float2*>(w);
 
     if (ncand > 0) {
-        CUtensorMap q128, i256;
+        // query rows and index rows as 2-D tensors, in boxes of 256 rows (the fixed
+        // operand) and of 128 rows (the streamed one)
+        CUtensorMap q256, q128, i256, i128;
         const uint64_t q_rows = (uint64_t)L * Hq * M, i_rows = (uint64_t)LH * Bcap;
-        if (!make_map(&q128, q, q_rows, BM) || !make_map(&i256, index, i_rows, kAccCols)) return cudaErrorInvalidValue;
+        if (!make_map(&q256, q, q_rows, kAccCols) || !make_map(&q128, q, q_rows, BM) ||
+            !make_map(&i256, index, i_rows, kAccCols) || !make_map(&i128, index, i_rows, BM))
+            return cudaErrorInvalidValue;
         cudaError_t e = cudaFuncSetAttribute(block_scores_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem_bytes<0>());
         if (e == cudaSuccess)
@@ -733,19 +782,17 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
         a.Bcap = Bcap;
         a.n_blocks = n_blocks;
         a.lse2 = lse2;
-        a.part = part;
         a.mass = mass;
         a.err = ctx->dev_err;
         a.wait_ns = wait_ns;
         a.stuck = stuck;
-        // row pass: a unit per 128 query rows, the candidate blocks streamed 256 at a time
-        a.units_per_lg = (rows_g + BM - 1) / BM;
+        // row pass: a unit per 256 query rows, the candidate blocks streamed 128 at a
+        // time; it writes lse2 of its rows
+        a.units_per_lg = (rows_g + kAccCols - 1) / kAccCols;
         a.n_units = LH * a.units_per_lg;
-        a.n_it = (ncand + kAccCols - 1) / kAccCols;
+        a.n_it = (ncand + BM - 1) / BM;
         int grid = a.n_units < ctx->num_sms ? a.n_units : ctx->num_sms;
-        block_scores_tc<0><<<grid, kThreads, smem_bytes<0>(), s>>>(q128, i256, a);
-        const int64_t n_rows = (int64_t)LH * rows_pad;
-        bs_lse_merge<<<(unsigned)((n_rows + 255) / 256), 256, 0, s>>>(part, lse2, LH, rows_g, rows_pad);
+        block_scores_tc<0><<<grid, kThreads, smem_bytes<0>(), s>>>(q256, i128, a);
         // column pass: a unit per 256 candidate blocks, the query rows streamed 128 at a time
         a.units_per_lg = (ncand + kAccCols - 1) / kAccCols;
         a.n_units = LH * a.units_per_lg;

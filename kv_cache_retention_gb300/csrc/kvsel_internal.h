@@ -2,6 +2,8 @@
 // the public ABI; see include/kvsel.h for the calls and their contracts).
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
 #include <stddef.h>
@@ -172,3 +174,5 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
                                 float* R_partial, void* ws, cudaStream_t s, uint64_t wait_ns = KVSEL_BLOCK_WAIT_NS,
                                 int stuck = 0);
 size_t block_scores_workspace(int L, int Hq, int Hkv, int M, int n_blocks);
+// The driver's cuTensorMapEncodeTiled (looked up once), or nullptr.
+PFN_cuTensorMapEncodeTiled_v12000 kvsel_tmap_encoder();
