@@ -153,7 +153,7 @@ def setup_session(kv, synth, ctx, tw, bw, torch):
 
 # kernel launches per C-ABI call (counted from the launchers in csrc/)
 LAUNCHES = {"memory_update": 1, "rule_scores": 3, "topk_retain": 1, "redirect_slots": 1, "meank_build": 1,
-            "block_scores": 4, "select_blocks": 1, "rerope_scatter": 1}
+            "block_scores": 3, "select_blocks": 1, "rerope_scatter": 1}
 
 
 # the step input each call reads first (end-to-end leg: the call waits for that input's copy only)
@@ -296,6 +296,17 @@ def ours(args, rank, world, local_rank):
     e_end.record()
     torch.cuda.synchronize()
     barrier()
+    # the same per-step input copies alone (no kernels), for reading the e2e figure:
+    # when they take longer than the device step, e2e is bound by the host link
+    c_start, c_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(copy_stream):
+        c_start.record(copy_stream)
+        for i in range(2):
+            for k in in_keys:
+                sets[i % 2][k].copy_(h_in[k], non_blocking=True)
+        c_end.record(copy_stream)
+    torch.cuda.synchronize()
+    h2d_alone_ms = c_start.elapsed_time(c_end) / 2
     token_rows, block_rows = workload_rows(tw, bw)
     rows_step = token_rows + block_rows
     value, ms_max = aggregate(ms_total, rows_step, args.steps, dist, "cuda")
@@ -341,6 +352,7 @@ def ours(args, rank, world, local_rank):
         "rows_per_step": {"token": token_rows, "block": block_rows},
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms_max / e2e_steps,
+                "h2d_alone_ms_per_step": h2d_alone_ms, "h2d_alone_gbs": h2d / (h2d_alone_ms / 1e3) / 1e9,
                 "inputs": "per-step query rows, new raw K and staged top-block K from pinned host, double-buffered "
                           "and copied on a second stream with one event per input (each call waits for the input "
                           "it reads; step t+1's inputs move while step t computes); K pool and Mean-K index "
@@ -356,10 +368,9 @@ def ours(args, rank, world, local_rank):
 # DRAM bytes (read + write) per call from an ncu capture of the current kernel code, scaled to the
 # bench workload; an entry is removed whenever its kernel changes.
 PROFILED_TRAFFIC = {
-    # block_scores_tc, 4-layer capture of both passes (row 352.5 + 11.4 MB, column 354.0 + 6.6 MB),
-    # x16 for 64 layers: ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on
-    # python bench.py --profile-kernel block_scores --profile-layers 4
-    "block_scores": 16 * (352.454912 + 11.352832 + 354.045952 + 6.576640) * 1e6,
+    # block_scores_tc, 4-layer capture of both passes (row 351.6 + 5.8 MB, column 354.3 + 7.1 MB),
+    # x16 for 64 layers: ncu --set full on python bench.py --profile-kernel block_scores --profile-layers 4
+    "block_scores": 16 * (351.567616 + 5.844992 + 354.290688 + 7.115520) * 1e6,
 }
 
 
@@ -597,7 +608,8 @@ def extra_profile_case(args):
     pages); workset_diff: two 2180-block working sets sharing two thirds; span_keep: N=92160 with
     100 of 400 cursors deleted; rule_scores_batch: 36 sessions of 1024-8192 tokens at the 8B shape;
     index_to_fp8 / index_from_fp8: the 1M-workspace index (32768 blocks, Hkv8 D128) per layer;
-    topk_small: top-C* of a 16384-token session (C=4096, the one-CTA path)."""
+    topk_small: top-C* of a 16384-token session (C=4096, the one-CTA path); topk_n<N>: top-C* of an
+    N-token session (C = N/4)."""
     import numpy as np
     import torch
 
@@ -643,12 +655,13 @@ def extra_profile_case(args):
         else:
             fn = lambda: ctx.index_from_fp8(codes, exps, out)  # noqa: E731
         moved = L * Hkv * nb * (3 * D + 1)
-    elif name == "topk_small":
-        N = 16384
+    elif name == "topk_small" or name.startswith("topk_n"):
+        N = 16384 if name == "topk_small" else int(name[len("topk_n"):])
         score = torch.rand(N, device="cuda")
         keep = torch.empty(N, dtype=torch.uint8, device="cuda")
         keep_idx = torch.empty(N, dtype=torch.int32, device="cuda")
-        fn = lambda: ctx.topk_retain(score, 256, N - 512, N, 4096, keep=keep, keep_idx=keep_idx)  # noqa: E731
+        C = 4096 if name == "topk_small" else N // 4
+        fn = lambda: ctx.topk_retain(score, 256, N - 512, N, C, keep=keep, keep_idx=keep_idx)  # noqa: E731
         moved = 5 * N
     elif name == "span_keep":
         N = 92160
@@ -702,7 +715,7 @@ def profile_case(args):
     import kv_cache_retention_gb300 as kv
     import synth
 
-    if args.profile_kernel in EXTRA_CASES:
+    if args.profile_kernel in EXTRA_CASES or args.profile_kernel.startswith("topk_n"):
         extra_profile_case(args)
         return
     torch.cuda.set_device(0)

@@ -281,7 +281,11 @@ int kvsel_topk_retain(kvsel_ctx* ctx, const float* score, int N, int pi, int q_s
     int64_t need = cstar < nH ? cstar : nH;
     if (n_keep_host) *n_keep_host = (int)(nF + need);
     if (N == 0) return KVSEL_OK;
-    return launched(ctx, launch_topk(score, N, pi, q_s, q_e, (int)need, (int)nH, keep, keep_idx, (cudaStream_t)stream),
+    void* ws = nullptr;
+    if (const size_t wb = topk_workspace(N)) {
+        if (!(ws = kvsel_workspace(ctx, wb))) return fail(ctx, KVSEL_ERR_CUDA, "topk_retain: workspace allocation failed");
+    }
+    return launched(ctx, launch_topk(score, N, pi, q_s, q_e, (int)need, (int)nH, keep, keep_idx, ws, (cudaStream_t)stream),
                     "topk_retain launch");
 }
 
@@ -292,6 +296,7 @@ int kvsel_topk_retain_batch(kvsel_ctx* ctx, const kvsel_topk_session* sessions, 
     if (rc) return rc;
     if (S < 0 || (S > 0 && !sessions)) return fail(ctx, KVSEL_ERR_INVALID_ARG, "topk_retain_batch: bad session table");
     std::vector<int> need((size_t)S), n_cand((size_t)S);
+    int max_N = 0;
     for (int i = 0; i < S; ++i) {
         const kvsel_topk_session& x = sessions[i];
         if (!x.rule || (!x.keep && !x.keep_idx)) return fail(ctx, KVSEL_ERR_INVALID_ARG, "topk_retain_batch: session %d: null score or no output", i);
@@ -302,10 +307,11 @@ int kvsel_topk_retain_batch(kvsel_ctx* ctx, const kvsel_topk_session* sessions, 
         const int64_t cstar = x.C - nF > 0 ? x.C - nF : 0;
         need[i] = (int)(cstar < nH ? cstar : nH);
         n_cand[i] = (int)nH;
+        if (x.N > max_N) max_N = x.N;
         if (n_keep_host) n_keep_host[i] = (int)(nF + need[i]);
     }
     if (S == 0) return KVSEL_OK;
-    void* ws = kvsel_workspace(ctx, topk_batch_workspace(S));
+    void* ws = kvsel_workspace(ctx, topk_batch_workspace(S, max_N));
     if (!ws) return fail(ctx, KVSEL_ERR_CUDA, "topk_retain_batch: workspace allocation failed");
     return launched(ctx, launch_topk_batch(sessions, need.data(), n_cand.data(), S, ws, (cudaStream_t)stream),
                     "topk_retain_batch launch");
@@ -487,7 +493,11 @@ int kvsel_select_blocks(kvsel_ctx* ctx, const float* R, int n_blocks, int n_sink
     int64_t need = k < nC ? k : nC;
     if (n_sel_host) *n_sel_host = (int)(nF + need);
     if (n_blocks == 0) return KVSEL_OK;
-    return launched(ctx, launch_topk(R, n_blocks, S, q_s, n_blocks, (int)need, (int)nC, nullptr, ids, (cudaStream_t)stream),
+    void* ws = nullptr;
+    if (const size_t wb = topk_workspace(n_blocks)) {
+        if (!(ws = kvsel_workspace(ctx, wb))) return fail(ctx, KVSEL_ERR_CUDA, "select_blocks: workspace allocation failed");
+    }
+    return launched(ctx, launch_topk(R, n_blocks, S, q_s, n_blocks, (int)need, (int)nC, nullptr, ids, ws, (cudaStream_t)stream),
                     "select_blocks launch");
 }
 

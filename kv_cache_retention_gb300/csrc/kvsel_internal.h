@@ -129,11 +129,13 @@ cudaError_t launch_rule_scores(kvsel_ctx* ctx, const void* k_pool, int dtype, co
 size_t rule_scores_workspace(kvsel_ctx* ctx, int L, int Hq, int N);
 
 // need: how many of the non-forced positions to keep by score (0..|H|).
-size_t topk_batch_workspace(int S);
+// Workspace of the grid-wide selection for sessions longer than one cluster holds (0 below).
+size_t topk_workspace(int N);
+size_t topk_batch_workspace(int S, int max_N);
 cudaError_t launch_topk_batch(const kvsel_topk_session* sess, const int* need, const int* n_cand, int S, void* ws,
                               cudaStream_t s);
 cudaError_t launch_topk(const float* score, int N, int pi, int q_s, int q_e, int need, int n_cand,
-                        uint8_t* keep, int32_t* keep_idx, cudaStream_t s);
+                        uint8_t* keep, int32_t* keep_idx, void* ws, cudaStream_t s);
 
 cudaError_t launch_redirect(const int32_t* slot_in, const uint8_t* keep, int N, int32_t dead,
                             int32_t* slot_out, cudaStream_t s);

@@ -213,8 +213,14 @@ def test_rule_scores_bad_slot_sets_device_error(ctx):
 @pytest.mark.parametrize("N,pi,qs,qe,C", [(5000, 64, 4872, 5000, 512), (92160, 256, 91136, 92160, 8192),
                                           (100, 10, 90, 100, 100), (100, 10, 90, 100, 5), (100, 100, 100, 100, 7),
                                           (1, 0, 1, 1, 0), (3000, 0, 3000, 3000, 2999), (777, 5, 700, 777, 200),
-                                          (16384, 64, 16000, 16384, 4096), (16385, 64, 16000, 16385, 4096)])
+                                          (16384, 64, 16000, 16384, 4096), (16385, 64, 16000, 16385, 4096),
+                                          (8192, 64, 7680, 8192, 2048), (8193, 64, 7680, 8193, 2048),
+                                          (131072, 256, 130048, 131072, 8192), (131073, 256, 130048, 131073, 8192),
+                                          (262144, 256, 261120, 262144, 16384), (262145, 256, 261120, 262145, 16384),
+                                          (1048576, 256, 1047552, 1048576, 65536)])
 def test_topk_exact_on_same_scores(ctx, N, pi, qs, qe, C):
+    """The one-CTA, 8-CTA cluster, 16-CTA cluster and re-reading paths on both sides of each
+    size limit, bit-exact against the oracle on the same (heavily tied) scores."""
     gen = torch.Generator(device="cuda").manual_seed(N + C)
     s = torch.rand(N, generator=gen, device="cuda")
     s = torch.round(s * 50) / 50  # many exact ties
