@@ -153,7 +153,7 @@ def setup_session(kv, synth, ctx, tw, bw, torch):
 
 # kernel launches per C-ABI call (counted from the launchers in csrc/)
 LAUNCHES = {"memory_update": 1, "rule_scores": 3, "topk_retain": 1, "redirect_slots": 1, "meank_build": 1,
-            "block_scores": 3, "select_blocks": 1, "rerope_scatter": 1}
+            "block_scores": 4, "select_blocks": 1, "rerope_scatter": 1}
 
 
 # the step input each call reads first (end-to-end leg: the call waits for that input's copy only)
@@ -266,21 +266,26 @@ def ours(args, rank, world, local_rank):
     ev_copied = [{k: torch.cuda.Event() for k in in_keys} for _ in range(2)]
     ev_done = [torch.cuda.Event(), torch.cuda.Event()]
 
-    def issue_copy(i):
+    def issue_copy(i, spans=None):
         with torch.cuda.stream(copy_stream):
             if i >= 2:
                 copy_stream.wait_event(ev_done[i % 2])  # step i-2 is done with this buffer set
+            if spans is not None:
+                spans.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+                spans[-1][0].record(copy_stream)
             for k in in_keys:
                 sets[i % 2][k].copy_(h_in[k], non_blocking=True)
                 ev_copied[i % 2][k].record(copy_stream)
+            if spans is not None:
+                spans[-1][1].record(copy_stream)
 
-    def e2e_run(n, start_event=None):
+    def e2e_run(n, start_event=None, spans=None):
         if start_event is not None:
             copy_stream.wait_event(start_event)
-        issue_copy(0)
+        issue_copy(0, spans)
         for i in range(n):
             if i + 1 < n:
-                issue_copy(i + 1)
+                issue_copy(i + 1, spans)
             run_step(ctx, sets[i % 2], ready=ev_copied[i % 2])
             ev_done[i % 2].record(compute_stream)
             for k, t in h_out.items():
@@ -292,10 +297,12 @@ def ours(args, rank, world, local_rank):
     barrier()
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_start.record()
-    e2e_run(e2e_steps, e_start)
+    copy_spans = []  # each step's input copies, start to end on the copy stream (the link rate under load)
+    e2e_run(e2e_steps, e_start, copy_spans)
     e_end.record()
     torch.cuda.synchronize()
     barrier()
+    h2d_in_e2e_ms = sum(a.elapsed_time(b) for a, b in copy_spans) / len(copy_spans)
     # the same per-step input copies alone (no kernels), for reading the e2e figure:
     # when they take longer than the device step, e2e is bound by the host link
     c_start, c_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -353,6 +360,7 @@ def ours(args, rank, world, local_rank):
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms_max / e2e_steps,
                 "h2d_alone_ms_per_step": h2d_alone_ms, "h2d_alone_gbs": h2d / (h2d_alone_ms / 1e3) / 1e9,
+                "h2d_during_ms_per_step": h2d_in_e2e_ms, "h2d_during_gbs": h2d / (h2d_in_e2e_ms / 1e3) / 1e9,
                 "inputs": "per-step query rows, new raw K and staged top-block K from pinned host, double-buffered "
                           "and copied on a second stream with one event per input (each call waits for the input "
                           "it reads; step t+1's inputs move while step t computes); K pool and Mean-K index "
@@ -368,9 +376,11 @@ def ours(args, rank, world, local_rank):
 # DRAM bytes (read + write) per call from an ncu capture of the current kernel code, scaled to the
 # bench workload; an entry is removed whenever its kernel changes.
 PROFILED_TRAFFIC = {
-    # block_scores_tc, 4-layer capture of both passes (row 351.6 + 5.8 MB, column 354.3 + 7.1 MB),
-    # x16 for 64 layers: ncu --set full on python bench.py --profile-kernel block_scores --profile-layers 4
-    "block_scores": 16 * (351.567616 + 5.844992 + 354.290688 + 7.115520) * 1e6,
+    # block_scores_tc, 4-layer capture of the three tensor-core launches (row pass 352.3 + 5.6 MB,
+    # exact pass 0.07 + 0 MB, column pass 353.8 + 3.5 MB), x16 for 64 layers:
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,... -k regex:block_scores_tc -c 3
+    # on python bench.py --profile-kernel block_scores --profile-layers 4 --steps 3 --warmup 1
+    "block_scores": 16 * (352.302336 + 5.601280 + 0.074496 + 353.814016 + 3.526656) * 1e6,
 }
 
 

@@ -14,13 +14,21 @@
 //   row pass:    a unit is (l,g, 256 query rows); tiles of 128 candidate blocks
 //                stream.  A warp reads its 32 blocks x 64 query rows as two
 //                16x256b loads, so a thread holds 4 blocks x 16 rows, and adds
-//                2^(x - ref) into 16 per-row sums.  ref: one per (warp, row),
-//                the row's largest logit over the warp's blocks of the unit's
-//                first tile plus 64 (log2) of headroom, moved up by 64 when a
+//                2^(x - ref) into 16 per-row sums.  ref: one per warp, the
+//                largest logit over the warp's 32 blocks x 64 rows of the unit's
+//                first tile plus 16 (log2) of headroom, moved up by 64 when a
 //                sum passes 2^100.  At the end of the unit the sums are added
 //                across the warp's lanes (butterfly) and merged across the four
 //                lane quarters with their references
 //                -> lse2[r] = log2 sum_{b in C} 2^(S[r,b] log2e/sqrt(d))
+//                A row whose merged sum is below 2^-90 of its reference (its
+//                largest logit lies more than 74 below the warp's), or not
+//                finite, may have lost terms to underflow or overflowed; the
+//                unit is then marked for
+//   exact pass:  the row pass again on the marked units only (every other unit
+//                is skipped by all roles), with one reference per (warp, row):
+//                the row's largest logit over the warp's blocks of the first
+//                tile plus 64.  It overwrites the unit's lse2.
 //   column pass: a unit is (l,g, 256 candidate blocks); tiles of 128 query rows
 //                stream.  A thread holds 4 rows x 16 blocks; it adds
 //                2^(x - lse2[r]) into 16 per-block sums (lse2 loaded one tile
@@ -28,7 +36,7 @@
 //                the unit the sums are added across lanes (butterfly) and across
 //                the four lane quarters -> mass[lg][b], complete per CTA
 //   finalize:    R[b] = sum_lg mass[lg][b] / (L*Hq), in fixed (l,g) order.
-// Either way each unit's results are complete inside one CTA: no atomics, no
+// Every pass completes each unit's results inside one CTA: no atomics, no
 // partial results in global memory.
 //
 // Kernel structure (one persistent CTA per SM, 608 threads):
@@ -119,9 +127,15 @@ struct TcArgs {
     float* lse2;       // [L*Hkv][rows_pad]; pad entries hold +inf
     float* mass;       // [L*Hkv][n_blocks]
     unsigned* err;
+    int* redo;         // [row-pass units]: set by the row pass where the exact pass must redo the unit
     uint64_t wait_ns;  // give-up limit of a bounded wait
     int stuck;         // test hook: the row pass's first MMA issuer waits on a barrier nothing completes
 };
+
+// MODE 0: row pass, one reference per warp; MODE 2: the exact row pass over the
+// units the row pass marked, one reference per (warp, row); MODE 1: column pass.
+template <int MODE>
+constexpr bool kRowPass = MODE != 1;
 
 template <int MODE>
 struct __align__(8) SmemTail {
@@ -130,15 +144,16 @@ struct __align__(8) SmemTail {
     uint64_t never;    // no thread arrives on it (the give-up test hook waits here)
     uint32_t tmem_base;
     int abort_flag;
-    // unit end: [slice][lane quarter][column] (reference, sum) pairs (row pass) or sums (column pass)
-    float red[(MODE == 0 ? 2 : 1) * kSlices * 4 * kSliceCols];
-    // row pass: each epilogue warp's negated references of its 64 query rows
-    float nref[MODE == 0 ? kEpiWarps * kSliceCols : 1];
+    // unit end: [slice][lane quarter][column] (reference, sum) pairs (row passes) or sums (column pass)
+    float red[(kRowPass<MODE> ? 2 : 1) * kSlices * 4 * kSliceCols];
+    // exact row pass: each epilogue warp's negated references of its 64 query rows
+    float nref[MODE == 2 ? kEpiWarps * kSliceCols : 1];
 };
 // operand buffers + barriers + room to align the buffers to 1024 bytes
 template <int MODE>
 constexpr size_t smem_bytes() { return (size_t)Tiling::kStageBytes + sizeof(SmemTail<MODE>) + 1024; }
-static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448, "shared memory per CTA");
+static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448,
+              "shared memory per CTA");
 
 // ---- PTX wrappers ----------------------------------------------------------
 
@@ -290,6 +305,17 @@ __device__ __forceinline__ bool epi_bar_and(bool v) {
     return r != 0;
 }
 
+// Barrier over the epilogue threads that ORs a flag across them.
+__device__ __forceinline__ bool epi_bar_or(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(kEpiThreads)
+        : "memory");
+    return r != 0;
+}
+
 // ---- epilogue helpers -----------------------------------------------------
 
 // Column pass: adds 2^(v*scale - lse2) of one TMEM lane of a 16x256b load
@@ -352,9 +378,9 @@ __device__ __forceinline__ void column_reduce(float (&f)[16], int lane) {
 
 // ---- the kernel -----------------------------------------------------------
 
-// MODE 0: row pass, MODE 1: column pass (operand roles in Tiling).  Either
-// way one tile is one 128 x 256 accumulator: TMEM lanes = the streamed rows,
-// columns = the unit's fixed rows.
+// MODE 0 / 2: row pass / exact row pass, MODE 1: column pass (operand roles in
+// Tiling).  Either way one tile is one 128 x 256 accumulator: TMEM lanes = the
+// streamed rows, columns = the unit's fixed rows.
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     block_scores_tc(const __grid_constant__ CUtensorMap mapF, const __grid_constant__ CUtensorMap mapS, const TcArgs a) {
@@ -401,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t f_it = 0, s_it = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
+                if (MODE == 2 && !a.redo[u]) continue;  // every role skips the same units
                 const int lg = u / a.units_per_lg, o = u % a.units_per_lg;
                 const int fs = f_it % T::kNF;
                 const int yf = MODE == 1 ? lg * a.Bcap + a.c0 + o * T::kFRows : lg * a.rows_g + o * T::kFRows;
@@ -439,6 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // copies and the other issuer's MMAs are in flight
             if (MODE == 0 && a.stuck && me == 0) ok = wait_phase(&t.never, 0, abort_flag, a.err, a.wait_ns);
             for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
+                if (MODE == 2 && !a.redo[u]) continue;
                 const int fs = f_it % T::kNF;
                 if (!(ok = wait_phase(&t.full_f[fs], (f_it / T::kNF) & 1, abort_flag, a.err, a.wait_ns))) break;
                 tc_fence_after();
@@ -492,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t acc_it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
+            if (MODE == 2 && !a.redo[u]) continue;
             const int lg = u / a.units_per_lg, o = u % a.units_per_lg;
             const float* lse_lg = a.lse2 + (int64_t)lg * a.rows_pad;
             // the thread's 16 sums (row pass: per query row, column pass: per block)
@@ -501,9 +530,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // column pass: lse2 of this lane's row in the next tile (loaded ahead)
             float lse_n = INFINITY;
             if (MODE == 1 && r_local < a.rows_pad) lse_n = __ldg(lse_lg + r_local);
-            // row pass: the warp's negated references of its 64 query rows, in shared
-            // memory (set by the unit's first tile)
-            float* const wref = t.nref + (MODE == 0 ? ew * kSliceCols : 0);
+            // exact row pass: the warp's negated references of its 64 query rows, in
+            // shared memory (set by the unit's first tile)
+            float* const wref = t.nref + (MODE == 2 ? ew * kSliceCols : 0);
+            // row pass: the warp's one negated reference (set by the unit's first tile)
+            float wnr = 0.f;
             bool ready = false;  // this tile's accumulator was seen complete by the probe below
             const uint32_t taddr_q = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(slice * kSliceCols);
             // One tile, accumulator K = the tile's position in the accumulator ring; MASK:
@@ -523,8 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint64_t* release = &t.go[(acc_it + kNAcc) % T::kNS];
                 const bool more = i + 1 < a.n_it;
                 const uint32_t next_par = ((acc_it + 1) >> 1) & 1u;
-                if (MODE == 0) {
-                    // row pass: TMEM lanes are candidate blocks, columns query rows; a
+                if constexpr (kRowPass<MODE>) {
+                    // row passes: TMEM lanes are candidate blocks, columns query rows; a
                     // thread holds 4 blocks x 16 rows and sums each row
                     float v0[32], v1[32];
                     tmem_ld16x256_8(taddr, v0);
@@ -546,48 +577,79 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (!ok11) v1[4 * j + 2] = v1[4 * j + 3] = -INFINITY;
                         }
                     }
-                    const int cq = 2 * (lane & 3);  // the thread's first column within each 8
-                    if (i == 0) {
-                        // references: each column's largest logit over the warp's 32 blocks of
-                        // the unit's first tile, plus 64 (log2) of headroom; 0 where the warp
-                        // holds no candidate
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            float2 m = col_max(v0, v1, j);
-#pragma unroll
-                            for (int o2 = 4; o2 <= 16; o2 <<= 1)
-                                m = make_float2(fmaxf(m.x, __shfl_xor_sync(0xffffffffu, m.x, o2)),
-                                                fmaxf(m.y, __shfl_xor_sync(0xffffffffu, m.y, o2)));
-                            if (lane < 4)
-                                *reinterpret_cast<float2*>(wref + 8 * j + cq) =
-                                    make_float2(m.x == -INFINITY ? 0.f : -(m.x * kScale + 64.f),
-                                                m.y == -INFINITY ? 0.f : -(m.y * kScale + 64.f));
-                        }
-                        __syncwarp();
-                    }
-                    // column pair by column pair, so that one pair's references are live at a time
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float2 nr = *reinterpret_cast<const float2*>(wref + 8 * j + cq);
-                        col_pair_terms(v0, v1, j, sc, nr, cs[j]);
-                    }
-                    float big = fmaxf(max3(cs[0].x, cs[0].y, cs[1].x), max3(cs[1].y, cs[2].x, cs[2].y));
-                    big = fmaxf(big, max3(cs[3].x, cs[3].y, cs[4].x));
-                    big = fmaxf(big, max3(cs[4].y, cs[5].x, cs[5].y));
-                    big = fmaxf(big, max3(cs[6].x, cs[6].y, fmaxf(cs[7].x, cs[7].y)));
-                    if (__any_sync(0xffffffffu, !(big <= 0x1p100f))) {
-                        // sums far above their references: move every reference of the warp
-                        // up by 64 and scale the sums down to match
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) cs[j] = make_float2(cs[j].x * 0x1p-64f, cs[j].y * 0x1p-64f);
-                        if (lane < 4) {
+                    if constexpr (MODE == 0) {
+                        if (i == 0) {
+                            // the reference: the largest logit over the warp's 32 blocks x 64
+                            // rows of the unit's first tile, plus 16 (log2) of headroom; 0
+                            // where the warp holds no candidate
+                            float mx = -INFINITY;
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
-                                float2* r = reinterpret_cast<float2*>(wref + 8 * j + cq);
-                                *r = make_float2(r->x - 64.f, r->y - 64.f);
+                                const float2 m = col_max(v0, v1, j);
+                                mx = fmaxf(mx, fmaxf(m.x, m.y));
                             }
+#pragma unroll
+                            for (int o2 = 1; o2 <= 16; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+                            wnr = mx == -INFINITY ? 0.f : -(mx * kScale + 16.f);
                         }
-                        __syncwarp();
+                        const float2 nr = make_float2(wnr, wnr);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) col_pair_terms(v0, v1, j, sc, nr, cs[j]);
+                        float big = fmaxf(max3(cs[0].x, cs[0].y, cs[1].x), max3(cs[1].y, cs[2].x, cs[2].y));
+                        big = fmaxf(big, max3(cs[3].x, cs[3].y, cs[4].x));
+                        big = fmaxf(big, max3(cs[4].y, cs[5].x, cs[5].y));
+                        big = fmaxf(big, max3(cs[6].x, cs[6].y, fmaxf(cs[7].x, cs[7].y)));
+                        if (__any_sync(0xffffffffu, !(big <= 0x1p100f))) {
+                            // sums far above the reference: move it up by 64 and scale the
+                            // sums down to match
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) cs[j] = make_float2(cs[j].x * 0x1p-64f, cs[j].y * 0x1p-64f);
+                            wnr -= 64.f;
+                        }
+                    } else {
+                        const int cq = 2 * (lane & 3);  // the thread's first column within each 8
+                        if (i == 0) {
+                            // references: each column's largest logit over the warp's 32 blocks of
+                            // the unit's first tile, plus 64 (log2) of headroom; 0 where the warp
+                            // holds no candidate
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                float2 m = col_max(v0, v1, j);
+#pragma unroll
+                                for (int o2 = 4; o2 <= 16; o2 <<= 1)
+                                    m = make_float2(fmaxf(m.x, __shfl_xor_sync(0xffffffffu, m.x, o2)),
+                                                    fmaxf(m.y, __shfl_xor_sync(0xffffffffu, m.y, o2)));
+                                if (lane < 4)
+                                    *reinterpret_cast<float2*>(wref + 8 * j + cq) =
+                                        make_float2(m.x == -INFINITY ? 0.f : -(m.x * kScale + 64.f),
+                                                    m.y == -INFINITY ? 0.f : -(m.y * kScale + 64.f));
+                            }
+                            __syncwarp();
+                        }
+                        // column pair by column pair, so that one pair's references are live at a time
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float2 nr = *reinterpret_cast<const float2*>(wref + 8 * j + cq);
+                            col_pair_terms(v0, v1, j, sc, nr, cs[j]);
+                        }
+                        float big = fmaxf(max3(cs[0].x, cs[0].y, cs[1].x), max3(cs[1].y, cs[2].x, cs[2].y));
+                        big = fmaxf(big, max3(cs[3].x, cs[3].y, cs[4].x));
+                        big = fmaxf(big, max3(cs[4].y, cs[5].x, cs[5].y));
+                        big = fmaxf(big, max3(cs[6].x, cs[6].y, fmaxf(cs[7].x, cs[7].y)));
+                        if (__any_sync(0xffffffffu, !(big <= 0x1p100f))) {
+                            // sums far above their references: move every reference of the warp
+                            // up by 64 and scale the sums down to match
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) cs[j] = make_float2(cs[j].x * 0x1p-64f, cs[j].y * 0x1p-64f);
+                            if (lane < 4) {
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) {
+                                    float2* r = reinterpret_cast<float2*>(wref + 8 * j + cq);
+                                    *r = make_float2(r->x - 64.f, r->y - 64.f);
+                                }
+                            }
+                            __syncwarp();
+                        }
                     }
                 } else {
                     // column pass: rows past rows_pad read +inf and add nothing
@@ -618,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             using M1 = std::integral_constant<bool, true>;
             for (int i = 0; i < a.n_it; ++i) {
                 // only the row pass's last tile can run past the candidate range
-                const bool mask = MODE == 0 && i + 1 == a.n_it;
+                const bool mask = kRowPass<MODE> && i + 1 == a.n_it;
                 if (acc_it & 1u) {
                     if (mask) tile(K1{}, M1{}, i); else tile(K1{}, M0{}, i);
                 } else {
@@ -627,7 +689,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++acc_it;
             }
             if (!(ok = epi_bar_and(ok))) break;
-            if (MODE == 0) {
+            bool redo = false;  // row pass: a row of the unit needs the exact pass
+            if constexpr (kRowPass<MODE>) {
                 // each query row's sum over the warp's blocks (one reference per warp and
                 // column), then a (reference, sum) merge over the four lane quarters in
                 // fixed order -> lse2 of the unit's 256 query rows
@@ -642,7 +705,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     const int col = 2 * lane + c;
-                    red[(slice * 4 + q) * kSliceCols + col] = make_float2(f[c] > 0.f ? -wref[col] : -INFINITY, f[c]);
+                    const float ref = MODE == 0 ? -wnr : -wref[col];
+                    red[(slice * 4 + q) * kSliceCols + col] = make_float2(f[c] > 0.f ? ref : -INFINITY, f[c]);
                 }
                 epi_bar();
                 if (etid < kAccCols) {
@@ -651,10 +715,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float2 m = lse2_merge(lse2_merge(lse2_merge(rc[0], rc[kSliceCols]), rc[2 * kSliceCols]),
                                                 rc[3 * kSliceCols]);
                     const int row = o * T::kFRows + etid;
-                    if (row < a.rows_g)
+                    if (row < a.rows_g) {
                         a.lse2[(int64_t)lg * a.rows_pad + row] = m.y > 0.f ? m.x + __log2f(m.y) : -INFINITY;
-                    else if (row < a.rows_pad)
+                        // every row has a candidate, so its sum is at least 2^-(74 + 16) of the
+                        // reference unless its largest logit lies more than 74 below the warp's
+                        redo = MODE == 0 && !(m.y >= 0x1p-90f && m.y <= 0x1p126f);
+                    } else if (row < a.rows_pad) {
                         a.lse2[(int64_t)lg * a.rows_pad + row] = INFINITY;
+                    }
                 }
             } else {
                 // sum each column over the warp's rows, then over the four lane quarters
@@ -677,7 +745,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (b < a.c1) a.mass[(int64_t)lg * a.n_blocks + b] = sum;
                 }
             }
-            epi_bar();
+            if (MODE == 0) {
+                redo = epi_bar_or(redo);
+                if (etid == 0) a.redo[u] = redo ? 1 : 0;
+            } else {
+                epi_bar();
+            }
         }
     }
 
@@ -739,8 +812,11 @@ PFN_cuTensorMapEncodeTiled_v12000 kvsel_tmap_encoder() {
 }
 
 size_t block_scores_workspace(int L, int Hq, int Hkv, int M, int n_blocks) {
-    const size_t rows_pad = (((size_t)(Hq / Hkv) * M + 3) & ~(size_t)3);
-    return align256((size_t)L * Hkv * rows_pad * sizeof(float)) + align256((size_t)L * Hkv * n_blocks * sizeof(float));
+    const size_t rows_g = (size_t)(Hq / Hkv) * M;
+    const size_t rows_pad = (rows_g + 3) & ~(size_t)3;
+    const size_t units = (size_t)L * Hkv * ((rows_g + kAccCols - 1) / kAccCols);
+    return align256((size_t)L * Hkv * rows_pad * sizeof(float)) + align256((size_t)L * Hkv * n_blocks * sizeof(float)) +
+           align256(units * sizeof(int));
 }
 
 cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index, int L, int Hq, int Hkv, int M, int D,
@@ -758,6 +834,8 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
     const int rows_pad = (rows_g + 3) & ~3;
     w += align256((size_t)LH * rows_pad * sizeof(float));
     float* mass_ws = reinterpret_cast<float*>(w);
+    w += align256((size_t)LH * n_blocks * sizeof(float));
+    int* redo = reinterpret_cast<int*>(w);
     float* mass = R_partial ? R_partial : mass_ws;
 
     if (ncand > 0) {
@@ -773,6 +851,9 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(block_scores_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)smem_bytes<1>());
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(block_scores_tc<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem_bytes<2>());
         if (e != cudaSuccess) return e;
         TcArgs a;
         a.rows_g = rows_g;
@@ -784,6 +865,7 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
         a.lse2 = lse2;
         a.mass = mass;
         a.err = ctx->dev_err;
+        a.redo = redo;
         a.wait_ns = wait_ns;
         a.stuck = stuck;
         // row pass: a unit per 256 query rows, the candidate blocks streamed 128 at a
@@ -793,13 +875,16 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
         a.n_it = (ncand + BM - 1) / BM;
         int grid = a.n_units < ctx->num_sms ? a.n_units : ctx->num_sms;
         block_scores_tc<0><<<grid, kThreads, smem_bytes<0>(), s>>>(q256, i128, a);
+        // exact pass: the units the row pass marked (none on ordinary inputs; then every
+        // CTA only reads its units' marks)
+        a.stuck = 0;  // the test hook and its wait limit apply to the row pass only
+        a.wait_ns = KVSEL_BLOCK_WAIT_NS;
+        block_scores_tc<2><<<grid, kThreads, smem_bytes<2>(), s>>>(q256, i128, a);
         // column pass: a unit per 256 candidate blocks, the query rows streamed 128 at a time
         a.units_per_lg = (ncand + kAccCols - 1) / kAccCols;
         a.n_units = LH * a.units_per_lg;
         a.n_it = (rows_g + BM - 1) / BM;
         grid = a.n_units < ctx->num_sms ? a.n_units : ctx->num_sms;
-        a.stuck = 0;  // the test hook and its wait limit apply to the row pass only
-        a.wait_ns = KVSEL_BLOCK_WAIT_NS;
         block_scores_tc<1><<<grid, kThreads, smem_bytes<1>(), s>>>(i256, q128, a);
     }
     bs_finalize<<<(n_blocks + 255) / 256, 256, 0, s>>>(mass, mass, R, LH, n_blocks, c0, c1,

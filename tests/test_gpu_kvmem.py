@@ -129,6 +129,48 @@ def test_block_scores_large_logits(ctx):
     assert_scores_close(f64(R), oracle.block_scores(bits(q), bits(ix), 400, 2, 2), what="R_b large logits")
 
 
+def test_block_scores_row_far_below_its_warp(ctx):
+    """Query rows whose logits lie far below the other rows of their 64-row slice:
+    one zero row (all logits 0) and one tiny row among rows scaled so that their
+    largest logits reach about 140 (log2).  Under the row pass's shared reference
+    the zero row's terms flush to zero, so only the exact pass over the marked
+    unit gets its total right.  Rows 256..511 form the second unit of each
+    (layer, kv head); the first and third units hold no such row and are not redone."""
+    L, Hq, Hkv, M, nb = 2, 2, 1, 300, 700
+    gen = torch.Generator(device="cuda").manual_seed(77)
+    q = torch.randn((L, Hq, M, 128), generator=gen, device="cuda") * 30.0
+    ix = torch.randn((L, Hkv, nb, 128), generator=gen, device="cuda")
+    q[:, 1, 0] = 0.0                # row 300 of each (l, g): logits exactly 0
+    q[:, 1, 5] *= 1e-3              # row 305: logits near 0
+    q, ix = q.to(torch.bfloat16), ix.to(torch.bfloat16)
+    R = torch.empty(nb, device="cuda")
+    part = torch.empty((L * Hkv, nb), device="cuda")
+    ctx.block_scores(q, ix, nb, 2, 2, R, R_partial=part)
+    ctx.check_device()
+    Rref, pref = oracle.block_scores(bits(q), bits(ix), nb, 2, 2, return_partial=True)
+    assert_scores_close(f64(part), pref, what="R_b partial, rows far below their slice")
+    assert_scores_close(f64(R), Rref, what="R_b, rows far below their slice")
+
+
+def test_block_scores_logit_jump_beyond_headroom(ctx):
+    """A block in the second tile whose logits exceed the first tile's by about 147
+    (log2): the shared reference's terms overflow, the unit is marked, and the
+    exact pass (a reference per row with more headroom) gets every total right."""
+    L, Hq, Hkv, M, nb = 1, 4, 2, 70, 400
+    gen = torch.Generator(device="cuda").manual_seed(78)
+    q = torch.full((L, Hq, M, 128), 3.0, device="cuda") + 0.1 * torch.randn((L, Hq, M, 128), generator=gen,
+                                                                             device="cuda")
+    ix = 0.05 * torch.randn((L, Hkv, nb, 128), generator=gen, device="cuda")
+    ix[:, :, 2 + 200] = 3.0         # candidate 200: second tile of 128
+    q, ix = q.to(torch.bfloat16), ix.to(torch.bfloat16)
+    R = torch.empty(nb, device="cuda")
+    ctx.block_scores(q, ix, nb, 2, 2, R)
+    ctx.check_device()
+    Rref = oracle.block_scores(bits(q), bits(ix), nb, 2, 2)
+    assert Rref[202] > 0.99 * Rref.sum()
+    assert_scores_close(f64(R), Rref, what="R_b, logit jump")
+
+
 @pytest.mark.parametrize("name", ["meank262k", "ws1m"])
 def test_block_scores_full_size_sampled(ctx, name):
     """Full-size R_b: invariants at full size, and sampled (l, g) masses against the oracle."""
