@@ -16,19 +16,20 @@
 //                16x256b loads, so a thread holds 4 blocks x 16 rows, and adds
 //                2^(x - ref) into 16 per-row sums.  ref: one per warp, the
 //                largest logit over the warp's 32 blocks x 64 rows of the unit's
-//                first tile plus 16 (log2) of headroom, moved up by 64 when a
-//                sum passes 2^100.  At the end of the unit the sums are added
-//                across the warp's lanes (butterfly) and merged across the four
-//                lane quarters with their references
+//                first tile plus 16 (log2) of headroom.  At the end of the unit
+//                the sums are added across the warp's lanes (butterfly) and
+//                merged across the four lane quarters with their references
 //                -> lse2[r] = log2 sum_{b in C} 2^(S[r,b] log2e/sqrt(d))
 //                A row whose merged sum is below 2^-90 of its reference (its
-//                largest logit lies more than 74 below the warp's), or not
-//                finite, may have lost terms to underflow or overflowed; the
-//                unit is then marked for
+//                largest logit lies more than 74 below the warp's) may have lost
+//                terms to underflow; a sum that is not finite overflowed (a
+//                logit more than about 134 above the reference's).  Either marks
+//                the unit for
 //   exact pass:  the row pass again on the marked units only (every other unit
 //                is skipped by all roles), with one reference per (warp, row):
 //                the row's largest logit over the warp's blocks of the first
-//                tile plus 64.  It overwrites the unit's lse2.
+//                tile plus 64, moved up by 64 when a sum passes 2^100.  It
+//                overwrites the unit's lse2.
 //   column pass: a unit is (l,g, 256 candidate blocks); tiles of 128 query rows
 //                stream.  A thread holds 4 rows x 16 blocks; it adds
 //                2^(x - lse2[r]) into 16 per-block sums (lse2 loaded one tile
@@ -385,6 +386,14 @@ template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     block_scores_tc(const __grid_constant__ CUtensorMap mapF, const __grid_constant__ CUtensorMap mapS, const TcArgs a) {
     using T = Tiling;
+    if constexpr (MODE == 2) {
+        // The row pass marks no unit on ordinary inputs: a CTA none of whose units is
+        // marked leaves before it sets anything up (one parallel read of the marks).
+        bool any = false;
+        for (int u = blockIdx.x + threadIdx.x * gridDim.x; u < a.n_units; u += blockDim.x * gridDim.x)
+            any |= a.redo[u] != 0;
+        if (!__syncthreads_or(any)) return;
+    }
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* sF = smem;                                   // [kNF][kFBytes]
@@ -595,17 +604,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float2 nr = make_float2(wnr, wnr);
 #pragma unroll
                         for (int j = 0; j < 8; ++j) col_pair_terms(v0, v1, j, sc, nr, cs[j]);
-                        float big = fmaxf(max3(cs[0].x, cs[0].y, cs[1].x), max3(cs[1].y, cs[2].x, cs[2].y));
-                        big = fmaxf(big, max3(cs[3].x, cs[3].y, cs[4].x));
-                        big = fmaxf(big, max3(cs[4].y, cs[5].x, cs[5].y));
-                        big = fmaxf(big, max3(cs[6].x, cs[6].y, fmaxf(cs[7].x, cs[7].y)));
-                        if (__any_sync(0xffffffffu, !(big <= 0x1p100f))) {
-                            // sums far above the reference: move it up by 64 and scale the
-                            // sums down to match
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) cs[j] = make_float2(cs[j].x * 0x1p-64f, cs[j].y * 0x1p-64f);
-                            wnr -= 64.f;
-                        }
                     } else {
                         const int cq = 2 * (lane & 3);  // the thread's first column within each 8
                         if (i == 0) {

@@ -12,9 +12,12 @@
 // Turning a pair (a, b) in fp32 this way leaves an absolute error below
 // 2^-20.5 * rho, rho = |(a, b)|.  That is under half a bf16 ulp of an output r
 // as long as |r| >= 2^-11.5 * rho.  Outputs that nearly cancel (|r| below
-// 2^-11 * max(|a|, |b|), about one pair in 1700) are turned again in fp64 from fp64
-// copies of the same tables and rounded once to bf16, so every output lands
-// within one bf16 ulp of the exactly rotated value rounded to bf16.
+// 2^-11 * max(|a|, |b|), about one pair in 1700) are turned again in
+// double-float arithmetic (pairs of fp32 numbers, about 44 bits) from
+// double-float copies of the same tables and rounded once to bf16, so every
+// output lands within one bf16 ulp of the exactly rotated value rounded to bf16.
+// Double-float rather than fp64: this GPU's fp64 pipe is narrow, and fp64 turns
+// kept it a quarter busy in the scatter.
 #include <cuda_bf16.h>
 
 #include "kvsel_internal.h"
@@ -23,8 +26,14 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-__global__ void rope_tables_kernel(float2* __restrict__ lo, float2* __restrict__ hi, double2* __restrict__ lo64,
-                                   double2* __restrict__ hi64, int D, double base) {
+// fp64 value v as a double-float (hi, lo): hi = v rounded to fp32, lo = the rest rounded to fp32.
+__device__ __forceinline__ float2 split_df(double v) {
+    const float h = (float)v;
+    return make_float2(h, (float)(v - (double)h));
+}
+
+__global__ void rope_tables_kernel(float2* __restrict__ lo, float2* __restrict__ hi, float4* __restrict__ lodf,
+                                   float4* __restrict__ hidf, int D, double base) {
     const int half = D / 2;
     const int64_t total = (int64_t)(KVSEL_ROPE_LO + KVSEL_ROPE_HI) * half;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
@@ -36,12 +45,14 @@ __global__ void rope_tables_kernel(float2* __restrict__ lo, float2* __restrict__
         if (row < KVSEL_ROPE_LO) {
             sincos((double)row * theta, &s, &c);
             lo[row * half + i] = make_float2((float)c, (float)s);
-            lo64[row * half + i] = make_double2(c, s);
+            const float2 cd = split_df(c), sd = split_df(s);
+            lodf[row * half + i] = make_float4(cd.x, cd.y, sd.x, sd.y);
         } else {
             const int64_t r = row - KVSEL_ROPE_LO;
             sincos((double)(r * KVSEL_ROPE_LO) * theta, &s, &c);
             hi[r * half + i] = make_float2((float)c, (float)s);
-            hi64[r * half + i] = make_double2(c, s);
+            const float2 cd = split_df(c), sd = split_df(s);
+            hidf[r * half + i] = make_float4(cd.x, cd.y, sd.x, sd.y);
         }
     }
 }
@@ -54,27 +65,58 @@ __device__ __forceinline__ float2 rope_cs(const float2* __restrict__ tlo, const 
     return make_float2(fmaf(a.x, b.x, -a.y * b.y), fmaf(a.y, b.x, a.x * b.y));
 }
 
-// The same in fp64, from the fp64 tables.
-__device__ __forceinline__ double2 rope_cs64(const double2* __restrict__ tlo, const double2* __restrict__ thi,
-                                             int half, int p, int i) {
-    const double2 a = __ldg(thi + (int64_t)(p >> KVSEL_ROPE_LO_BITS) * half + i);
-    const double2 b = __ldg(tlo + (int64_t)(p & (KVSEL_ROPE_LO - 1)) * half + i);
-    return make_double2(fma(a.x, b.x, -a.y * b.y), fma(a.y, b.x, a.x * b.y));
+// Double-float arithmetic: a value held as the unevaluated sum hi + lo of two
+// fp32 numbers.  Products take the exact remainder of the leading product from
+// an fma; sums take the exact rounding error of the leading sum (Knuth's
+// two-sum), so each operation keeps about 44 bits where fp32 keeps 24.  The
+// explicitly rounded intrinsics keep the compiler from fusing a product into a
+// later sum, which would break the error terms.
+struct DF {
+    float hi, lo;
+};
+__device__ __forceinline__ DF df_mul(DF x, DF y) {
+    const float p = __fmul_rn(x.hi, y.hi);
+    float e = fmaf(x.hi, y.hi, -p);
+    e = fmaf(x.hi, y.lo, e);
+    e = fmaf(x.lo, y.hi, e);
+    return {p, e};
 }
+__device__ __forceinline__ DF df_mul(float x, DF y) {
+    const float p = __fmul_rn(x, y.hi);
+    float e = fmaf(x, y.hi, -p);
+    e = fmaf(x, y.lo, e);
+    return {p, e};
+}
+__device__ __forceinline__ DF df_add(DF x, DF y) {
+    const float s = __fadd_rn(x.hi, y.hi);
+    const float bb = __fsub_rn(s, x.hi);
+    const float err = __fadd_rn(__fsub_rn(x.hi, __fsub_rn(s, bb)), __fsub_rn(y.hi, bb));
+    const float lo = __fadd_rn(err, __fadd_rn(x.lo, y.lo));
+    const float h = __fadd_rn(s, lo);
+    return {h, __fsub_rn(lo, __fsub_rn(h, s))};
+}
+__device__ __forceinline__ DF df_neg(DF x) { return {-x.hi, -x.lo}; }
 
-// fp64 turn of one rotation pair, elements ia and ib of a bf16 row read again from
-// memory (the row is not overwritten before this runs), at position p and
-// frequency f (sine negated when neg); each output rounded once to bf16 and
-// returned as the exactly representable fp32 value.  Out of line: it runs for
-// about one pair in 1700, and an inlined copy would be predicated into every pass.
-__device__ __noinline__ float2 turn_pair_fp64(const __nv_bfloat16* __restrict__ row, int ia, int ib,
-                                              const double2* __restrict__ tlo64, const double2* __restrict__ thi64,
-                                              int half, int p, int f, int neg) {
-    const double a = __bfloat162float(row[ia]), b = __bfloat162float(row[ib]);
-    double2 c = rope_cs64(tlo64, thi64, half, p, f);
-    if (neg) c.y = -c.y;
-    return make_float2(__bfloat162float(__double2bfloat16(fma(a, c.x, -b * c.y))),
-                       __bfloat162float(__double2bfloat16(fma(b, c.x, a * c.y))));
+// Double-float turn of one rotation pair, elements ia and ib of a bf16 row read
+// again from memory (the row is not overwritten before this runs), at position
+// p and frequency f (sine negated when neg): cos and sin of p * theta_f by angle
+// addition of the double-float table entries, then the rotation, each output
+// rounded once to bf16 and returned as the exactly representable fp32 value.
+// Out of line: it runs for about one pair in 1700, and an inlined copy would be
+// predicated into every pass.
+__device__ __noinline__ float2 turn_pair_df(const __nv_bfloat16* __restrict__ row, int ia, int ib,
+                                            const float4* __restrict__ tlo, const float4* __restrict__ thi,
+                                            int half, int p, int f, int neg) {
+    const float a = __bfloat162float(row[ia]), b = __bfloat162float(row[ib]);
+    const float4 u = __ldg(thi + (int64_t)(p >> KVSEL_ROPE_LO_BITS) * half + f);
+    const float4 v = __ldg(tlo + (int64_t)(p & (KVSEL_ROPE_LO - 1)) * half + f);
+    const DF cu = {u.x, u.y}, su = {u.z, u.w}, cv = {v.x, v.y}, sv = {v.z, v.w};
+    const DF c = df_add(df_mul(cu, cv), df_neg(df_mul(su, sv)));
+    DF s = df_add(df_mul(su, cv), df_mul(cu, sv));
+    if (neg) s = df_neg(s);
+    const DF ra = df_add(df_mul(a, c), df_neg(df_mul(b, s)));
+    const DF rb = df_add(df_mul(b, c), df_mul(a, s));
+    return make_float2(__bfloat162float(__float2bfloat16_rn(ra.hi)), __bfloat162float(__float2bfloat16_rn(rb.hi)));
 }
 
 // (cos, sin) tables in shared memory, one row of D/2 frequencies per position.
@@ -100,11 +142,11 @@ __device__ __forceinline__ void mark_near(unsigned& near, int k, float a, float 
     near |= (fminf(fabsf(ra), fabsf(rb)) < fmaxf(fabsf(a), fabsf(b)) * 0x1p-11f ? 1u : 0u) << k;
 }
 
-// Turns again in fp64 the pairs marked in `near`, reading their inputs from `row`.
+// Turns again in double-float arithmetic the pairs marked in `near`, reading their inputs from `row`.
 template <bool NEOX>
 __device__ __forceinline__ void fix_near(unsigned near, float (&xa)[8], float (&xb)[8], int f0, int fa, int fb,
                                          const __nv_bfloat16* __restrict__ row, int ca, int cb,
-                                         const double2* __restrict__ tlo64, const double2* __restrict__ thi64,
+                                         const float4* __restrict__ tlodf, const float4* __restrict__ thidf,
                                          int half, int p, bool neg) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -114,7 +156,7 @@ __device__ __forceinline__ void fix_near(unsigned near, float (&xa)[8], float (&
             const int ia = NEOX ? 8 * ca + k : (k < 4 ? 8 * ca + 2 * k : 8 * cb + 2 * (k - 4));
             const int ib = NEOX ? 8 * cb + k : ia + 1;
             const int f = NEOX ? f0 + k : (k < 4 ? fa + k : fb + k - 4);
-            const float2 r = turn_pair_fp64(row, ia, ib, tlo64, thi64, half, p, f, neg ? 1 : 0);
+            const float2 r = turn_pair_df(row, ia, ib, tlodf, thidf, half, p, f, neg ? 1 : 0);
             a = r.x;
             b = r.y;
         }
@@ -126,11 +168,11 @@ __device__ __forceinline__ void fix_near(unsigned near, float (&xa)[8], float (&
 // k is (xa[k], xb[k]) at frequency f0 + k (f0 a multiple of 8), turned two pairs
 // at a time in packed fp32x2; interleaved: pairs (xa[2k], xa[2k+1]) at fa + k and
 // (xb[2k], xb[2k+1]) at fb + k.  A pair with an output below 2^-11 of its larger
-// input is turned again in fp64.
+// input is turned again in double-float arithmetic.
 template <bool NEOX>
 __device__ __forceinline__ void turn_chunks(float (&xa)[8], float (&xb)[8], const float4* __restrict__ tq, int f0,
                                             int fa, int fb, const __nv_bfloat16* __restrict__ row, int ca, int cb,
-                                            const double2* __restrict__ tlo64, const double2* __restrict__ thi64,
+                                            const float4* __restrict__ tlodf, const float4* __restrict__ thidf,
                                             int half, int p, bool neg) {
     unsigned near = 0;
     if (NEOX) {
@@ -163,7 +205,7 @@ __device__ __forceinline__ void turn_chunks(float (&xa)[8], float (&xb)[8], cons
         }
     }
     if (__any_sync(__activemask(), near != 0))
-        fix_near<NEOX>(near, xa, xb, f0, fa, fb, row, ca, cb, tlo64, thi64, half, p, neg);
+        fix_near<NEOX>(near, xa, xb, f0, fa, fb, row, ca, cb, tlodf, thidf, half, p, neg);
 }
 
 __device__ __forceinline__ void unpack8(uint4 raw, float (&x)[8]) {
@@ -300,7 +342,7 @@ __global__ void __launch_bounds__(256, KVSEL_REROPE_MINB) rerope_kernel(const __
                                                      const int32_t* __restrict__ dst_page,
                                                      const int32_t* __restrict__ dst_pos0, const int32_t* n_dev,
                                                      int L, int Hkv, int D, int page, const float2* tlo,
-                                                     const float2* thi, const double2* tlo64, const double2* thi64,
+                                                     const float2* thi, const float4* tlodf, const float4* thidf,
                                                      int style, __nv_bfloat16* __restrict__ pool,
                                                      const __nv_bfloat16* __restrict__ v_src,
                                                      __nv_bfloat16* __restrict__ v_pool, int P, unsigned* dev_err) {
@@ -377,9 +419,9 @@ __global__ void __launch_bounds__(256, KVSEL_REROPE_MINB) rerope_kernel(const __
         unpack8(wb, xb);
         const float4* cst = cs + t * qrow;
         if (style == KVSEL_ROPE_NEOX)
-            turn_chunks<true>(xa, xb, cst, 8 * cp, 0, 0, srow, ca, cb, tlo64, thi64, half, p0 + t, false);
+            turn_chunks<true>(xa, xb, cst, 8 * cp, 0, 0, srow, ca, cb, tlodf, thidf, half, p0 + t, false);
         else
-            turn_chunks<false>(xa, xb, cst, 0, 4 * ca, 4 * cb, srow, ca, cb, tlo64, thi64, half, p0 + t, false);
+            turn_chunks<false>(xa, xb, cst, 0, 4 * ca, 4 * cb, srow, ca, cb, tlodf, thidf, half, p0 + t, false);
         __stcs(reinterpret_cast<uint4*>(drow + 8 * ca), pack8(xa));
         __stcs(reinterpret_cast<uint4*>(drow + 8 * cb), pack8(xb));
         if constexpr (WITH_V) {
@@ -406,7 +448,7 @@ __global__ void __launch_bounds__(256, KVSEL_REROPE_MINB) shift_kernel(__nv_bflo
                                                     const int32_t* __restrict__ pages,
                                                     const int32_t* __restrict__ shifts, const int32_t* n_dev, int L,
                                                     int Hkv, int D, int page, const float2* tlo, const float2* thi,
-                                                    const double2* tlo64, const double2* thi64, int style,
+                                                    const float4* tlodf, const float4* thidf, int style,
                                                     unsigned* dev_err) {
     __shared__ float4 cs[16 * kQuadsPerGroup];  // one table row (D <= 256)
     if (n_dev && (int)blockIdx.x >= __ldg(n_dev)) return;
@@ -456,9 +498,9 @@ __global__ void __launch_bounds__(256, KVSEL_REROPE_MINB) shift_kernel(__nv_bflo
         unpack8(wa, xa);
         unpack8(wb, xb);
         if (style == KVSEL_ROPE_NEOX)
-            turn_chunks<true>(xa, xb, cs, 8 * cp, 0, 0, row, ca, cb, tlo64, thi64, half, mag, sh < 0);
+            turn_chunks<true>(xa, xb, cs, 8 * cp, 0, 0, row, ca, cb, tlodf, thidf, half, mag, sh < 0);
         else
-            turn_chunks<false>(xa, xb, cs, 0, 4 * ca, 4 * cb, row, ca, cb, tlo64, thi64, half, mag, sh < 0);
+            turn_chunks<false>(xa, xb, cs, 0, 4 * ca, 4 * cb, row, ca, cb, tlodf, thidf, half, mag, sh < 0);
         *reinterpret_cast<uint4*>(row + 8 * ca) = pack8(xa);
         *reinterpret_cast<uint4*>(row + 8 * cb) = pack8(xb);
         if (!more) break;
@@ -472,12 +514,12 @@ __global__ void __launch_bounds__(256, KVSEL_REROPE_MINB) shift_kernel(__nv_bflo
 
 }  // namespace
 
-cudaError_t launch_rope_tables(float2* lo, float2* hi, double2* lo64, double2* hi64, int D, double base,
+cudaError_t launch_rope_tables(float2* lo, float2* hi, float4* lodf, float4* hidf, int D, double base,
                                cudaStream_t s) {
     const int64_t total = (int64_t)(KVSEL_ROPE_LO + KVSEL_ROPE_HI) * (D / 2);
     int grid = (int)((total + 255) / 256);
     if (grid > 8192) grid = 8192;
-    rope_tables_kernel<<<grid, 256, 0, s>>>(lo, hi, lo64, hi64, D, base);
+    rope_tables_kernel<<<grid, 256, 0, s>>>(lo, hi, lodf, hidf, D, base);
     return cudaGetLastError();
 }
 
@@ -505,7 +547,7 @@ cudaError_t launch_rerope(const void* k_src, int64_t sls, int64_t shs, int src_t
         if (e != cudaSuccess) return e;
     }
     kern<<<grid, 256, smem, s>>>(static_cast<const __nv_bfloat16*>(k_src), sls, shs, src_tokens, src_block, dst_page,
-                                 dst_pos0, n_dev, L, Hkv, D, page, tab->lo, tab->hi, tab->lo64, tab->hi64, rope_style,
+                                 dst_pos0, n_dev, L, Hkv, D, page, tab->lo, tab->hi, tab->lodf, tab->hidf, rope_style,
                                  static_cast<__nv_bfloat16*>(pool), static_cast<const __nv_bfloat16*>(v_src),
                                  static_cast<__nv_bfloat16*>(v_pool), P, dev_err);
     return cudaGetLastError();
@@ -516,6 +558,6 @@ cudaError_t launch_shift(void* pool, int P, const int32_t* pages, const int32_t*
                          unsigned* dev_err, cudaStream_t s) {
     const dim3 grid((unsigned)n, (unsigned)((L + kLayerGroup - 1) / kLayerGroup));
     shift_kernel<<<grid, 256, 0, s>>>(static_cast<__nv_bfloat16*>(pool), P, pages, shifts, n_dev, L, Hkv, D, page,
-                                      tab->lo, tab->hi, tab->lo64, tab->hi64, rope_style, dev_err);
+                                      tab->lo, tab->hi, tab->lodf, tab->hidf, rope_style, dev_err);
     return cudaGetLastError();
 }

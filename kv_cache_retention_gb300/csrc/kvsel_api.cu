@@ -118,22 +118,22 @@ const kvsel_ctx::RopeTab* kvsel_rope_tables(kvsel_ctx* ctx, int D, double base, 
     auto release = [&t]() {
         cudaFree(t.lo);
         cudaFree(t.hi);
-        cudaFree(t.lo64);
-        cudaFree(t.hi64);
+        cudaFree(t.lodf);
+        cudaFree(t.hidf);
         t.lo = t.hi = nullptr;
-        t.lo64 = t.hi64 = nullptr;
+        t.lodf = t.hidf = nullptr;
         t.D = 0;
     };
     if (t.lo) release();
     size_t half = (size_t)D / 2;
     if (cudaMalloc(&t.lo, sizeof(float2) * half * KVSEL_ROPE_LO) != cudaSuccess ||
         cudaMalloc(&t.hi, sizeof(float2) * half * KVSEL_ROPE_HI) != cudaSuccess ||
-        cudaMalloc(&t.lo64, sizeof(double2) * half * KVSEL_ROPE_LO) != cudaSuccess ||
-        cudaMalloc(&t.hi64, sizeof(double2) * half * KVSEL_ROPE_HI) != cudaSuccess) {
+        cudaMalloc(&t.lodf, sizeof(float4) * half * KVSEL_ROPE_LO) != cudaSuccess ||
+        cudaMalloc(&t.hidf, sizeof(float4) * half * KVSEL_ROPE_HI) != cudaSuccess) {
         release();
         return nullptr;
     }
-    if (launch_rope_tables(t.lo, t.hi, t.lo64, t.hi64, D, base, s) != cudaSuccess) {
+    if (launch_rope_tables(t.lo, t.hi, t.lodf, t.hidf, D, base, s) != cudaSuccess) {
         release();
         return nullptr;
     }
@@ -177,8 +177,8 @@ int kvsel_ctx_destroy(kvsel_ctx* ctx) {
     for (int i = 0; i < ctx->n_rope; ++i) {
         cudaFree(ctx->rope[i].lo);
         cudaFree(ctx->rope[i].hi);
-        cudaFree(ctx->rope[i].lo64);
-        cudaFree(ctx->rope[i].hi64);
+        cudaFree(ctx->rope[i].lodf);
+        cudaFree(ctx->rope[i].hidf);
     }
     delete ctx;
     return KVSEL_OK;

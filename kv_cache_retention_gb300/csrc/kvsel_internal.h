@@ -21,14 +21,14 @@ struct kvsel_ctx {
     // Device error word: kernels OR kvsel_devcheck bits into it on bad data.
     unsigned* dev_err = nullptr;
     // RoPE angle tables, one per (D, base): split-position cos/sin pairs, in
-    // fp32 for the fast path and in fp64 for outputs that nearly cancel.
+    // fp32 for the fast path and as double-floats for outputs that nearly cancel.
     struct RopeTab {
         int D = 0;
         double base = 0.0;
         float2* lo = nullptr;     // [KVSEL_ROPE_LO][D/2]: angle lo * theta_i
         float2* hi = nullptr;     // [KVSEL_ROPE_HI][D/2]: angle hi * LO * theta_i
-        double2* lo64 = nullptr;  // the same angles in fp64
-        double2* hi64 = nullptr;
+        float4* lodf = nullptr;   // the same angles as double-floats (cos hi, cos lo, sin hi, sin lo)
+        float4* hidf = nullptr;
     };
     RopeTab rope[8];
     int n_rope = 0;
@@ -140,7 +140,7 @@ cudaError_t launch_topk(const float* score, int N, int pi, int q_s, int q_e, int
 cudaError_t launch_redirect(const int32_t* slot_in, const uint8_t* keep, int N, int32_t dead,
                             int32_t* slot_out, cudaStream_t s);
 
-cudaError_t launch_rope_tables(float2* lo, float2* hi, double2* lo64, double2* hi64, int D, double base,
+cudaError_t launch_rope_tables(float2* lo, float2* hi, float4* lodf, float4* hidf, int D, double base,
                                cudaStream_t s);
 
 cudaError_t launch_meank(const void* k_src, int L, int Hkv, int T, int D, int block, int first_block,

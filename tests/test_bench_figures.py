@@ -35,3 +35,8 @@ def test_launches_and_traffic():
     assert sum(bench.LAUNCHES.values()) == 13
     assert bench.LAUNCHES["block_scores"] == 4 and bench.LAUNCHES["rule_scores"] == 3
     assert abs(bench.PROFILED_TRAFFIC["block_scores"] - 11.445e9) < 0.01e9
+
+
+def test_block_scores_ceiling():
+    # two tensor-core passes over the same logits against one counted contraction
+    assert bench.ALGORITHMIC_CEILING == {"block_scores": 0.5}

@@ -152,16 +152,18 @@ def test_block_scores_row_far_below_its_warp(ctx):
     assert_scores_close(f64(R), Rref, what="R_b, rows far below their slice")
 
 
-def test_block_scores_logit_jump_beyond_headroom(ctx):
-    """A block in the second tile whose logits exceed the first tile's by about 147
-    (log2): the shared reference's terms overflow, the unit is marked, and the
-    exact pass (a reference per row with more headroom) gets every total right."""
+@pytest.mark.parametrize("v", [2.6, 3.0])
+def test_block_scores_logit_jump_beyond_headroom(ctx, v):
+    """A block in the second tile whose logits exceed the first tile's by about 110
+    (v = 2.6) or 147 (v = 3.0) in log2 units.  At 110 the row pass's sums grow to about
+    2^100 and stay finite; at 147 its terms overflow, the unit is marked, and the exact
+    pass (a reference per row with more headroom) gets every total right."""
     L, Hq, Hkv, M, nb = 1, 4, 2, 70, 400
     gen = torch.Generator(device="cuda").manual_seed(78)
-    q = torch.full((L, Hq, M, 128), 3.0, device="cuda") + 0.1 * torch.randn((L, Hq, M, 128), generator=gen,
-                                                                             device="cuda")
+    q = torch.full((L, Hq, M, 128), v, device="cuda") + 0.1 * torch.randn((L, Hq, M, 128), generator=gen,
+                                                                           device="cuda")
     ix = 0.05 * torch.randn((L, Hkv, nb, 128), generator=gen, device="cuda")
-    ix[:, :, 2 + 200] = 3.0         # candidate 200: second tile of 128
+    ix[:, :, 2 + 200] = v           # candidate 200: second tile of 128
     q, ix = q.to(torch.bfloat16), ix.to(torch.bfloat16)
     R = torch.empty(nb, device="cuda")
     ctx.block_scores(q, ix, nb, 2, 2, R)
