@@ -146,10 +146,11 @@ def test_rule_scores_parity_full_size(ctx, name):
     ctx.check_device()
 
 
+@pytest.mark.parametrize("Hq", [10, 8])  # G = 5 and G = 4
 @pytest.mark.parametrize("N,pi,qs,qe", [(1000, 3, 950, 1000), (129, 0, 129, 129), (64, 10, 20, 30),
                                         (1, 0, 1, 1), (300, 300, 300, 300), (77, 76, 0, 1)])
-def test_rule_scores_ragged_and_degenerate(ctx, N, pi, qs, qe):
-    w = synth.scaled(synth.TOKEN["8b"], L=2, Hq=10, Hkv=2, N=N, turns=1, R=4, page=0)
+def test_rule_scores_ragged_and_degenerate(ctx, N, pi, qs, qe, Hq):
+    w = synth.scaled(synth.TOKEN["8b"], L=2, Hq=Hq, Hkv=2, N=N, turns=1, R=4, page=0)
     inp = synth.token_inputs(w, "cuda")
     g = torch.Generator(device="cuda").manual_seed(N)
     M32 = torch.nn.functional.normalize(torch.randn((w.L, w.Hq, w.D), generator=g, device="cuda"), dim=-1)
@@ -177,9 +178,10 @@ def test_rule_scores_shapes(ctx, G, Hkv, D):
     assert_scores_close(f64(rule), ref, what=f"rule_j G={G} Hkv={Hkv} D={D}")
 
 
-def test_rule_scores_strided_pool_16B_aligned(ctx):
+@pytest.mark.parametrize("D", [64, 128])
+def test_rule_scores_strided_pool_16B_aligned(ctx, D):
     """slot_stride with 16-byte (not 32-byte) alignment takes the split-load path."""
-    L, Hq, Hkv, D, N = 2, 4, 2, 64, 200
+    L, Hq, Hkv, N = 2, 4, 2, 200
     stride = Hkv * D + 8  # 16 bytes of padding per slot in bf16
     gen = torch.Generator(device="cuda").manual_seed(3)
     flat = torch.randn((L, N, stride), generator=gen, device="cuda").to(torch.bfloat16)
@@ -192,8 +194,9 @@ def test_rule_scores_strided_pool_16B_aligned(ctx):
     assert_scores_close(f64(rule), ref, what="rule_j strided")
 
 
-def test_rule_scores_bad_slot_sets_device_error(ctx):
-    L, Hq, Hkv, D, N = 1, 2, 1, 64, 40
+@pytest.mark.parametrize("Hq,D", [(2, 64), (4, 128)])
+def test_rule_scores_bad_slot_sets_device_error(ctx, Hq, D):
+    L, Hkv, N = 1, 1, 40
     pool = torch.zeros((L, N, Hkv, D), device="cuda", dtype=torch.bfloat16)
     smap = torch.arange(N, device="cuda", dtype=torch.int32)
     smap[17] = N + 5  # outside the pool: read as a zero row and flagged
