@@ -40,19 +40,24 @@
 // Every pass completes each unit's results inside one CTA: no atomics, no
 // partial results in global memory.
 //
-// Kernel structure (one persistent CTA per SM, 608 threads):
+// Kernel structure (one persistent CTA per SM, 640 threads = 5 warpgroups):
 //   warp 0      TMA producer: the unit's fixed tile (64 KB), then the streamed
 //               tiles through a ring of 4 x 32 KB (128-byte swizzled, K-major,
 //               no multicast)
-//   warps 1, 18 allocate 512 TMEM columns (warp 1); lane 0 of each issues
+//   warps 1, 2  allocate 512 TMEM columns (warp 1); lane 0 of each issues
 //               tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M=128 N=256 K=16,
 //               8 per tile) for alternate tiles, each into its own 256-column
 //               accumulator, and commits to mbarriers that free the smem stage
 //               and hand the accumulator on
-//   warps 2-17  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
+//   warp 3      idle (completes the first warpgroup)
+//   warps 4-19  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
 //               32*(w%4)..+31; four column slices of 64), release, a
 //               non-blocking probe of the next tile's accumulator, exp2 on the
 //               MUFU, packed fp32 arithmetic
+// The first warpgroup gives registers back (setmaxnreg.dec to kRegsCtl) and the
+// four epilogue warpgroups take them (setmaxnreg.inc to kRegsEpi): the launch
+// allows 96 per thread, the epilogue's 64 accumulator values, 16 sums and
+// addressing need more.
 // Every mbarrier wait is bounded (1 s of globaltimer); on a timeout the CTA
 // flags KVSEL_ERR_TIMEOUT in the device error word, drains its own copies and
 // MMAs, frees TMEM and returns.
@@ -102,9 +107,21 @@ constexpr int kEpiWarps = 16;                   // 4 TMEM lane quarters x kSlice
 constexpr int kSlices = kEpiWarps / 4;
 constexpr int kSliceCols = kAccCols / kSlices;  // accumulator columns per epilogue thread and tile
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kIssuer2 = 2 + kEpiWarps;         // the second MMA-issuing warp
+constexpr int kIssuer2 = 2;                     // the second MMA-issuing warp
+constexpr int kEpi0 = 4;                        // first epilogue warp (warps 0-3: one warpgroup)
 static_assert(kNAcc == 2, "the two MMA issuers own one accumulator each");
-constexpr int kThreads = 64 + kEpiThreads + 32;
+static_assert(kEpiWarps == 16 && kEpi0 == 4, "one first warpgroup and four epilogue warpgroups");
+constexpr int kThreads = 128 + kEpiThreads;
+// Registers per thread after the first warpgroup's setmaxnreg.dec / the epilogue's .inc.
+// Each SM sub-partition holds one first-group warp and four epilogue warps, so the
+// split fits the launch's registers iff kRegsCtl + 4 * kRegsEpi <= 5 * (registers at
+// launch); an .inc beyond that would wait forever.  Here it fits exactly
+// (64 + 4 * 104 = 5 * 96), and the launcher checks the compiled kernel's count
+// before any launch.
+constexpr int kRegsCtl = 64, kRegsEpi = 104;
+constexpr int kRegsLaunch = 96;  // registers per thread the launch of 640 threads allows
+static_assert(kRegsCtl + 4 * kRegsEpi <= 5 * kRegsLaunch && kRegsLaunch * kThreads <= 65536, "register split");
+static_assert(kRegsCtl % 8 == 0 && kRegsEpi % 8 == 0 && kRegsCtl >= 24 && kRegsEpi <= 256, "setmaxnreg values");
 constexpr uint64_t kWaitNs = 1000000000ull;     // 1 s per wait
 #ifndef KVSEL_SUSPEND_NS
 #define KVSEL_SUSPEND_NS 20000
@@ -203,9 +220,9 @@ __device__ __forceinline__ uint64_t gtimer() {
 
 // Bounded wait for the phase of parity `parity`, giving up after limit_ns.
 // Returns false if this or another role gave up (the CTA is then draining).
-// The first try_wait (which may park the thread until the phase completes) is
-// inlined; the retry loop with its time limit is not.
-__device__ __noinline__ bool wait_phase_retry(uint64_t* b, uint32_t parity, volatile int* abort_flag, unsigned* err,
+// Everything is inlined: a called function would be compiled for one register
+// budget, and the kernel's warpgroups run under two (setmaxnreg).
+__device__ __forceinline__ bool wait_phase_retry(uint64_t* b, uint32_t parity, volatile int* abort_flag, unsigned* err,
                                              uint64_t limit_ns) {
     const uint64_t t0 = gtimer();
     for (uint32_t i = 1;; ++i) {
@@ -227,7 +244,7 @@ __device__ __forceinline__ bool wait_phase(uint64_t* b, uint32_t parity, volatil
 
 // Bounded wait that ignores the abort flag: used to drain this thread's own
 // copies and MMAs before the CTA frees TMEM and exits.
-__device__ __noinline__ void drain_phase(uint64_t* b, uint32_t parity) {
+__device__ __forceinline__ void drain_phase(uint64_t* b, uint32_t parity) {
     const uint64_t t0 = gtimer();
     while (!mbar_test(b, parity) && gtimer() - t0 < kWaitNs) {
     }
@@ -430,6 +447,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = t.tmem_base;
 
+    // The two register budgets: each branch below runs to the kernel's end on its own
+    // (no code is shared after a setmaxnreg).
+    if (warp < kEpi0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
@@ -515,9 +536,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(&t.mma_done);
             drain_phase(&t.mma_done, 0);
         }
-    } else if (warp < kIssuer2) {
+    }
+    // first warpgroup's end: TMEM is released once every MMA has completed (the MMA
+    // lanes drained above) and the epilogue has passed the same barrier
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                     : "memory");
+    }
+    return;
+    }
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
+    {
         // ------------------------------ epilogue ------------------------------
-        const int ew = warp - 2;                 // 0 .. kEpiWarps-1
+        const int ew = warp - kEpi0;             // 0 .. kEpiWarps-1
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
         const int slice = ew >> 2;               // column slice
         const int r_local = q * 32 + lane;       // this lane's TMEM lane (column pass: a query row of the tile)
@@ -752,14 +786,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    // all roles: TMEM is released once every MMA has completed (MMA lane drained above)
+    // epilogue's end: the barrier the first warpgroup waits on before it frees TMEM
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) {
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
-                     : "memory");
-    }
 }
 
 // R[b] = sum_lg mass[lg][b] / (L*Hq) on C; zero outside C (also in mass).
@@ -844,6 +874,14 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
         if (!make_map(&q256, q, q_rows, kAccCols) || !make_map(&q128, q, q_rows, BM) ||
             !make_map(&i256, index, i_rows, kAccCols) || !make_map(&i128, index, i_rows, BM))
             return cudaErrorInvalidValue;
+        // the register split needs every pass compiled to exactly the launch's count
+        for (const void* f : {(const void*)block_scores_tc<0>, (const void*)block_scores_tc<1>,
+                              (const void*)block_scores_tc<2>}) {
+            cudaFuncAttributes fa;
+            const cudaError_t ea = cudaFuncGetAttributes(&fa, f);
+            if (ea != cudaSuccess) return ea;
+            if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
+        }
         cudaError_t e = cudaFuncSetAttribute(block_scores_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem_bytes<0>());
         if (e == cudaSuccess)
