@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(256) meank_kernel(const __nv_bfloat16* __restr
 // NeoX halves (i, i + D/2) of 8 frequencies, or two chunks of interleaved
 // pairs -- so no data crosses lanes.  Rows r = t*Hkv + g are contiguous in the
 // destination page; each source row is contiguous too.
-constexpr int kLayerGroup = 8;
+constexpr int kLayerGroup = 16;
 #ifndef KVSEL_REROPE_MINB
 #define KVSEL_REROPE_MINB 4  // resident CTAs per SM the register budget allows (64 registers)
 #endif
@@ -363,17 +363,11 @@ __global__ void __launch_bounds__(256, KVSEL_REROPE_MINB) rerope_kernel(const __
     const int half = D / 2;
     const int PR = D >> 4;              // chunk pairs per row = frequency groups of eight
     const int qrow = PR * kQuadsPerGroup;  // float4 per table row
-    for (int idx = threadIdx.x; idx < page * half; idx += blockDim.x) {
-        const float2 c = rope_cs(tlo, thi, half, p0 + idx / half, idx % half);
-        cs_put(cs + (idx / half) * qrow, idx % half, c.x, c.y);
-    }
-    __syncthreads();
     // A thread keeps one chunk pair cp of rows r0, r0 + dr, ... of every layer
     // (blockDim is a multiple of PR), and loads its next row's chunks before it
     // turns the current ones.
     const int rows = page * Hkv;
     const int cp = threadIdx.x & (PR - 1), r0 = threadIdx.x / PR;
-    if (r0 >= rows) return;  // no barrier follows
     const int dr = blockDim.x / PR, dt = dr / Hkv, dg = dr % Hkv;
     const int t0 = r0 / Hkv, g0 = r0 % Hkv;
     // NeoX: chunk cp holds dims 8cp.. (first half), chunk cp + PR holds dims 8cp + D/2..
@@ -384,8 +378,18 @@ __global__ void __launch_bounds__(256, KVSEL_REROPE_MINB) rerope_kernel(const __
     };
     int l = l0, r = r0, t = t0, g = g0;
     const __nv_bfloat16* srow = src_row(l, t, g);
-    uint4 wa = __ldcs(reinterpret_cast<const uint4*>(srow + 8 * ca));
-    uint4 wb = __ldcs(reinterpret_cast<const uint4*>(srow + 8 * cb));
+    // the first row's chunks are on their way while the table is built
+    uint4 wa = make_uint4(0, 0, 0, 0), wb = wa;
+    if (r0 < rows) {
+        wa = __ldcs(reinterpret_cast<const uint4*>(srow + 8 * ca));
+        wb = __ldcs(reinterpret_cast<const uint4*>(srow + 8 * cb));
+    }
+    for (int idx = threadIdx.x; idx < page * half; idx += blockDim.x) {
+        const float2 c = rope_cs(tlo, thi, half, p0 + idx / half, idx % half);
+        cs_put(cs + (idx / half) * qrow, idx % half, c.x, c.y);
+    }
+    __syncthreads();
+    if (r0 >= rows) return;  // no barrier follows
     for (;;) {
         int ln = l, rn = r + dr, tn = t + dt, gn = g + dg;
         if (gn >= Hkv) {
