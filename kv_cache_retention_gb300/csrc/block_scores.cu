@@ -19,7 +19,8 @@
 //                first tile plus 16 (log2) of headroom.  At the end of the unit
 //                the sums are added across the warp's lanes (butterfly) and
 //                merged across the four lane quarters with their references
-//                -> lse2[r] = log2 sum_{b in C} 2^(S[r,b] log2e/sqrt(d))
+//                -> lse2[r] = log2 sum_{b in C} 2^(S[r,b] log2e/sqrt(d)), stored
+//                negated, the row range padded to whole column-pass tiles with -inf
 //                A row whose merged sum is below 2^-90 of its reference (its
 //                largest logit lies more than 74 below the warp's) may have lost
 //                terms to underflow; a sum that is not finite overflowed (a
@@ -32,8 +33,9 @@
 //                overwrites the unit's lse2.
 //   column pass: a unit is (l,g, 256 candidate blocks); tiles of 128 query rows
 //                stream.  A thread holds 4 rows x 16 blocks; it adds
-//                2^(x - lse2[r]) into 16 per-block sums (lse2 loaded one tile
-//                ahead, one lane per row, handed on by shuffles).  At the end of
+//                2^(x - lse2[r]) into 16 per-block sums (-lse2 loaded one tile
+//                ahead, one lane per row, handed on by shuffles, and used as the
+//                fma's addend as it is; no bounds test, the padding reads -inf).  At the end of
 //                the unit the sums are added across lanes (butterfly) and across
 //                the four lane quarters -> mass[lg][b], complete per CTA
 //   finalize:    R[b] = sum_lg mass[lg][b] / (L*Hq), in fixed (l,g) order.
@@ -138,11 +140,11 @@ struct TcArgs {
     int units_per_lg;
     int n_it;          // streamed tiles per unit
     int rows_g;        // G*M
-    int rows_pad;      // rows_g rounded up to a multiple of 4 (row stride of lse2)
+    int rows_pad;      // rows_g rounded up to a multiple of 128 (row stride of nlse2)
     int c0, c1;        // candidate blocks [c0, c1)
     int Bcap;
     int n_blocks;
-    float* lse2;       // [L*Hkv][rows_pad]; pad entries hold +inf
+    float* nlse2;      // [L*Hkv][rows_pad]: -lse2 of each query row; pad entries hold -inf
     float* mass;       // [L*Hkv][n_blocks]
     unsigned* err;
     int* redo;         // [row-pass units]: set by the row pass where the exact pass must redo the unit
@@ -338,8 +340,8 @@ __device__ __forceinline__ bool epi_bar_or(bool v) {
 
 // Column pass: adds 2^(v*scale - lse2) of one TMEM lane of a 16x256b load
 // (e = 0: lane t/4, e = 1: lane t/4 + 8) into the thread's 8 packed column sums.
-__device__ __forceinline__ void col_terms(const float (&v)[32], int e, float2 sc, float lse, float2 (&cs)[8]) {
-    const float2 nl = make_float2(-lse, -lse);
+__device__ __forceinline__ void col_terms(const float (&v)[32], int e, float2 sc, float nlse, float2 (&cs)[8]) {
+    const float2 nl = make_float2(nlse, nlse);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const float2 x = __ffma2_rn(make_float2(v[4 * j + 2 * e], v[4 * j + 2 * e + 1]), sc, nl);
@@ -565,14 +567,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
             if (MODE == 2 && !a.redo[u]) continue;
             const int lg = u / a.units_per_lg, o = u % a.units_per_lg;
-            const float* lse_lg = a.lse2 + (int64_t)lg * a.rows_pad;
+            const float* nlse_lg = a.nlse2 + (int64_t)lg * a.rows_pad;
             // the thread's 16 sums (row pass: per query row, column pass: per block)
             float2 cs[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) cs[j] = make_float2(0.f, 0.f);
-            // column pass: lse2 of this lane's row in the next tile (loaded ahead)
-            float lse_n = INFINITY;
-            if (MODE == 1 && r_local < a.rows_pad) lse_n = __ldg(lse_lg + r_local);
+            // column pass: -lse2 of this lane's row in the next tile (loaded ahead; every
+            // tile's rows lie inside the padded row range)
+            float nl_n = 0.f;
+            if (MODE == 1) nl_n = __ldg(nlse_lg + r_local);
             // exact row pass: the warp's negated references of its 64 query rows, in
             // shared memory (set by the unit's first tile)
             float* const wref = t.nref + (MODE == 2 ? ew * kSliceCols : 0);
@@ -684,10 +687,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 } else {
-                    // column pass: rows past rows_pad read +inf and add nothing
-                    const float lse = lse_n;
-                    const int r1 = (i + 1) * BM + r_local;
-                    lse_n = (more && r1 < a.rows_pad) ? __ldg(lse_lg + r1) : INFINITY;
+                    // column pass: pad rows read -inf and add nothing
+                    const float nl = nl_n;
+                    if (more) nl_n = __ldg(nlse_lg + (i + 1) * BM + r_local);
                     // the warp's 32 lanes in two halves of 16; each thread gets 4 rows x 16
                     // columns, so the whole slice is read before the accumulator is released
                     float v0[32], v1[32];
@@ -698,12 +700,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     mbar_arrive_lane0(release, lane);
                     ready = more && mbar_done(&t.acc_full[1 - K], next_par);
-                    // lse2 of the thread's rows, from the lanes that loaded them
+                    // -lse2 of the thread's rows, from the lanes that loaded them
                     const int rl = lane >> 2;
-                    col_terms(v0, 0, sc, __shfl_sync(0xffffffffu, lse, rl), cs);
-                    col_terms(v0, 1, sc, __shfl_sync(0xffffffffu, lse, rl + 8), cs);
-                    col_terms(v1, 0, sc, __shfl_sync(0xffffffffu, lse, rl + 16), cs);
-                    col_terms(v1, 1, sc, __shfl_sync(0xffffffffu, lse, rl + 24), cs);
+                    col_terms(v0, 0, sc, __shfl_sync(0xffffffffu, nl, rl), cs);
+                    col_terms(v0, 1, sc, __shfl_sync(0xffffffffu, nl, rl + 8), cs);
+                    col_terms(v1, 0, sc, __shfl_sync(0xffffffffu, nl, rl + 16), cs);
+                    col_terms(v1, 1, sc, __shfl_sync(0xffffffffu, nl, rl + 24), cs);
                 }
             };
             using K0 = std::integral_constant<int, 0>;
@@ -748,12 +750,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                 rc[3 * kSliceCols]);
                     const int row = o * T::kFRows + etid;
                     if (row < a.rows_g) {
-                        a.lse2[(int64_t)lg * a.rows_pad + row] = m.y > 0.f ? m.x + __log2f(m.y) : -INFINITY;
+                        a.nlse2[(int64_t)lg * a.rows_pad + row] = m.y > 0.f ? -(m.x + __log2f(m.y)) : INFINITY;
                         // every row has a candidate, so its sum is at least 2^-(74 + 16) of the
                         // reference unless its largest logit lies more than 74 below the warp's
                         redo = MODE == 0 && !(m.y >= 0x1p-90f && m.y <= 0x1p126f);
                     } else if (row < a.rows_pad) {
-                        a.lse2[(int64_t)lg * a.rows_pad + row] = INFINITY;
+                        a.nlse2[(int64_t)lg * a.rows_pad + row] = -INFINITY;
                     }
                 }
             } else {
@@ -841,7 +843,7 @@ PFN_cuTensorMapEncodeTiled_v12000 kvsel_tmap_encoder() {
 
 size_t block_scores_workspace(int L, int Hq, int Hkv, int M, int n_blocks) {
     const size_t rows_g = (size_t)(Hq / Hkv) * M;
-    const size_t rows_pad = (rows_g + 3) & ~(size_t)3;
+    const size_t rows_pad = (rows_g + BM - 1) / BM * BM;
     const size_t units = (size_t)L * Hkv * ((rows_g + kAccCols - 1) / kAccCols);
     return align256((size_t)L * Hkv * rows_pad * sizeof(float)) + align256((size_t)L * Hkv * n_blocks * sizeof(float)) +
            align256(units * sizeof(int));
@@ -858,8 +860,8 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
     const int ncand = c1 - c0;
     const int LH = L * Hkv;
     char* w = static_cast<char*>(ws);
-    float* lse2 = reinterpret_cast<float*>(w);
-    const int rows_pad = (rows_g + 3) & ~3;
+    float* nlse2 = reinterpret_cast<float*>(w);
+    const int rows_pad = (rows_g + BM - 1) / BM * BM;  // whole column-pass tiles
     w += align256((size_t)LH * rows_pad * sizeof(float));
     float* mass_ws = reinterpret_cast<float*>(w);
     w += align256((size_t)LH * n_blocks * sizeof(float));
@@ -898,7 +900,7 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
         a.c1 = c1;
         a.Bcap = Bcap;
         a.n_blocks = n_blocks;
-        a.lse2 = lse2;
+        a.nlse2 = nlse2;
         a.mass = mass;
         a.err = ctx->dev_err;
         a.redo = redo;
