@@ -20,8 +20,8 @@
 //                the sums are added across the warp's lanes (butterfly) and
 //                merged across the four lane quarters with their references
 //                -> lse2[r] = log2 sum_{b in C} 2^(S[r,b] log2e/sqrt(d)), stored
-//                negated, the row range padded to whole column-pass tiles with -inf
-//                A row whose merged sum is below 2^-90 of its reference (its
+//                negated, the row range padded to whole column-pass tiles with
+//                -inf.  A row whose merged sum is below 2^-90 of its reference (its
 //                largest logit lies more than 74 below the warp's) may have lost
 //                terms to underflow; a sum that is not finite overflowed (a
 //                logit more than about 134 above the reference's).  Either marks
@@ -33,11 +33,12 @@
 //                overwrites the unit's lse2.
 //   column pass: a unit is (l,g, 256 candidate blocks); tiles of 128 query rows
 //                stream.  A thread holds 4 rows x 16 blocks; it adds
-//                2^(x - lse2[r]) into 16 per-block sums (-lse2 loaded one tile
-//                ahead, one lane per row, handed on by shuffles, and used as the
-//                fma's addend as it is; no bounds test, the padding reads -inf).  At the end of
-//                the unit the sums are added across lanes (butterfly) and across
-//                the four lane quarters -> mass[lg][b], complete per CTA
+//                2^(x - lse2[r]) into 16 per-block sums.  -lse2 is loaded one
+//                tile ahead, one lane per row, handed on by shuffles and used as
+//                the fma's addend as it is (no bounds test: the padding reads
+//                -inf).  At the end of the unit the sums are added across lanes
+//                (butterfly) and across the four lane quarters -> mass[lg][b],
+//                complete per CTA
 //   finalize:    R[b] = sum_lg mass[lg][b] / (L*Hq), in fixed (l,g) order.
 // Every pass completes each unit's results inside one CTA: no atomics, no
 // partial results in global memory.
