@@ -383,11 +383,11 @@ def ours(args, rank, world, local_rank):
 # DRAM bytes (read + write) per call from an ncu capture of the current kernel code, scaled to the
 # bench workload; an entry is removed whenever its kernel changes.
 PROFILED_TRAFFIC = {
-    # block_scores_tc, 4-layer capture of the three tensor-core launches (row pass 352.3 + 5.6 MB,
-    # exact pass 0.07 + 0 MB, column pass 353.8 + 3.5 MB), x16 for 64 layers:
+    # block_scores_tc, 4-layer capture of the three tensor-core launches (row pass 352.0 + 4.7 MB,
+    # exact pass 0.06 + 0 MB, column pass 353.8 + 6.9 MB), x16 for 64 layers:
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,... -k regex:block_scores_tc -c 3
     # on python bench.py --profile-kernel block_scores --profile-layers 4 --steps 3 --warmup 1
-    "block_scores": 16 * (352.302336 + 5.601280 + 0.074496 + 353.814016 + 3.526656) * 1e6,
+    "block_scores": 16 * (351.990016 + 4.710912 + 0.063488 + 353.807360 + 6.911232) * 1e6,
 }
 
 

@@ -34,7 +34,7 @@ def test_algorithmic_amounts():
 def test_launches_and_traffic():
     assert sum(bench.LAUNCHES.values()) == 13
     assert bench.LAUNCHES["block_scores"] == 4 and bench.LAUNCHES["rule_scores"] == 3
-    assert abs(bench.PROFILED_TRAFFIC["block_scores"] - 11.445e9) < 0.01e9
+    assert abs(bench.PROFILED_TRAFFIC["block_scores"] - 11.48e9) < 0.01e9
 
 
 def test_block_scores_ceiling():
