@@ -588,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the row pass's last tile, whose TMEM lanes past the candidate range are masked.
             auto tile = [&](auto kc, auto maskc, int i) {
                 constexpr int K = decltype(kc)::value;
-                constexpr bool MASK = decltype(maskc)::value;
+                [[maybe_unused]] constexpr bool MASK = decltype(maskc)::value;
                 // After a timed-out wait a thread waits no more: its warp still runs the
                 // remaining tiles' TMEM loads (always in range, and warp-collective) and
                 // math on whatever the accumulator holds, and the epilogue warps agree on
