@@ -152,6 +152,26 @@ def test_block_scores_row_far_below_its_warp(ctx):
     assert_scores_close(f64(R), Rref, what="R_b, rows far below their slice")
 
 
+def test_block_scores_every_unit_redone(ctx):
+    """A zero query row in every 64-row slice, among rows whose logits reach about 140
+    (log2): every row-pass unit of every (layer, kv head) is marked, so the exact pass redoes
+    all of them (several units per CTA, none skipped) and must still match the oracle."""
+    L, Hq, Hkv, M, nb = 2, 2, 1, 600, 700
+    gen = torch.Generator(device="cuda").manual_seed(79)
+    q = torch.randn((L, Hq, M, 128), generator=gen, device="cuda") * 30.0
+    ix = torch.randn((L, Hkv, nb, 128), generator=gen, device="cuda")
+    rows = q.view(L, Hkv, Hq // Hkv * M, 128)
+    rows[:, :, ::64] = 0.0          # one zero row per 64-row slice of every unit
+    q, ix = q.to(torch.bfloat16), ix.to(torch.bfloat16)
+    R = torch.empty(nb, device="cuda")
+    part = torch.empty((L * Hkv, nb), device="cuda")
+    ctx.block_scores(q, ix, nb, 2, 2, R, R_partial=part)
+    ctx.check_device()
+    Rref, pref = oracle.block_scores(bits(q), bits(ix), nb, 2, 2, return_partial=True)
+    assert_scores_close(f64(part), pref, what="R_b partial, every unit redone")
+    assert_scores_close(f64(R), Rref, what="R_b, every unit redone")
+
+
 @pytest.mark.parametrize("v", [2.6, 3.0])
 def test_block_scores_logit_jump_beyond_headroom(ctx, v):
     """A block in the second tile whose logits exceed the first tile's by about 110
