@@ -160,6 +160,8 @@ int kvsel_rule_scores_noalloc(kvsel_ctx* ctx, const void* k_pool, int k_dtype, c
  *   keep      [N] uint8 out (1 = kept) or NULL
  *   keep_idx  [|K*|] int32 out, kept positions ascending, or NULL
  *   n_keep_host  host out: |K*| = |F| + min(C*, |H|) (closed form, no sync)
+ * Uses no workspace for N <= 131072; above that the grid-wide selection may use
+ * 4 KB + 16 bytes per 4096 positions of it.
  */
 int kvsel_topk_retain(kvsel_ctx* ctx, const float* score, int N, int pi, int q_s, int q_e,
                       int C, uint8_t* keep, int32_t* keep_idx, int* n_keep_host, void* stream);
@@ -207,7 +209,9 @@ int kvsel_meank_build(kvsel_ctx* ctx, const void* k_src, int L, int Hkv, int T, 
  *              each (l, g), sum over its Hq/Hkv heads and M query tokens
  * The dot products run on the tensor cores (bf16 in, fp32 accumulate), the
  * softmax in fp32.  Requires D == 128, Hq % Hkv == 0, n_blocks <= Bcap,
- * 16-byte aligned q and index.  Uses workspace: 4*L*Hq*M + 4*L*Hkv*n_blocks bytes.
+ * 16-byte aligned q and index.  Uses workspace: 4*L*Hkv*R bytes for the query
+ * rows' log-sum-exps, R = Hq/Hkv*M rounded up to a multiple of 128, plus
+ * 4*L*Hkv*n_blocks for the masses and 4 bytes per 256 query rows of each (l, g).
  */
 int kvsel_block_scores(kvsel_ctx* ctx, const void* q, const void* index, int L, int Hq, int Hkv,
                        int M, int D, int n_blocks, int Bcap, int n_sink, int n_recent, float* R,
@@ -221,6 +225,7 @@ int kvsel_block_scores(kvsel_ctx* ctx, const void* q, const void* index, int L, 
  *   R         [n_blocks] fp32
  *   ids       [|W|] int32 out
  *   n_sel_host host out: |W| = |sink U recent| + min(k, |C|)
+ * Workspace as kvsel_topk_retain with N = n_blocks.
  */
 int kvsel_select_blocks(kvsel_ctx* ctx, const float* R, int n_blocks, int n_sink, int n_recent,
                         int k, int32_t* ids, int* n_sel_host, void* stream);
@@ -302,8 +307,9 @@ typedef struct {
 
 /*
  * kvsel_topk_retain for S sessions.  Sessions of N <= 131072 share one launch:
- * one CTA each when every one of them has N <= 16384, else one thread-block
- * cluster each; larger sessions are selected one launch each.  Results are
+ * one CTA each when every one of them has N <= 8192, else one thread-block
+ * cluster each; larger sessions are selected one call each, on the paths (and
+ * the workspace) of kvsel_topk_retain.  Results are
  * those of kvsel_topk_retain on each session.
  * n_keep_host: NULL or a host int array [S] receiving each session's |keep|.
  */

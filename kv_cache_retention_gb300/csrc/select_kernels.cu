@@ -9,7 +9,7 @@
 // The keep set is therefore a pure function of the scores: ties resolve to the
 // lower index, NaN ranks lowest, -0 == +0.
 //
-// N <= KVSEL_TOPK_CTA_MAX (16384 at most): one CTA, keys in registers.
+// N <= KVSEL_TOPK_CTA_MAX (8192; 16384 at most): one CTA, keys in registers.
 // N <= 131072: the same code on one cluster of 8 CTAs, histograms merged through
 // distributed shared memory; N <= 262144: a cluster of 16 (where the GPU can
 // place one).  Larger N: the grid-wide variant below (several launches, a small
@@ -554,8 +554,8 @@ size_t topk_batch_workspace(int S, int max_N) {
 }
 
 // Sessions that fit one cluster share one launch (a cluster each, or a CTA each when
-// every such session fits one CTA); larger ones take the single-CTA re-reading
-// kernel one by one.  need / n_cand per session as kvsel_topk_retain.
+// every such session fits one CTA); larger ones take launch_topk's paths (16-CTA
+// cluster or grid-wide) one by one.  need / n_cand per session as kvsel_topk_retain.
 cudaError_t launch_topk_batch(const kvsel_topk_session* sess, const int* need, const int* n_cand, int S, void* ws,
                               cudaStream_t s) {
     std::vector<TopkJob> jobs;
