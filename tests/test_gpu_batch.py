@@ -179,11 +179,15 @@ def test_batched_token_step(ctx):
         assert np.array_equal(keeps[i].cpu().numpy(), ref_keep)
 
 
-def test_topk_retain_batch_all_small_sessions(ctx):
-    """Every session fits one CTA (N <= 16384): the batch runs one CTA per session."""
+@pytest.mark.parametrize("Ns,Cs", [
+    # every session fits one CTA (N <= 8192): the batch runs one CTA per session
+    ([8192, 1, 2048, 8191, 300, 5000, 8192], [1000, 1, 2048, 20000, 0, 2500, 8191]),
+    # sessions up to 16384: one 8-CTA cluster per session
+    ([16384, 1, 2048, 16383, 300, 9000, 16384], [1000, 1, 2048, 20000, 0, 4500, 16383]),
+])
+def test_topk_retain_batch_all_small_sessions(ctx, Ns, Cs):
+    """Sessions that fit one launch: one CTA each, or one cluster each."""
     rng = np.random.default_rng(5)
-    Ns = [16384, 1, 2048, 16383, 300, 9000, 16384]
-    Cs = [1000, 1, 2048, 20000, 0, 4500, 16383]
     rules, forced = [], []
     for N in Ns:
         r = np.round(rng.standard_normal(N) * 8) / 8  # many ties
