@@ -795,19 +795,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
 }
 
-// R[b] = sum_lg mass[lg][b] / (L*Hq) on C; zero outside C (also in mass).
-__global__ void bs_finalize(const float* __restrict__ mass_in, float* mass, float* R, int LH, int n_blocks, int c0,
-                            int c1, float inv) {
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= n_blocks) return;
-    if (b < c0 || b >= c1) {
-        R[b] = 0.f;
-        for (int lg = 0; lg < LH; ++lg) mass[(int64_t)lg * n_blocks + b] = 0.f;
-        return;
-    }
+// R[b] = sum_lg mass[lg][b] / (L*Hq) on C; zero outside C (also in mass).  A CTA
+// takes 64 blocks; its four thread groups add a quarter of the (l,g) rows each, in
+// ascending order, and the four partial sums are added in fixed order.
+constexpr int kFinBlocks = 64, kFinParts = 4;
+static_assert(kFinParts == 4, "the partial sums are added as ((p0 + p1) + p2) + p3");
+__global__ void __launch_bounds__(kFinBlocks * kFinParts) bs_finalize(const float* __restrict__ mass_in, float* mass,
+                                                                        float* R, int LH, int n_blocks, int c0, int c1,
+                                                                        float inv) {
+    __shared__ float part_sum[kFinParts][kFinBlocks];
+    const int bl = threadIdx.x % kFinBlocks, part = threadIdx.x / kFinBlocks;
+    const int b = blockIdx.x * kFinBlocks + bl;
+    const bool in_range = b < n_blocks;
+    const bool cand = in_range && b >= c0 && b < c1;
+    const int lg0 = (int)((int64_t)LH * part / kFinParts), lg1 = (int)((int64_t)LH * (part + 1) / kFinParts);
     float acc = 0.f;
-    for (int lg = 0; lg < LH; ++lg) acc += mass_in[(int64_t)lg * n_blocks + b];
-    R[b] = acc * inv;
+    if (cand) {
+        for (int lg = lg0; lg < lg1; ++lg) acc += mass_in[(int64_t)lg * n_blocks + b];
+    } else if (in_range) {
+        for (int lg = lg0; lg < lg1; ++lg) mass[(int64_t)lg * n_blocks + b] = 0.f;
+    }
+    part_sum[part][bl] = acc;
+    __syncthreads();
+    if (part == 0 && in_range)
+        R[b] = cand ? (((part_sum[0][bl] + part_sum[1][bl]) + part_sum[2][bl]) + part_sum[3][bl]) * inv : 0.f;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -926,7 +937,7 @@ cudaError_t launch_block_scores(kvsel_ctx* ctx, const void* q, const void* index
         grid = a.n_units < ctx->num_sms ? a.n_units : ctx->num_sms;
         block_scores_tc<1><<<grid, kThreads, smem_bytes<1>(), s>>>(i256, q128, a);
     }
-    bs_finalize<<<(n_blocks + 255) / 256, 256, 0, s>>>(mass, mass, R, LH, n_blocks, c0, c1,
-                                                       1.0f / ((float)L * (float)Hq));
+    bs_finalize<<<(n_blocks + kFinBlocks - 1) / kFinBlocks, kFinBlocks * kFinParts, 0, s>>>(
+        mass, mass, R, LH, n_blocks, c0, c1, 1.0f / ((float)L * (float)Hq));
     return cudaGetLastError();
 }
