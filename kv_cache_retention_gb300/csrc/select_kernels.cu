@@ -534,7 +534,9 @@ cudaError_t launch_topk_grid(const float* score, int N, int pi, int q_s, int q_e
 
 }  // namespace
 
-size_t topk_workspace(int N) { return N > kCluster16Cap || N > kClusterCap ? grid_workspace(N) : 0; }
+// Above one 8-CTA cluster the grid-wide path may run (it does wherever the 16-CTA
+// cluster cannot be placed), so its workspace is reserved for every such N.
+size_t topk_workspace(int N) { return N > kClusterCap ? grid_workspace(N) : 0; }
 
 cudaError_t launch_topk(const float* score, int N, int pi, int q_s, int q_e, int need, int n_cand, uint8_t* keep,
                         int32_t* keep_idx, void* ws, cudaStream_t s) {
