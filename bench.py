@@ -1175,6 +1175,84 @@ def run_step_only(ctx, s, name, ev):
     ev.setdefault(name, []).append((a, b))
 
 
+def e2e_timeline(args):
+    """The end-to-end loop of the bench line with CUDA events on both streams: when each
+    step's input copies start and land (copy stream) and when its calls run (compute
+    stream), in ms from the loop's start, plus the copies alone afterwards.  Shows whether
+    the copies of step t+1 overlap step t and which side waits."""
+    import torch
+
+    import kv_cache_retention_gb300 as kv
+    import synth
+
+    torch.cuda.set_device(0)
+    tw, bw = synth.TOKEN[TOKEN_WL], synth.BLOCK[BLOCK_WL]
+    ctx = kv.Context(0)
+    s = setup_session(kv, synth, ctx, tw, bw, torch)
+    for _ in range(args.warmup):
+        run_step(ctx, s)
+    torch.cuda.synchronize()
+    in_keys = ("q_last", "raw_new", "q", "staging")
+    h_in = {k: s[k].detach().cpu().pin_memory() for k in in_keys}
+    h_out = {k: torch.empty_like(s[k], device="cpu").pin_memory() for k in ("rule", "slot_out", "keep_idx", "R", "ids")}
+    sets = [s, dict(s)]
+    for k in in_keys:
+        sets[1][k] = torch.empty_like(s[k])
+    copy_stream, comp = torch.cuda.Stream(), torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev_copied = [{k: ev() for k in in_keys} for _ in range(2)]
+    ev_done = [ev(), ev()]
+    marks = []
+
+    def issue_copy(i):
+        with torch.cuda.stream(copy_stream):
+            if i >= 2:
+                copy_stream.wait_event(ev_done[i % 2])
+            a = ev()
+            a.record(copy_stream)
+            marks.append((f"copy {i} start", a))
+            for k in in_keys:
+                sets[i % 2][k].copy_(h_in[k], non_blocking=True)
+                ev_copied[i % 2][k].record(copy_stream)  # reused two steps later: the wait's event
+                m = ev()  # the mark's own event
+                m.record(copy_stream)
+                marks.append((f"copy {i} {k} landed", m))
+
+    start = ev()
+    start.record()
+    copy_stream.wait_event(start)
+    issue_copy(0)
+    n = max(2, args.steps)
+    for i in range(n):
+        if i + 1 < n:
+            issue_copy(i + 1)
+        calls = {}
+        run_step(ctx, sets[i % 2], calls, ready=ev_copied[i % 2])
+        for name, v in calls.items():
+            marks.append((f"step {i} {name} start", v[0][0]))
+            marks.append((f"step {i} {name} end", v[0][1]))
+        ev_done[i % 2].record(comp)
+        for k, t in h_out.items():
+            t.copy_(sets[i % 2][k], non_blocking=True)
+    end = ev()
+    end.record()
+    torch.cuda.synchronize()
+    rows = []
+    for name, e in marks:
+        rows.append((round(start.elapsed_time(e), 2), name))
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    c0, c1 = ev(), ev()
+    with torch.cuda.stream(copy_stream):
+        c0.record(copy_stream)
+        for k in in_keys:
+            sets[0][k].copy_(h_in[k], non_blocking=True)
+        c1.record(copy_stream)
+    torch.cuda.synchronize()
+    print(json.dumps({"e2e_timeline": "bench step, inputs from pinned host memory", "steps": n,
+                      "ms_per_step": start.elapsed_time(end) / n, "h2d_bytes_per_step": h2d,
+                      "copies_alone_ms": c0.elapsed_time(c1), "events": sorted(rows)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1190,7 +1268,12 @@ def main():
     ap.add_argument("--block-sweep", action="store_true", help="Mean-K block size sweep (16 / 32 / 64 tokens)")
     ap.add_argument("--batch-sessions", action="store_true", help="36-session batched IntentKV step vs one by one")
     ap.add_argument("--fp8-index", action="store_true", help="FP8 (E4M3) index storage: quantise / expand cost, R_b change")
+    ap.add_argument("--e2e-timeline", action="store_true",
+                    help="the end-to-end loop with events on the copy and compute streams (overlap check)")
     args = ap.parse_args()
+    if args.e2e_timeline:
+        e2e_timeline(args)
+        return
     if args.batch_sessions:
         batch_sessions(args)
         return
