@@ -713,8 +713,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             using K1 = std::integral_constant<int, 1>;
             using M0 = std::integral_constant<bool, false>;
             using M1 = std::integral_constant<bool, true>;
-            for (int i = 0; i < a.n_it; ++i) {
-                // only the row pass's last tile can run past the candidate range
+            // Tiles in pairs (accumulator 0 then 1) after at most one tile that aligns the
+            // ring; the row pass's ragged last tile (the only one past the candidate range)
+            // and an odd remainder go one at a time.
+            const int n_plain = kRowPass<MODE> ? a.n_it - 1 : a.n_it;
+            int i = 0;
+            if ((acc_it & 1u) && i < n_plain) {
+                tile(K1{}, M0{}, i);
+                ++acc_it;
+                ++i;
+            }
+            for (; i + 2 <= n_plain; i += 2) {
+                tile(K0{}, M0{}, i);
+                ++acc_it;
+                tile(K1{}, M0{}, i + 1);
+                ++acc_it;
+            }
+            for (; i < a.n_it; ++i) {
                 const bool mask = kRowPass<MODE> && i + 1 == a.n_it;
                 if (acc_it & 1u) {
                     if (mask) tile(K1{}, M1{}, i); else tile(K1{}, M0{}, i);
