@@ -586,21 +586,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t taddr_q = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(slice * kSliceCols);
             // One tile, accumulator K = the tile's position in the accumulator ring; MASK:
             // the row pass's last tile, whose TMEM lanes past the candidate range are masked.
-            auto tile = [&](auto kc, auto maskc, int i) {
+            auto tile = [&](auto kc, auto maskc, auto posc, int i) {
                 constexpr int K = decltype(kc)::value;
                 [[maybe_unused]] constexpr bool MASK = decltype(maskc)::value;
+                // POS: acc_it % 4 when the caller knows it (barrier indices and parities are
+                // then constants), else -1
+                constexpr int POS = decltype(posc)::value;
                 // After a timed-out wait a thread waits no more: its warp still runs the
                 // remaining tiles' TMEM loads (always in range, and warp-collective) and
                 // math on whatever the accumulator holds, and the epilogue warps agree on
                 // giving up at the end of the unit.  No per-tile vote or branch: in the
                 // column pass that alone cost a tenth of the tensor pipe's time.
-                if (ok && !ready) ok = wait_phase(&t.acc_full[K], (acc_it >> 1) & 1u, abort_flag, a.err, a.wait_ns);
+                const uint32_t par = POS >= 0 ? (uint32_t)((POS >> 1) & 1) : (acc_it >> 1) & 1u;
+                if (ok && !ready) ok = wait_phase(&t.acc_full[K], par, abort_flag, a.err, a.wait_ns);
                 tc_fence_after();
                 const uint32_t taddr = taddr_q + (uint32_t)(K * kAccCols);
                 // releases accumulator K on the stage barrier of the tile kNAcc ahead
-                uint64_t* release = &t.go[(acc_it + kNAcc) % T::kNS];
+                uint64_t* release = POS >= 0 ? &t.go[(POS + kNAcc) % T::kNS] : &t.go[(acc_it + kNAcc) % T::kNS];
                 const bool more = i + 1 < a.n_it;
-                const uint32_t next_par = ((acc_it + 1) >> 1) & 1u;
+                const uint32_t next_par = POS >= 0 ? (uint32_t)(((POS + 1) >> 1) & 1) : ((acc_it + 1) >> 1) & 1u;
                 if constexpr (kRowPass<MODE>) {
                     // row passes: TMEM lanes are candidate blocks, columns query rows; a
                     // thread holds 4 blocks x 16 rows and sums each row
@@ -713,31 +717,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             using K1 = std::integral_constant<int, 1>;
             using M0 = std::integral_constant<bool, false>;
             using M1 = std::integral_constant<bool, true>;
-            // Tiles in pairs (accumulator 0 then 1) after at most one tile that aligns the
-            // ring; the row pass's ragged last tile (the only one past the candidate range)
-            // and an odd remainder go one at a time.
+            // Tiles in fours (accumulators 0, 1, 0, 1 and the four stages' barriers, all
+            // known at compile time) after at most three tiles that align the ring; the
+            // row pass's ragged last tile (the only one past the candidate range) and the
+            // remainder go one at a time.
+            static_assert(T::kNS == 4 && kNAcc == 2, "four tiles cycle through the stages once");
+            using PR = std::integral_constant<int, -1>;
+            using P0 = std::integral_constant<int, 0>;
+            using P1 = std::integral_constant<int, 1>;
+            using P2 = std::integral_constant<int, 2>;
+            using P3 = std::integral_constant<int, 3>;
             const int n_plain = kRowPass<MODE> ? a.n_it - 1 : a.n_it;
             int i = 0;
-            if ((acc_it & 1u) && i < n_plain) {
-                tile(K1{}, M0{}, i);
-                ++acc_it;
-                ++i;
-            }
-            for (; i + 2 <= n_plain; i += 2) {
-                tile(K0{}, M0{}, i);
-                ++acc_it;
-                tile(K1{}, M0{}, i + 1);
-                ++acc_it;
-            }
-            for (; i < a.n_it; ++i) {
-                const bool mask = kRowPass<MODE> && i + 1 == a.n_it;
+            auto one = [&](int ii) {
+                const bool mask = kRowPass<MODE> && ii + 1 == a.n_it;
                 if (acc_it & 1u) {
-                    if (mask) tile(K1{}, M1{}, i); else tile(K1{}, M0{}, i);
+                    if (mask) tile(K1{}, M1{}, PR{}, ii); else tile(K1{}, M0{}, PR{}, ii);
                 } else {
-                    if (mask) tile(K0{}, M1{}, i); else tile(K0{}, M0{}, i);
+                    if (mask) tile(K0{}, M1{}, PR{}, ii); else tile(K0{}, M0{}, PR{}, ii);
                 }
                 ++acc_it;
+            };
+            for (; (acc_it & 3u) && i < n_plain; ++i) one(i);
+            for (; i + 4 <= n_plain; i += 4) {
+                tile(K0{}, M0{}, P0{}, i);
+                ++acc_it;
+                tile(K1{}, M0{}, P1{}, i + 1);
+                ++acc_it;
+                tile(K0{}, M0{}, P2{}, i + 2);
+                ++acc_it;
+                tile(K1{}, M0{}, P3{}, i + 3);
+                ++acc_it;
             }
+            for (; i < a.n_it; ++i) one(i);
             if (!(ok = epi_bar_and(ok))) break;
             bool redo = false;  // row pass: a row of the unit needs the exact pass
             if constexpr (kRowPass<MODE>) {
